@@ -1,0 +1,153 @@
+/*
+ * pagedkv.h — C ABI of the GB300 paged decode-attention library (libpagedkv.so).
+ *
+ * The library implements the decode-time hot path of a blocked ("paged") KV
+ * cache as described by:
+ *   - "AI大模型推理速度翻倍，Colossal-Inference开源发布", sections
+ *     分块式KV缓存 (BlockedKeyValueCache), KV缓存量化 (KVCache Quant),
+ *     投机采样 (Speculative decoding) and 分页注意力算法 (PagedAttention);
+ *   - "AI 大模型推理优化技术详解", sections 2.1.2 Paged Attention (block size 16,
+ *     logical-to-physical block table), 2.2.1 Flash Attention (softmax reduced
+ *     without the whole row) and 2.2.2 GQA (query-head groups sharing one KV head);
+ *   - "TACO-LLM 如何实现降本增效?", section 3 (TurboAttention: paged + flash
+ *     attention for long generation) — the split-KV path serves that case.
+ *
+ * Conventions for every call
+ *   - All pointers are DEVICE pointers unless stated otherwise. The caller owns
+ *     every buffer; the library allocates no device memory and keeps no state
+ *     besides a per-device cache of device properties.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). Calls are
+ *     asynchronous: they enqueue kernels and return.
+ *   - Return value: PKV_OK (0) or a negative pkv_status. Arguments are checked on
+ *     the host before anything is launched; on error nothing is launched.
+ *     Nothing throws across this boundary.
+ *   - Problems only the device can see (an out-of-range block id or slot, a
+ *     context length outside [q_per_seq, max_blocks_per_seq*16]) are reported by
+ *     OR-ing PKV_DEV_* bits into `*device_status` when that pointer is not NULL.
+ *     The library never clears it; the caller zeroes it when it wants a fresh
+ *     reading. Such inputs never fault: a bad block reads as zeros, a bad slot is
+ *     skipped.
+ *
+ * Cache layout (our own choice; the pages' [blocks, heads, head/x, block, x] key
+ * layout is prior art, not used): K and V caches are separate arrays, each
+ *     [num_blocks][num_kv_heads][block_size = 16][head_size]
+ * row-major, elements fp16, bf16 or E5M2 (one byte). One (block, head) tile is
+ * 16*head_size contiguous elements (4 KiB for fp16 at head_size 128), which the
+ * decode kernel moves with one tensor-memory-accelerator copy. Token p of a
+ * sequence lives in physical block block_tables[s][p / 16] at offset p % 16; its
+ * slot number is block * 16 + offset.
+ */
+#ifndef PAGEDKV_H_
+#define PAGEDKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types. The pages' FP8 cache is E5M2 (KVCache Quant section). */
+typedef enum {
+  PKV_FP16 = 0,
+  PKV_BF16 = 1,
+  PKV_FP8_E5M2 = 2
+} pkv_dtype;
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARGUMENT = -1,   /* null pointer, non-positive size, misaligned pointer */
+  PKV_ERR_UNSUPPORTED = -2,        /* shape or dtype combination this build does not handle */
+  PKV_ERR_WORKSPACE_TOO_SMALL = -3,
+  PKV_ERR_CUDA = -4,               /* a CUDA runtime call failed (launch, attribute, ...) */
+  PKV_ERR_NO_DEVICE = -5
+} pkv_status;
+
+/* Device-side status bits OR-ed into *device_status. */
+#define PKV_DEV_BAD_SLOT   0x1  /* kv_cache_write: slot outside [-1, num_blocks*16) */
+#define PKV_DEV_BAD_BLOCK  0x2  /* decode: block id outside [0, num_blocks); read as zeros */
+#define PKV_DEV_BAD_CTX    0x4  /* decode: context_len < q_per_seq or > max_blocks_per_seq*16 */
+#define PKV_DEV_TIMEOUT    0x8  /* decode: a pipeline wait gave up (never expected) */
+
+/* Description of one K/V cache pair. block_size must be 16 (the pages' default,
+ * 2.1.2 Paged Attention); head_size 64 or 128. */
+typedef struct {
+  int32_t num_blocks;
+  int32_t block_size;
+  int32_t num_kv_heads;
+  int32_t head_size;
+} pkv_cache_desc;
+
+/*
+ * pkv_kv_cache_write — scatter new tokens into the cache ("kernel1" of the
+ * KVCache Quant section: the writer casts fp16 to FP8 when the cache is E5M2).
+ *
+ *   key, value    [num_tokens][num_kv_heads][head_size], contiguous, src_dtype
+ *                 (PKV_FP16 or PKV_BF16). 16-byte aligned.
+ *   slot_mapping  [num_tokens] int32: physical slot (block*16 + offset) of each
+ *                 token; -1 = skip the token. Other out-of-range values are
+ *                 skipped and flagged PKV_DEV_BAD_SLOT.
+ *   k_cache, v_cache  caches in the layout above, element type kv_dtype, 16-byte aligned.
+ *   Allowed (src_dtype, kv_dtype): (FP16, FP16), (BF16, BF16), (FP16, FP8_E5M2).
+ *   FP8 cast: round to nearest even; |x| > 57344 and +-inf saturate to +-57344;
+ *   NaN -> 0x7E | sign. fp16/bf16 caches are plain copies.
+ *   Two tokens mapped to the same slot race; the result is then unspecified.
+ *   num_tokens == 0 is a no-op returning PKV_OK.
+ */
+int pkv_kv_cache_write(const void* key, const void* value, pkv_dtype src_dtype,
+                       int32_t num_tokens, const int32_t* slot_mapping,
+                       void* k_cache, void* v_cache, pkv_dtype kv_dtype,
+                       const pkv_cache_desc* cache, int32_t* device_status, void* stream);
+
+/*
+ * pkv_decode_workspace_bytes — size of the scratch buffer paged attention needs
+ * on the CURRENT device for this problem shape (split-KV partial results and a
+ * per-(sequence, KV head) descriptor). It depends only on the arguments and the
+ * device's multiprocessor count; any buffer at least this large works, and it
+ * needs no initialisation. Returns 0 on invalid arguments.
+ */
+size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t q_per_seq,
+                                  const pkv_cache_desc* cache);
+
+/*
+ * pkv_paged_attention_decode — decode attention over the blocked cache
+ * ("kernel2" of the KVCache Quant section, the PagedAttention section's decode
+ * kernel, with the GQA grouping of 2.2.2 and the multi-token verify of the
+ * speculative-decoding section).
+ *
+ *   out, q        [num_seqs * q_per_seq][num_q_heads][head_size], contiguous.
+ *                 Row s*q_per_seq + j is query token j of sequence s. Element
+ *                 type: bf16 when kv_dtype is PKV_BF16, else fp16. 16-byte aligned.
+ *   block_tables  [num_seqs][max_blocks_per_seq] int32 physical block ids.
+ *   context_lens  [num_seqs] int32: cached tokens of each sequence INCLUDING its
+ *                 q_per_seq query tokens, which are its last q_per_seq positions.
+ *   scale         softmax scale (typically 1/sqrt(head_size)).
+ *   workspace     device scratch of at least pkv_decode_workspace_bytes(...)
+ *                 bytes, 16-byte aligned; contents need no initialisation.
+ *
+ *   For each sequence s, query head hq (KV head h = hq / (num_q_heads/num_kv_heads))
+ *   and query token j, with L = context_lens[s] - q_per_seq + j + 1:
+ *       out[s,j,hq,:] = sum_{p<L} softmax_p(scale * q[s,j,hq,:] . K[s,p,h,:]) * V[s,p,h,:]
+ *   accumulated in fp32 on tensor cores (P in the query dtype), rounded to the
+ *   output dtype once. Requires num_q_heads % num_kv_heads == 0 and
+ *   (num_q_heads/num_kv_heads) * q_per_seq <= 64.
+ */
+int pkv_paged_attention_decode(void* out, const void* q, int32_t num_seqs,
+                               int32_t num_q_heads, int32_t q_per_seq,
+                               const void* k_cache, const void* v_cache, pkv_dtype kv_dtype,
+                               const pkv_cache_desc* cache, const int32_t* block_tables,
+                               int32_t max_blocks_per_seq, const int32_t* context_lens,
+                               float scale, void* workspace, size_t workspace_bytes,
+                               int32_t* device_status, void* stream);
+
+/* Static description of a status code. Never NULL. */
+const char* pkv_error_string(int code);
+
+/* Library version (major*10000 + minor*100 + patch). */
+int pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H_ */

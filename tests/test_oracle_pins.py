@@ -1,0 +1,381 @@
+"""Pins for the CPU oracle: checks against what the formats, the mathematics and
+library routines fix, never against the oracle itself.
+
+Pages followed: "AI大模型推理速度翻倍，Colossal-Inference开源发布" (分块式KV缓存,
+KV缓存量化, 分页注意力算法, 投机采样) and "AI 大模型推理优化技术详解" (2.1.2 Paged
+Attention, 2.2.2 GQA).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_252_gb300 import workloads as wl
+from _helpers import (bits16, oracle_caches, oracle_attention, sdpa_reference, KV_CODE,
+                      cache_shape)
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+ALL16 = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+
+
+# ---------------------------------------------------------------------------------
+# number formats
+# ---------------------------------------------------------------------------------
+
+def _e5m2_code_values():
+    """The 256 E5M2 codes decoded from the format definition (numpy, independent)."""
+    b = np.arange(256)
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    e = (b >> 2) & 0x1F
+    m = b & 0x3
+    mag = np.where(e == 0, m * 2.0 ** -16, (1 + m / 4.0) * 2.0 ** (e.astype(np.float64) - 15))
+    mag = np.where(e == 31, np.where(m == 0, np.inf, np.nan), mag)
+    return sign * mag
+
+
+def _nearest_e5m2(x: np.ndarray) -> np.ndarray:
+    """Nearest finite E5M2 code by exhaustive search; ties to the even code; beyond the
+    largest finite magnitude (and +-inf) saturate; NaN -> 0x7E with the sign bit."""
+    vals = _e5m2_code_values()
+    finite = np.isfinite(vals)
+    codes = np.arange(256)[finite]
+    cv = vals[finite]
+    out = np.zeros(x.shape, dtype=np.uint8)
+    sign = np.signbit(x)
+    nan = np.isnan(x)
+    xs = np.where(nan, 0.0, np.clip(x, -57344.0, 57344.0))  # saturate (covers inf)
+    dist = np.abs(xs[:, None] - cv[None, :])
+    best = dist.min(axis=1, keepdims=True)
+    cand = dist == best
+    # among tied candidates prefer an even mantissa code; for +-0 prefer the input's sign
+    score = cand * (2 + (codes[None, :] % 2 == 0) * 2 + (np.signbit(cv)[None, :] == sign[:, None]))
+    out = codes[np.argmax(score, axis=1)].astype(np.uint8)
+    out = np.where(nan, np.where(sign, 0xFE, 0x7E), out).astype(np.uint8)
+    return out
+
+
+def test_e5m2_exhaustive_vs_nearest_code_search(orc):
+    x = ALL16.view(np.float16).astype(np.float64)
+    got = orc.e5m2_from_fp16(ALL16)
+    want = _nearest_e5m2(x)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, [(hex(int(ALL16[i])), hex(int(got[i])), hex(int(want[i]))) for i in bad[:8]]
+
+
+def test_e5m2_matches_torch_cast_in_range(orc):
+    """torch's float8_e5m2 cast (round-to-nearest-even, no saturation) agrees on every
+    finite fp16 value below the overflow threshold 61440."""
+    x16 = torch.from_numpy(ALL16.view(np.int16)).view(torch.float16)
+    finite = torch.isfinite(x16) & (x16.abs() < 61440)
+    t = x16[finite].to(torch.float8_e5m2).view(torch.uint8).numpy()
+    got = orc.e5m2_from_fp16(ALL16[finite.numpy()])
+    assert np.array_equal(got, t)
+
+
+def test_e5m2_roundtrip_and_bit_identity(orc):
+    vals = _e5m2_code_values()
+    for b in range(256):
+        h = orc.fp16_from_e5m2(b)
+        if np.isnan(vals[b]):
+            continue
+        # the fp16 pattern of an E5M2 value is the byte followed by 8 zero bits
+        assert h == (b << 8), (b, h)
+        assert orc.e5m2_to_f64(b) == vals[b]
+        back = int(orc.e5m2_from_fp16(np.array([h], np.uint16))[0])
+        if np.isinf(vals[b]):
+            assert back == (b & 0x80) | 0x7B   # infinities saturate (satfinite reading)
+        else:
+            assert back == b
+
+
+def test_e5m2_golden_cases(orc):
+    """Hand-worked cases (tests/golden/e5m2_cases.json): ties, subnormals, saturation, NaN."""
+    with open(os.path.join(GOLDEN, "e5m2_cases.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        h = int(c["fp16"], 16)
+        got = int(orc.e5m2_from_fp16(np.array([h], np.uint16))[0])
+        assert got == int(c["e5m2"], 16), (c, hex(got))
+
+
+def test_fp16_bf16_decode_exhaustive(orc):
+    got16 = orc.decode_to_f64(ALL16, orc.FP16)
+    ref16 = ALL16.view(np.float16).astype(np.float64)
+    assert np.array_equal(np.isnan(got16), np.isnan(ref16))
+    ok = ~np.isnan(ref16)
+    assert np.array_equal(got16[ok], ref16[ok])
+    assert np.array_equal(np.signbit(got16[ok]), np.signbit(ref16[ok]))
+    gotb = orc.decode_to_f64(ALL16, orc.BF16)
+    refb = torch.from_numpy(ALL16.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(gotb), np.isnan(refb))
+    ok = ~np.isnan(refb)
+    assert np.array_equal(gotb[ok], refb[ok])
+
+
+def test_round_from_f64_fp16_matches_numpy(orc):
+    rng = np.random.default_rng(0)
+    x = np.concatenate([
+        rng.standard_normal(20000) * 10.0 ** rng.integers(-8, 5, 20000),
+        # exact halfway points between adjacent fp16 values (ties)
+        (ALL16[:0x7BFF].view(np.float16).astype(np.float64)
+         + ALL16[1:0x7C00].view(np.float16).astype(np.float64)) / 2.0,
+        [65504.0, 65519.99, 65520.0, 1e6, -1e6, 5.96e-8, 2.98e-8, 0.0, -0.0],
+    ])
+    got = orc.round_from_f64(x, orc.FP16)
+    want = x.astype(np.float16).view(np.uint16)
+    assert np.array_equal(got, want)
+
+
+def test_round_from_f64_bf16_matches_torch(orc):
+    rng = np.random.default_rng(1)
+    # fp32-representable inputs, so torch's fp32 -> bf16 rounding is a single rounding
+    x = (rng.standard_normal(50000) * 10.0 ** rng.integers(-30, 30, 50000)).astype(np.float32)
+    ties = (np.arange(1, 40000, dtype=np.uint32) << 15).view(np.float32)  # bit 15 set: halfway cases
+    x = np.concatenate([x, ties, -ties]).astype(np.float64)
+    got = orc.round_from_f64(x, orc.BF16)
+    want = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, want)
+
+
+# ---------------------------------------------------------------------------------
+# cache write
+# ---------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("kv", ["fp16", "bf16", "e5m2"])
+def test_cache_write_roundtrip_through_block_table(orc, kv):
+    """Writing every token through the slot mapping and reading position p back through
+    block_tables[s][p // 16] returns the token (cast for E5M2), for every sequence."""
+    w = wl.custom(num_seqs=3, num_q_heads=4, num_kv_heads=2, head_size=64, q_per_seq=1,
+                  kv_dtype=kv, context_lens=[5, 16, 40], seed=11)
+    vals = wl.token_values(w)
+    kc, vc = oracle_caches(orc, w, vals)
+    starts = w.seq_starts()
+    kb = bits16(vals["k_all"])
+    for s in range(w.num_seqs):
+        for p in range(int(w.context_lens[s])):
+            blk = w.block_tables[s, p // 16]
+            row = kc[blk, :, p % 16, :]
+            src = kb[starts[s] + p]
+            if kv == "e5m2":
+                src = orc.e5m2_from_fp16(src)
+            assert np.array_equal(row, src)
+
+
+def test_cache_write_skips_minus_one_and_flags_out_of_range(orc):
+    kc = np.zeros((2, 1, 16, 8), np.uint16)
+    vc = np.zeros_like(kc)
+    key = np.full((3, 1, 8), 0x3C00, np.uint16)
+    rc = orc.kv_cache_write(key, key, orc.FP16, np.array([-1, 3, 31], np.int32), kc, vc, orc.FP16)
+    assert rc == 0
+    assert kc.reshape(-1, 8)[3].tolist() == [0x3C00] * 8
+    assert kc.reshape(-1, 8)[31].tolist() == [0x3C00] * 8
+    assert int((kc != 0).sum()) == 16
+    rc = orc.kv_cache_write(key, key, orc.FP16, np.array([0, 32, 1], np.int32), kc, vc, orc.FP16)
+    assert rc == -1
+
+
+def test_cache_write_golden_fixture(orc):
+    """Two tokens, one KV head, head size 8, written into a 2-block pool as E5M2
+    (tests/golden/cache_write_e5m2.json, worked by hand from the format)."""
+    with open(os.path.join(GOLDEN, "cache_write_e5m2.json")) as f:
+        g = json.load(f)
+    key = np.array([[int(x, 16) for x in row] for row in g["key_fp16"]], np.uint16)[:, None, :]
+    kc = np.zeros((2, 1, 16, 8), np.uint8)
+    vc = np.zeros_like(kc)
+    rc = orc.kv_cache_write(key, key, orc.FP16, np.array(g["slot_mapping"], np.int32), kc, vc,
+                            orc.E5M2)
+    assert rc == 0
+    for slot, row in zip(g["slot_mapping"], g["expect_e5m2"]):
+        assert kc.reshape(-1, 8)[slot].tolist() == [int(x, 16) for x in row]
+
+
+# ---------------------------------------------------------------------------------
+# attention
+# ---------------------------------------------------------------------------------
+
+CASES = [
+    # (kv, S, Hq, Hkv, D, n, lens)
+    ("fp16", 4, 4, 2, 64, 1, [1, 17, 33, 64]),
+    ("bf16", 3, 8, 2, 64, 1, [15, 16, 47]),
+    ("e5m2", 3, 8, 8, 128, 1, [2, 31, 70]),
+    ("fp16", 2, 8, 1, 64, 1, [20, 50]),
+    ("e5m2", 3, 8, 2, 64, 4, [4, 19, 40]),
+    ("fp16", 2, 4, 4, 64, 3, [3, 33]),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"{c[0]}-G{c[2] // c[3]}-n{c[5]}" for c in CASES])
+def test_attention_matches_torch_sdpa_dense(orc, case):
+    kv, S, Hq, Hkv, D, n, lens = case
+    w = wl.custom(num_seqs=S, num_q_heads=Hq, num_kv_heads=Hkv, head_size=D, q_per_seq=n,
+                  kv_dtype=kv, context_lens=lens, seed=31 + S + n)
+    vals = wl.token_values(w)
+    kc, vc = oracle_caches(orc, w, vals)
+    out, _, rc = oracle_attention(orc, w, vals, kc, vc)
+    assert rc == 0
+    for s in range(S):
+        ref = sdpa_reference(w, vals, s)
+        got = out[s * n:(s + 1) * n]
+        np.testing.assert_allclose(got, ref, rtol=1e-10, atol=1e-12)
+
+
+def test_tiny_workload_matches_sdpa(orc):
+    w = wl.tiny()
+    assert w.num_blocks == 32 and int(((w.context_lens + 15) // 16).sum()) == 10
+    vals = wl.token_values(w)
+    kc, vc = oracle_caches(orc, w, vals)
+    out, _, rc = oracle_attention(orc, w, vals, kc, vc)
+    assert rc == 0
+    for s in range(w.num_seqs):
+        np.testing.assert_allclose(out[s:s + 1], sdpa_reference(w, vals, s), rtol=1e-10, atol=1e-12)
+
+
+def test_block_permutation_invariance(orc):
+    """Moving every physical block elsewhere in the pool (and re-pointing the block table)
+    leaves the output bit-for-bit unchanged."""
+    w = wl.custom(num_seqs=3, num_q_heads=8, num_kv_heads=2, head_size=64, q_per_seq=2,
+                  kv_dtype="e5m2", context_lens=[9, 40, 77], seed=5)
+    vals = wl.token_values(w)
+    kc, vc = oracle_caches(orc, w, vals)
+    out1, _, _ = oracle_attention(orc, w, vals, kc, vc)
+    perm = np.random.default_rng(3).permutation(w.num_blocks)
+    kc2, vc2 = np.empty_like(kc), np.empty_like(vc)
+    kc2[perm] = kc
+    vc2[perm] = vc
+    bt = w.block_tables.copy()
+    bt[bt >= 0] = perm[bt[bt >= 0]]
+    q = bits16(vals["q"])
+    out2, _, rc = orc.paged_attention(q, 0, w.q_per_seq, kc2, vc2, KV_CODE["e5m2"], bt,
+                                      w.context_lens, w.scale)
+    assert rc == 0
+    assert np.array_equal(out1, out2)
+
+
+def test_weights_sum_to_one_and_respect_causality(orc):
+    w = wl.custom(num_seqs=3, num_q_heads=4, num_kv_heads=2, head_size=64, q_per_seq=4,
+                  kv_dtype="fp16", context_lens=[4, 21, 64], seed=9)
+    vals = wl.token_values(w)
+    kc, vc = oracle_caches(orc, w, vals)
+    _, wts, rc = oracle_attention(orc, w, vals, kc, vc, want_weights=True)
+    assert rc == 0
+    sums = wts.sum(axis=-1)
+    assert np.max(np.abs(sums - 1.0)) <= 1e-12
+    for s in range(w.num_seqs):
+        ctx = int(w.context_lens[s])
+        for j in range(w.q_per_seq):
+            row = wts[s * w.q_per_seq + j]
+            assert np.all(row[:, ctx - w.q_per_seq + j + 1:] == 0.0)
+            assert np.all(row[:, :ctx - w.q_per_seq + j + 1] > 0.0)
+
+
+@pytest.mark.parametrize("kv", ["fp16", "bf16", "e5m2"])
+def test_single_token_context_returns_v(orc, kv):
+    """ctx = 1: the only weight is exactly 1, so the output is V itself (dequantised)."""
+    w = wl.custom(num_seqs=2, num_q_heads=4, num_kv_heads=2, head_size=64, q_per_seq=1,
+                  kv_dtype=kv, context_lens=[1, 1], seed=4)
+    vals = wl.token_values(w)
+    kc, vc = oracle_caches(orc, w, vals)
+    out, _, rc = oracle_attention(orc, w, vals, kc, vc)
+    assert rc == 0
+    for s in range(2):
+        blk = w.block_tables[s, 0]
+        v = orc.decode_to_f64(vc[blk, :, 0, :], KV_CODE[kv])   # [Hkv, D]
+        want = np.repeat(v, w.group, axis=0)
+        assert np.array_equal(out[s], want)
+
+
+def test_gqa_group_equals_replicated_mha(orc):
+    """GQA-G equals MHA on a cache where KV head hq // G is copied to every query head
+    (the grouping reading: contiguous query heads share a KV head)."""
+    G, Hkv, D = 4, 2, 64
+    w = wl.custom(num_seqs=2, num_q_heads=G * Hkv, num_kv_heads=Hkv, head_size=D, q_per_seq=2,
+                  kv_dtype="bf16", context_lens=[18, 50], seed=21)
+    vals = wl.token_values(w)
+    kc, vc = oracle_caches(orc, w, vals)
+    out, _, _ = oracle_attention(orc, w, vals, kc, vc)
+    kc_m = np.repeat(kc, G, axis=1)
+    vc_m = np.repeat(vc, G, axis=1)
+    out_m, _, rc = orc.paged_attention(bits16(vals["q"]), 1, 2, kc_m, vc_m, KV_CODE["bf16"],
+                                       w.block_tables, w.context_lens, w.scale)
+    assert rc == 0
+    assert np.array_equal(out, out_m)
+
+
+def test_gqa_one_is_mqa_and_gqa_h_is_mha(orc):
+    """GQA-1 (one KV head) = MQA: every query head attends to the same K/V, so its output
+    equals a one-head run of that head's query. GQA-H (G = 1) = MHA: head h equals a
+    one-head run on KV head h alone."""
+    for Hkv in (1, 4):
+        w = wl.custom(num_seqs=2, num_q_heads=4, num_kv_heads=Hkv, head_size=64, q_per_seq=1,
+                      kv_dtype="fp16", context_lens=[7, 35], seed=40 + Hkv)
+        vals = wl.token_values(w)
+        kc, vc = oracle_caches(orc, w, vals)
+        out, _, _ = oracle_attention(orc, w, vals, kc, vc)
+        q = bits16(vals["q"])
+        for hq in range(4):
+            h = hq // w.group
+            o1, _, rc = orc.paged_attention(np.ascontiguousarray(q[:, hq:hq + 1]), 0, 1,
+                                            np.ascontiguousarray(kc[:, h:h + 1]),
+                                            np.ascontiguousarray(vc[:, h:h + 1]), 0,
+                                            w.block_tables, w.context_lens, w.scale)
+            assert rc == 0
+            assert np.array_equal(out[:, hq:hq + 1], o1)
+
+
+def test_spec_verify_row_equals_shorter_single_token_decode(orc):
+    """Query token j of an n-token verify equals a one-token decode whose context ends at
+    position ctx - n + j."""
+    n = 4
+    w = wl.custom(num_seqs=3, num_q_heads=8, num_kv_heads=2, head_size=64, q_per_seq=n,
+                  kv_dtype="e5m2", context_lens=[4, 20, 63], seed=12)
+    vals = wl.token_values(w)
+    kc, vc = oracle_caches(orc, w, vals)
+    out, _, _ = oracle_attention(orc, w, vals, kc, vc)
+    q = bits16(vals["q"])
+    for j in range(n):
+        qj = np.ascontiguousarray(q.reshape(w.num_seqs, n, 8, 64)[:, j])
+        lens = (w.context_lens - n + j + 1).astype(np.int32)
+        o1, _, rc = orc.paged_attention(qj, 0, 1, kc, vc, 2, w.block_tables, lens, w.scale)
+        assert rc == 0
+        assert np.array_equal(out.reshape(w.num_seqs, n, 8, 64)[:, j], o1)
+
+
+def test_zero_scale_gives_mean_of_v(orc):
+    w = wl.custom(num_seqs=2, num_q_heads=4, num_kv_heads=2, head_size=64, q_per_seq=2,
+                  kv_dtype="fp16", context_lens=[5, 30], seed=2, scale=0.0)
+    vals = wl.token_values(w)
+    kc, vc = oracle_caches(orc, w, vals)
+    out, _, _ = oracle_attention(orc, w, vals, kc, vc)
+    starts = w.seq_starts()
+    v = vals["v_all"].to(torch.float64).numpy()
+    for s in range(2):
+        ctx = int(w.context_lens[s])
+        for j in range(2):
+            lim = ctx - 2 + j + 1
+            mean = v[starts[s]:starts[s] + lim].mean(axis=0)   # [Hkv, D]
+            want = np.repeat(mean, w.group, axis=0)
+            np.testing.assert_allclose(out[s * 2 + j], want, rtol=1e-13, atol=1e-15)
+
+
+def test_bad_block_id_is_reported(orc):
+    w = wl.custom(num_seqs=1, num_q_heads=2, num_kv_heads=1, head_size=64, q_per_seq=1,
+                  kv_dtype="fp16", context_lens=[20], seed=2)
+    vals = wl.token_values(w)
+    kc, vc = oracle_caches(orc, w, vals)
+    bt = w.block_tables.copy()
+    bt[0, 1] = w.num_blocks  # out of range
+    _, _, rc = orc.paged_attention(bits16(vals["q"]), 0, 1, kc, vc, 0, bt, w.context_lens, w.scale)
+    assert rc == -1
+
+
+def test_threads_do_not_change_results(orc):
+    w = wl.custom(num_seqs=5, num_q_heads=8, num_kv_heads=2, head_size=64, q_per_seq=2,
+                  kv_dtype="bf16", context_lens=[3, 17, 33, 64, 90], seed=8)
+    vals = wl.token_values(w)
+    kc, vc = oracle_caches(orc, w, vals)
+    o1, _, _ = oracle_attention(orc, w, vals, kc, vc, num_threads=1)
+    o4, _, _ = oracle_attention(orc, w, vals, kc, vc, num_threads=4)
+    assert np.array_equal(o1, o4)
