@@ -1,0 +1,385 @@
+// C ABI of libpagedkv.so (declared in include/pagedkv.h): host-side argument
+// checks, launch geometry, tensor-map encoding and kernel launches. No device
+// memory is allocated here; every buffer comes from the caller.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "pagedkv.h"
+#include "pkv_internal.h"
+
+namespace {
+
+using namespace pkv;
+
+constexpr int kMaxDevices = 64;
+
+struct GeomEntry {
+  bool ready = false;
+  DecodeGeometry geom{};
+  int ctas_per_sm = 0;
+};
+
+struct DeviceState {
+  bool ready = false;
+  int sm_count = 0;
+  bool write_attr_done = false;
+  // [kv][d==128][ntw==2]
+  GeomEntry geom[3][2][2];
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+int current_device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return PKV_ERR_NO_DEVICE;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_NO_DEVICE;
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+      cudaGetLastError();
+      return PKV_ERR_NO_DEVICE;
+    }
+    st.sm_count = sms;
+    st.ready = true;
+  }
+  *out = &st;
+  return PKV_OK;
+}
+
+const void* decode_fn(int kv, int d, int ntw) {
+  switch (kv) {
+    case kKvF16: return decode_kernel_ptr_f16(d, ntw);
+    case kKvBf16: return decode_kernel_ptr_bf16(d, ntw);
+    case kKvE5m2: return decode_kernel_ptr_e5m2(d, ntw);
+    default: return nullptr;
+  }
+}
+
+const void* reduce_fn(int kv) {
+  switch (kv) {
+    case kKvF16: return reduce_kernel_ptr_f16();
+    case kKvBf16: return reduce_kernel_ptr_bf16();
+    case kKvE5m2: return reduce_kernel_ptr_e5m2();
+    default: return nullptr;
+  }
+}
+
+// Warp layout and ring depth for a unit of `rows` query rows. Consumers form a
+// WR x WB grid: WR warps split the rows (8*NTW each), WB warp groups take turns
+// on blocks. The ring gets as many stages as fit in about half of an SM's
+// shared memory, so that two CTAs share each SM.
+DecodeGeometry choose_geometry(int kv, int d, int rows) {
+  DecodeGeometry g{};
+  const int nt = (rows + 7) / 8;
+  if (nt <= 1) { g.ntw = 1; g.warps_rows = 1; g.warps_blocks = 4; }
+  else if (nt <= 2) { g.ntw = 2; g.warps_rows = 1; g.warps_blocks = 4; }
+  else if (nt <= 4) { g.ntw = 2; g.warps_rows = 2; g.warps_blocks = 2; }
+  else { g.ntw = 2; g.warps_rows = 4; g.warps_blocks = 1; }
+  g.threads = (g.warps_rows * g.warps_blocks + 1) * 32;
+  const size_t target = 110 * 1024;
+  const size_t fixed = decode_smem_layout(kv, d, g.ntw, g.warps_rows, g.warps_blocks, 0).total + 1024;
+  const size_t per_stage = 2 * static_cast<size_t>(tile_bytes(kv, d)) + 16;
+  long long st = target > fixed ? static_cast<long long>((target - fixed) / per_stage) : 0;
+  if (st < 4) st = 4;
+  if (st > 16) st = 16;
+  g.stages = static_cast<int>(st);
+  g.smem_bytes = decode_smem_layout(kv, d, g.ntw, g.warps_rows, g.warps_blocks, g.stages).total + 1024;
+  return g;
+}
+
+int get_geometry(DeviceState* st, int kv, int d, int rows, GeomEntry** out) {
+  const DecodeGeometry g0 = choose_geometry(kv, d, rows);
+  GeomEntry& e = st->geom[kv][d == 128 ? 1 : 0][g0.ntw == 2 ? 1 : 0];
+  // The entry depends on (kv, d, ntw, warps, stages); rows only pick ntw and the
+  // warp grid, so re-derive and compare.
+  if (!e.ready || e.geom.warps_rows != g0.warps_rows || e.geom.warps_blocks != g0.warps_blocks) {
+    const void* fn = decode_fn(kv, d, g0.ntw);
+    if (!fn) return PKV_ERR_UNSUPPORTED;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(g0.smem_bytes)) != cudaSuccess) {
+      cudaGetLastError();
+      return PKV_ERR_CUDA;
+    }
+    cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    cudaGetLastError();
+    int nblk = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nblk, fn, g0.threads, g0.smem_bytes) !=
+            cudaSuccess || nblk <= 0) {
+      cudaGetLastError();
+      return PKV_ERR_CUDA;
+    }
+    e.geom = g0;
+    e.ctas_per_sm = nblk < kMaxCtasPerSm ? nblk : kMaxCtasPerSm;
+    e.ready = true;
+  }
+  *out = &e;
+  return PKV_OK;
+}
+
+int encode_cache_map(CUtensorMap* map, const void* base, int kv, int d, long long total_rows) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    cudaGetLastError();
+  });
+  if (!g_encode) return PKV_ERR_CUDA;
+  const int rb = tile_row_bytes(kv, d);
+  const int esz = kv_elem_bytes(kv);
+  const CUtensorMapDataType dt = esz == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+  CUresult r;
+  if (rb == 256) {
+    // 256-byte token rows: view each row as 2 x 128 bytes so the 128-byte swizzle
+    // applies; the box [16][2][64] is the dense [16][128] tile.
+    cuuint64_t dims[3] = {64, 2, static_cast<cuuint64_t>(total_rows)};
+    cuuint64_t strides[2] = {128, 256};
+    cuuint32_t box[3] = {64, 2, static_cast<cuuint32_t>(kBlockSize)};
+    cuuint32_t es[3] = {1, 1, 1};
+    r = g_encode(map, dt, 3, const_cast<void*>(base), dims, strides, box, es,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(rb / esz), static_cast<cuuint64_t>(total_rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(rb)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(rb / esz), static_cast<cuuint32_t>(kBlockSize)};
+    cuuint32_t es[2] = {1, 1};
+    r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, es,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE,
+                 rb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
+}
+
+bool valid_cache(const pkv_cache_desc* c) {
+  if (!c) return false;
+  if (c->block_size != kBlockSize) return false;
+  if (c->head_size != 64 && c->head_size != 128) return false;
+  if (c->num_blocks <= 0 || c->num_kv_heads <= 0) return false;
+  const long long rows = static_cast<long long>(c->num_blocks) * c->num_kv_heads * kBlockSize;
+  return rows < (1ll << 31) - kBlockSize;
+}
+
+// Workspace layout: [unit descriptors, 256-aligned][partial slots].
+size_t desc_bytes(long long units) { return static_cast<size_t>((units * 8 + 255) / 256 * 256); }
+
+size_t workspace_bytes_for(long long units, int sm_count, int rows, int d) {
+  const long long slots = units + static_cast<long long>(sm_count) * kMaxCtasPerSm;
+  return desc_bytes(units) + static_cast<size_t>(slots) * partial_slot_floats(rows, d) * sizeof(float);
+}
+
+cudaError_t launch(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, void** args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_version(void) { return 100; }
+
+const char* pkv_error_string(int code) {
+  switch (code) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case PKV_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case PKV_ERR_CUDA: return "CUDA runtime error";
+    case PKV_ERR_NO_DEVICE: return "no usable CUDA device";
+    default: return "unknown status";
+  }
+}
+
+int pkv_kv_cache_write(const void* key, const void* value, pkv_dtype src_dtype, int32_t num_tokens,
+                       const int32_t* slot_mapping, void* k_cache, void* v_cache, pkv_dtype kv_dtype,
+                       const pkv_cache_desc* cache, int32_t* device_status, void* stream) {
+  if (num_tokens < 0 || !valid_cache(cache)) return PKV_ERR_INVALID_ARGUMENT;
+  const bool pair_ok = (src_dtype == PKV_FP16 && kv_dtype == PKV_FP16) ||
+                       (src_dtype == PKV_BF16 && kv_dtype == PKV_BF16) ||
+                       (src_dtype == PKV_FP16 && kv_dtype == PKV_FP8_E5M2);
+  if (!pair_ok) return PKV_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PKV_OK;
+  if (!key || !value || !slot_mapping || !k_cache || !v_cache) return PKV_ERR_INVALID_ARGUMENT;
+  if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned4(slot_mapping) || (device_status && !aligned4(device_status)))
+    return PKV_ERR_INVALID_ARGUMENT;
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* st = nullptr;
+  if (int rc = current_device_state(&st)) return rc;
+
+  CacheWriteArgs a{};
+  a.key = static_cast<const uint4*>(key);
+  a.value = static_cast<const uint4*>(value);
+  a.slot_mapping = slot_mapping;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.status = device_status;
+  a.num_slots = static_cast<long long>(cache->num_blocks) * kBlockSize;
+  a.num_tokens = num_tokens;
+  a.num_kv_heads = cache->num_kv_heads;
+  a.head_size = cache->head_size;
+  a.kv = static_cast<int32_t>(kv_dtype);
+
+  const long long chunks = 2ll * num_tokens * cache->num_kv_heads * (cache->head_size / 8);
+  long long blocks = (chunks + 255) / 256;
+  const long long max_blocks = static_cast<long long>(st->sm_count) * 16;
+  if (blocks > max_blocks) blocks = max_blocks;
+  void* args[1] = {&a};
+  const cudaError_t e = launch(kv_cache_write_kernel_ptr(), dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                               static_cast<cudaStream_t>(stream), args);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return PKV_ERR_CUDA;
+  }
+  return PKV_OK;
+}
+
+size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t q_per_seq,
+                                  const pkv_cache_desc* cache) {
+  if (num_seqs < 0 || num_q_heads <= 0 || q_per_seq <= 0 || !valid_cache(cache)) return 0;
+  if (num_q_heads % cache->num_kv_heads != 0) return 0;
+  const int rows = (num_q_heads / cache->num_kv_heads) * q_per_seq;
+  if (rows > kMaxRows) return 0;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* st = nullptr;
+  if (current_device_state(&st)) return 0;
+  const long long units = static_cast<long long>(num_seqs) * cache->num_kv_heads;
+  return workspace_bytes_for(units, st->sm_count, rows, cache->head_size);
+}
+
+int pkv_paged_attention_decode(void* out, const void* q, int32_t num_seqs, int32_t num_q_heads,
+                               int32_t q_per_seq, const void* k_cache, const void* v_cache,
+                               pkv_dtype kv_dtype, const pkv_cache_desc* cache,
+                               const int32_t* block_tables, int32_t max_blocks_per_seq,
+                               const int32_t* context_lens, float scale, void* workspace,
+                               size_t workspace_bytes, int32_t* device_status, void* stream) {
+  if (num_seqs < 0 || num_q_heads <= 0 || q_per_seq <= 0 || max_blocks_per_seq <= 0 ||
+      !valid_cache(cache))
+    return PKV_ERR_INVALID_ARGUMENT;
+  if (kv_dtype != PKV_FP16 && kv_dtype != PKV_BF16 && kv_dtype != PKV_FP8_E5M2)
+    return PKV_ERR_UNSUPPORTED;
+  if (num_q_heads % cache->num_kv_heads != 0) return PKV_ERR_INVALID_ARGUMENT;
+  const int group = num_q_heads / cache->num_kv_heads;
+  const long long rows_ll = static_cast<long long>(group) * q_per_seq;
+  if (rows_ll > kMaxRows) return PKV_ERR_UNSUPPORTED;
+  const int rows = static_cast<int>(rows_ll);
+  if (static_cast<long long>(num_seqs) * q_per_seq * num_q_heads >= (1ll << 31))
+    return PKV_ERR_UNSUPPORTED;
+  if (static_cast<long long>(num_seqs) * max_blocks_per_seq >= (1ll << 31) ||
+      max_blocks_per_seq > (1 << 26))
+    return PKV_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace)
+    return PKV_ERR_INVALID_ARGUMENT;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(workspace) || !aligned4(block_tables) || !aligned4(context_lens) ||
+      (device_status && !aligned4(device_status)))
+    return PKV_ERR_INVALID_ARGUMENT;
+
+  const int d = cache->head_size;
+  const int kv = static_cast<int>(kv_dtype);
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* st = nullptr;
+  if (int rc = current_device_state(&st)) return rc;
+  const long long units = static_cast<long long>(num_seqs) * cache->num_kv_heads;
+  if (workspace_bytes < workspace_bytes_for(units, st->sm_count, rows, d)) return PKV_ERR_WORKSPACE_TOO_SMALL;
+
+  GeomEntry* ge = nullptr;
+  if (int rc = get_geometry(st, kv, d, rows, &ge)) return rc;
+  const DecodeGeometry& g = ge->geom;
+
+  const long long total_rows = static_cast<long long>(cache->num_blocks) * cache->num_kv_heads * kBlockSize;
+  CUtensorMap tmk, tmv;
+  if (int rc = encode_cache_map(&tmk, k_cache, kv, d, total_rows)) return rc;
+  if (int rc = encode_cache_map(&tmv, v_cache, kv, d, total_rows)) return rc;
+
+  // One wave: every CTA resident at once; never more CTAs than blocks could exist.
+  long long grid = static_cast<long long>(st->sm_count) * ge->ctas_per_sm;
+  const long long max_work = units * max_blocks_per_seq;
+  if (grid > max_work) grid = max_work;
+  if (grid < 1) grid = 1;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  DecodeArgs a{};
+  a.out = out;
+  a.q = q;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.unit_desc = reinterpret_cast<int2*>(ws);
+  a.partials = reinterpret_cast<float*>(ws + desc_bytes(units));
+  a.status = device_status;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = cache->num_kv_heads;
+  a.q_per_seq = q_per_seq;
+  a.group = group;
+  a.rows = rows;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_blocks = cache->num_blocks;
+  a.warps_rows = g.warps_rows;
+  a.warps_blocks = g.warps_blocks;
+  a.stages = g.stages;
+  a.slot_floats = partial_slot_floats(rows, d);
+  a.scale_log2 = scale * 1.4426950408889634f;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* dargs[3] = {&tmk, &tmv, &a};
+  cudaError_t e = launch(decode_fn(kv, d, g.ntw), dim3(static_cast<unsigned>(grid)), dim3(g.threads),
+                         g.smem_bytes, s, dargs);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return PKV_ERR_CUDA;
+  }
+
+  ReduceArgs r{};
+  r.out = out;
+  r.partials = a.partials;
+  r.unit_desc = a.unit_desc;
+  r.num_kv_heads = cache->num_kv_heads;
+  r.num_q_heads = num_q_heads;
+  r.q_per_seq = q_per_seq;
+  r.group = group;
+  r.rows = rows;
+  r.head_size = d;
+  r.slot_floats = a.slot_floats;
+  r.num_ctas = static_cast<int32_t>(grid);
+  r.status = device_status;
+  void* rargs[1] = {&r};
+  e = launch(reduce_fn(kv), dim3(static_cast<unsigned>(units)), dim3(128), 0, s, rargs);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return PKV_ERR_CUDA;
+  }
+  return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,16 @@
+// Instantiations of the decode and reduce kernels for the e5m2 KV cache.
+#include "decode_kernel.cuh"
+
+namespace pkv {
+
+const void* decode_kernel_ptr_e5m2(int d, int ntw) {
+  if (d == 64 && ntw == 1) return reinterpret_cast<const void*>(&decode_kernel<2, 64, 1>);
+  if (d == 64 && ntw == 2) return reinterpret_cast<const void*>(&decode_kernel<2, 64, 2>);
+  if (d == 128 && ntw == 1) return reinterpret_cast<const void*>(&decode_kernel<2, 128, 1>);
+  if (d == 128 && ntw == 2) return reinterpret_cast<const void*>(&decode_kernel<2, 128, 2>);
+  return nullptr;
+}
+
+const void* reduce_kernel_ptr_e5m2() { return reinterpret_cast<const void*>(&reduce_kernel<2>); }
+
+}  // namespace pkv

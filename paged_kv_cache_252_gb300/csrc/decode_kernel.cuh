@@ -1,0 +1,643 @@
+// Paged decode attention for sm_103a: one persistent wave of CTAs splits the
+// whole batch's KV blocks evenly (a stream over (sequence, KV head, block)),
+// each CTA streaming its share through a TMA-fed shared-memory ring.
+//
+// What it computes follows "AI大模型推理速度翻倍，Colossal-Inference开源发布"
+// (分页注意力算法 PagedAttention: decode attention over KV blocks reached through
+// a block table; KV缓存量化 KVCache Quant: the E5M2 cache is cast back to fp16
+// on read), "AI 大模型推理优化技术详解" (2.2.1 Flash Attention: softmax reduced
+// block by block with a running max and sum; 2.2.2 GQA: one KV head serves a
+// group of query heads) and the speculative-decoding sections (several query
+// tokens per sequence, causal among themselves).
+//
+// Structure of one CTA
+//   warp NC (the last) : producer. Walks the CTA's block range, reads physical
+//                        block ids from the block table and issues one TMA copy
+//                        for the K tile and one for the V tile of each block.
+//   warps 0..NC-1      : consumers, a WR x WB grid. Row-group wr owns 8*NTW of
+//                        the unit's G*n query rows; block-stream wb takes every
+//                        WB-th block. Per block: S^T = K Q^T and O^T += V^T P^T on
+//                        tensor cores (mma.sync m16n8k16, fp32 accumulate), online
+//                        softmax in base 2 with quad shuffles. E5M2 tiles are
+//                        widened to fp16 in registers (byte << 8 is exact).
+//   At the end of each (sequence, KV head) piece the block streams are merged in
+//   shared memory; a piece covering a whole unit writes the normalised output,
+//   a partial piece writes (m, l, o) to its workspace slot for the reduce kernel.
+//
+// Tile layout in shared memory: the TMA box of a (block, head) tile is the
+// dense [16 tokens][head_size] array with the 128-byte (or 64-byte) swizzle
+// applied, so ldmatrix reads of 8 token rows hit 8 different bank groups.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "pkv_internal.h"
+#include "pkv_ptx.cuh"
+
+namespace pkv {
+
+template <int RB>
+__device__ __forceinline__ uint32_t swz(uint32_t off) {
+  if constexpr (RB >= 128) {
+    return off ^ ((off >> 3) & 0x70u);   // 16-byte chunk ^= 128-byte line index (mod 8)
+  } else {
+    return off ^ ((off >> 3) & 0x30u);   // 64-byte swizzle
+  }
+}
+
+// Blocks of one (sequence, KV head) unit. A context length outside
+// [1, max_blocks*16] is clamped so that every unit owns at least one block (and
+// so gets its output written) and never reads past its block-table row.
+__device__ __forceinline__ int unit_blocks(int ctx, int mbs) {
+  int c = ctx < 1 ? 1 : ctx;
+  const int cap = mbs * kBlockSize;
+  c = c > cap ? cap : c;
+  return (c + kBlockSize - 1) / kBlockSize;
+}
+
+__device__ __forceinline__ long long warp_sum_ll(long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Wait for an mbarrier phase; gives up after kWaitLimitNs or when another warp
+// of the CTA has already given up (abort flag in shared memory).
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
+                                              volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0u) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+  }
+}
+
+template <int KV>
+__device__ __forceinline__ uint32_t pack_p(float lo, float hi) {
+  if constexpr (KV == kKvBf16) {
+    return pack_bf16x2(lo, hi);
+  } else {
+    return pack_f16x2(lo, hi);
+  }
+}
+
+template <int KV>
+__device__ __forceinline__ void mma_kv(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                       uint32_t a3, uint32_t b0, uint32_t b1) {
+  if constexpr (KV == kKvBf16) {
+    mma_bf16(d, a0, a1, a2, a3, b0, b1);
+  } else {
+    mma_f16(d, a0, a1, a2, a3, b0, b1);
+  }
+}
+
+template <int KV, int D, int NTW>
+__global__ void __launch_bounds__(288)
+    decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const DecodeArgs a) {
+  constexpr int RB = tile_row_bytes(KV, D);   // bytes of one token row of a tile
+  constexpr int TILE = tile_bytes(KV, D);     // bytes of one (block, head) tile
+  constexpr int KS = D / 16;                  // k-steps of S^T = K Q^T
+  constexpr int MT = D / 16;                  // m-tiles of O^T = V^T P^T
+  constexpr bool kFp8 = (KV == kKvE5m2);
+  constexpr int QS = D * 2 + 16;              // query row stride in shared memory (bytes)
+  constexpr float kNegInf = -INFINITY;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int WR = a.warps_rows, WB = a.warps_blocks, NC = WR * WB, stages = a.stages;
+  const int R = a.rows, R_pad = 8 * NTW * WR;
+  const DecodeSmem lay = decode_smem_layout(KV, D, NTW, WR, WB, stages);
+  const uint32_t ring = smem_addr(smem + lay.ring);
+  const uint32_t bars = smem_addr(smem + lay.bars);   // full[k]: +8k, empty[k]: +8(stages+k)
+  uint8_t* qs = smem + lay.qs;
+  float* mrg_o = reinterpret_cast<float*>(smem + lay.mrg_o);
+  float* mrg_m = reinterpret_cast<float*>(smem + lay.mrg_ml);
+  float* mrg_l = mrg_m + WB * R_pad;
+  long long* red = reinterpret_cast<long long*>(smem + lay.misc);   // [10] block-reduce scratch
+  long long* plan = red + 10;                                      // total, b0, b1, s0, cum0
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(plan + 5);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nwarps = blockDim.x >> 5;
+  const bool is_producer = (warp == NC);
+
+  if (tid == 0) {
+    for (int k = 0; k < stages; ++k) {
+      mbar_init(bars + 8 * k, 1);
+      mbar_init(bars + 8 * (stages + k), WR);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (is_producer && lane == 0) {
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
+  }
+  // Padding rows of the query tile stay zero for the whole kernel.
+  for (int idx = tid; idx < (R_pad - R) * (QS / 16); idx += blockDim.x) {
+    reinterpret_cast<uint4*>(qs + R * QS)[idx] = make_uint4(0, 0, 0, 0);
+  }
+
+  // Everything below reads inputs a previous kernel in the stream may write.
+  pdl_wait_prior_grid();
+
+  const int S = a.num_seqs, Hkv = a.num_kv_heads, mbs = a.max_blocks_per_seq;
+  const int n = a.q_per_seq, G = a.group, Hq = a.num_q_heads;
+  const long long ncta = gridDim.x, cta = blockIdx.x;
+
+  // ---- plan: this CTA's share [b0, b1) of all (sequence, head, block) triples ----
+  {
+    long long local = 0;
+    for (int s = tid; s < S; s += blockDim.x) local += unit_blocks(a.context_lens[s], mbs);
+    local = warp_sum_ll(local);
+    if (lane == 0) red[warp] = local;
+    __syncthreads();
+    long long tot = 0;
+    for (int w = 0; w < nwarps; ++w) tot += red[w];
+    tot *= Hkv;
+    const long long b0 = cta * tot / ncta, b1 = (cta + 1) * tot / ncta;
+    __syncthreads();
+    if (tid == 0) { plan[0] = tot; plan[1] = b0; plan[2] = b1; plan[3] = -1; plan[4] = 0; }
+    if (b0 < b1) {
+      // Locate the sequence holding global block b0 with a block-wide scan.
+      long long carry = 0;
+      for (int base = 0; base < S; base += blockDim.x) {
+        const int s = base + tid;
+        const long long wblk = (s < S) ? (long long)Hkv * unit_blocks(a.context_lens[s], mbs) : 0;
+        long long v = wblk;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const long long t = __shfl_up_sync(0xffffffffu, v, o);
+          if (lane >= o) v += t;
+        }
+        if (lane == 31) red[warp] = v;
+        __syncthreads();
+        long long pre = 0, all = 0;
+        for (int w = 0; w < nwarps; ++w) {
+          if (w < warp) pre += red[w];
+          all += red[w];
+        }
+        const long long incl = v + pre, excl = incl - wblk;
+        if (s < S && carry + excl <= b0 && b0 < carry + incl) {
+          plan[3] = s;
+          plan[4] = (carry + excl) / Hkv;
+        }
+        carry += all;
+        __syncthreads();
+        if (carry > b0) break;
+      }
+    }
+    __syncthreads();
+  }
+  pdl_launch_dependents();
+
+  const long long total = plan[0], b0 = plan[1], b1 = plan[2];
+  if (b0 >= b1 || plan[3] < 0) return;
+
+  // Walk state, identical in every warp: current unit (s, h), block lb within it.
+  int s = static_cast<int>(plan[3]);
+  int ctx = a.context_lens[s];
+  int nb = unit_blocks(ctx, mbs);
+  int h, lb;
+  {
+    const long long off = b0 - (long long)Hkv * plan[4];
+    h = static_cast<int>(off / nb);
+    lb = static_cast<int>(off % nb);
+  }
+  long long gpos = b0;
+
+  if (is_producer) {
+    // ------------------------------- producer ------------------------------------
+    const uint64_t pol = l2_policy_evict_first();
+    const int total_rows = a.num_blocks * Hkv * kBlockSize;   // host guarantees < 2^31
+    int i = 0;
+    bool ok = true;
+    while (gpos < b1 && ok) {
+      const int take = static_cast<int>(min(static_cast<long long>(nb - lb), b1 - gpos));
+      if (lb == 0 && lane == 0) {
+        // This CTA owns the unit's first block: record which CTAs cover the unit.
+        const long long last_blk = gpos + nb - 1;
+        const int last_cta = static_cast<int>(((last_blk + 1) * ncta - 1) / total);
+        a.unit_desc[s * Hkv + h] = make_int2(static_cast<int>(cta), last_cta);
+      }
+      const int32_t* bt = a.block_tables + static_cast<size_t>(s) * mbs + lb;
+      int nxt = (lane < take) ? bt[lane] : 0;
+      for (int k0 = 0; k0 < take && ok; k0 += 32) {
+        const int cur = nxt;
+        const int cnt = min(32, take - k0);
+        if (k0 + 32 < take) nxt = (k0 + 32 + lane < take) ? bt[k0 + 32 + lane] : 0;
+        for (int k = 0; k < cnt; ++k, ++i) {
+          const int blk = __shfl_sync(0xffffffffu, cur, k);
+          int good = ok ? 1 : 0;
+          if (lane == 0 && good) {
+            const int stage = i % stages;
+            if (i >= stages &&
+                !wait_or_abort(bars + 8 * (stages + stage), ((i / stages) - 1) & 1, abort_flag)) {
+              good = 0;
+              *abort_flag = 1;
+              if (a.status) atomicOr(a.status, kDevTimeout);
+            } else {
+              const bool bad = static_cast<unsigned>(blk) >= static_cast<unsigned>(a.num_blocks);
+              if (bad && a.status) atomicOr(a.status, kDevBadBlock);
+              // A bad block id reads a box wholly past the end: TMA fills it with zeros.
+              const int row = bad ? total_rows : (blk * Hkv + h) * kBlockSize;
+              const uint32_t full = bars + 8 * stage;
+              const uint32_t kdst = ring + stage * 2 * TILE;
+              mbar_arrive_expect_tx(full, 2 * TILE);
+              if constexpr (RB == 256) {
+                tma_load_3d(kdst, &tm_k, 0, 0, row, full, pol);
+                tma_load_3d(kdst + TILE, &tm_v, 0, 0, row, full, pol);
+              } else {
+                tma_load_2d(kdst, &tm_k, 0, row, full, pol);
+                tma_load_2d(kdst + TILE, &tm_v, 0, row, full, pol);
+              }
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, good, 0) != 0;
+          if (!ok) break;   // block i was not issued
+        }
+      }
+      gpos += take;
+      lb += take;
+      if (lb == nb) {
+        lb = 0;
+        if (++h == Hkv) {
+          h = 0;
+          ++s;
+          if (gpos < b1) {
+            ctx = a.context_lens[s];
+            nb = unit_blocks(ctx, mbs);
+          }
+        }
+      }
+    }
+    // Drain: every copy issued into this CTA's shared memory lands before exit.
+    if (lane == 0) {
+      for (int k = (i > stages ? i - stages : 0); k < i; ++k) {
+        mbar_wait(bars + 8 * (k % stages), (k / stages) & 1);
+      }
+    }
+    return;
+  }
+
+  // --------------------------------- consumers -------------------------------------
+  const int wr = warp % WR, wb = warp / WR;
+  const int g8 = lane >> 2, c4 = lane & 3;
+  const int nthr_c = NC * 32;
+  const int row_base = wr * 8 * NTW;
+  bool alive = true;
+  int i = 0;
+
+  while (gpos < b1) {
+    const int take = static_cast<int>(min(static_cast<long long>(nb - lb), b1 - gpos));
+    const bool first = (lb == 0), last = (lb + take == nb);
+    const bool split = !(first && last);
+    const int u = s * Hkv + h;
+    const int cap = mbs * kBlockSize;
+    const int ctx_eff = ctx < cap ? ctx : cap;
+    if (first && warp == 0 && lane == 0 && (ctx < n || ctx > cap) && a.status) {
+      atomicOr(a.status, kDevBadCtx);
+    }
+
+    // Query rows of this unit -> shared memory. Row r = j*G + gi is query token j,
+    // query head h*G + gi.
+    for (int idx = tid; idx < R * (D / 8); idx += nthr_c) {
+      const int r = idx / (D / 8), ch = idx % (D / 8);
+      const int j = r / G, gi = r - j * G;
+      const size_t src = (static_cast<size_t>(s * n + j) * Hq + h * G + gi) * D + ch * 8;
+      *reinterpret_cast<uint4*>(qs + r * QS + ch * 16) =
+          *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) + src);
+    }
+    named_bar_sync(1, nthr_c);
+
+    // B fragments of Q^T for this warp's rows (held for the whole piece).
+    uint32_t qf[NTW][KS][2];
+#pragma unroll
+    for (int nt = 0; nt < NTW; ++nt) {
+      const int rb = row_base + nt * 8;
+      if constexpr (kFp8) {
+        // k-slot permutation matching the widened E5M2 K fragments: slots
+        // {2c,2c+1} <-> d = 16ks+4c+{0,1}, slots {2c+8,2c+9} <-> d = 16ks+4c+{2,3}.
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          const uint2 v = *reinterpret_cast<const uint2*>(qs + (rb + g8) * QS + (16 * ks + 4 * c4) * 2);
+          qf[nt][ks][0] = v.x;
+          qf[nt][ks][1] = v.y;
+        }
+      } else {
+#pragma unroll
+        for (int kp = 0; kp < KS / 2; ++kp) {
+          const uint32_t addr = smem_addr(qs) + (rb + (lane & 7)) * QS + (4 * kp + (lane >> 3)) * 16;
+          ldsm_x4(addr, qf[nt][2 * kp][0], qf[nt][2 * kp][1], qf[nt][2 * kp + 1][0],
+                  qf[nt][2 * kp + 1][1]);
+        }
+      }
+    }
+
+    float m_run[NTW][2], l_run[NTW][2];
+    float o_acc[MT][NTW][4];
+    int lim[NTW][2];
+#pragma unroll
+    for (int nt = 0; nt < NTW; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        m_run[nt][e] = kNegInf;
+        l_run[nt][e] = 0.f;
+        const int r = row_base + nt * 8 + 2 * c4 + e;
+        const int j = r / G;
+        const int lj = ctx_eff - n + j;             // last visible position of token j
+        lim[nt][e] = lj < ctx_eff - 1 ? lj : ctx_eff - 1;
+      }
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        o_acc[mt][nt][0] = o_acc[mt][nt][1] = o_acc[mt][nt][2] = o_acc[mt][nt][3] = 0.f;
+      }
+    }
+
+    const int k_first = ((wb - (i % WB)) % WB + WB) % WB;
+    for (int k = k_first; k < take; k += WB) {
+      const int ib = i + k;
+      const int stage = ib % stages;
+      const uint32_t parity = static_cast<uint32_t>((ib / stages) & 1);
+      const uint32_t kt = ring + stage * 2 * TILE, vt = kt + TILE;
+      if (alive && !wait_or_abort(bars + 8 * stage, parity, abort_flag)) {
+        alive = false;
+        *abort_flag = 1;
+        if (lane == 0 && a.status) atomicOr(a.status, kDevTimeout);
+      }
+      if (alive) {
+        const int tok0 = (lb + k) * kBlockSize;
+        if (tok0 + kBlockSize > ctx_eff) {
+          // Positions >= ctx are not part of the sequence; their V rows may hold
+          // anything (even NaN), so zero them before P V (their weight is 0).
+          const int tv = ctx_eff - tok0 > 0 ? ctx_eff - tok0 : 0;
+          uint4* vt_ptr = reinterpret_cast<uint4*>(smem + lay.ring + stage * 2 * TILE + TILE);
+          for (int idx = tv * (RB / 16) + lane; idx < kBlockSize * (RB / 16); idx += 32) {
+            vt_ptr[idx] = make_uint4(0, 0, 0, 0);
+          }
+          __syncwarp();
+          fence_proxy_async_smem();
+        }
+
+        // ---- S^T (16 tokens x 8*NTW rows) = K Q^T, two independent chains ----
+        float sa[2][NTW][4];
+#pragma unroll
+        for (int x = 0; x < 2; ++x)
+#pragma unroll
+          for (int nt = 0; nt < NTW; ++nt) sa[x][nt][0] = sa[x][nt][1] = sa[x][nt][2] = sa[x][nt][3] = 0.f;
+        {
+          const int mi = lane >> 3;
+          const int tok = (lane & 7) + 8 * (mi & 1);
+          if constexpr (!kFp8) {
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+              const int ch = 2 * ks + (mi >> 1);
+              uint32_t a0, a1, a2, a3;
+              ldsm_x4(kt + swz<RB>(tok * RB + ch * 16), a0, a1, a2, a3);
+#pragma unroll
+              for (int nt = 0; nt < NTW; ++nt)
+                mma_kv<KV>(sa[ks & 1][nt], a0, a1, a2, a3, qf[nt][ks][0], qf[nt][ks][1]);
+            }
+          } else {
+#pragma unroll
+            for (int kp = 0; kp < KS / 2; ++kp) {
+              const int ch = 2 * kp + (mi >> 1);
+              uint32_t r0, r1, r2, r3;
+              ldsm_x4(kt + swz<RB>(tok * RB + ch * 16), r0, r1, r2, r3);
+              // E5M2 byte b is the fp16 pattern b << 8: widen with byte permutes.
+              const uint32_t k0 = __byte_perm(r0, 0, 0x1404), k2 = __byte_perm(r0, 0, 0x3424);
+              const uint32_t k1 = __byte_perm(r1, 0, 0x1404), k3 = __byte_perm(r1, 0, 0x3424);
+              const uint32_t k4 = __byte_perm(r2, 0, 0x1404), k6 = __byte_perm(r2, 0, 0x3424);
+              const uint32_t k5 = __byte_perm(r3, 0, 0x1404), k7 = __byte_perm(r3, 0, 0x3424);
+#pragma unroll
+              for (int nt = 0; nt < NTW; ++nt) {
+                mma_f16(sa[0][nt], k0, k1, k2, k3, qf[nt][2 * kp][0], qf[nt][2 * kp][1]);
+                mma_f16(sa[1][nt], k4, k5, k6, k7, qf[nt][2 * kp + 1][0], qf[nt][2 * kp + 1][1]);
+              }
+            }
+          }
+        }
+
+        // ---- online softmax (base 2) over this block ----
+        const bool masked = tok0 + (kBlockSize - 1) > ctx_eff - n;
+        const int p_lo = tok0 + g8, p_hi = p_lo + 8;
+        uint32_t pb[NTW][2];
+        float alpha[NTW][2];
+#pragma unroll
+        for (int nt = 0; nt < NTW; ++nt) {
+          float pv[4];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float x_lo = (sa[0][nt][e] + sa[1][nt][e]) * a.scale_log2;
+            float x_hi = (sa[0][nt][2 + e] + sa[1][nt][2 + e]) * a.scale_log2;
+            if (masked) {
+              x_lo = (p_lo <= lim[nt][e]) ? x_lo : kNegInf;
+              x_hi = (p_hi <= lim[nt][e]) ? x_hi : kNegInf;
+            }
+            float mx = fmaxf(x_lo, x_hi);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float m_new = fmaxf(m_run[nt][e], mx);
+            const float m_use = (m_new == kNegInf) ? 0.f : m_new;
+            alpha[nt][e] = fast_exp2(m_run[nt][e] - m_use);
+            pv[e] = fast_exp2(x_lo - m_use);
+            pv[2 + e] = fast_exp2(x_hi - m_use);
+            l_run[nt][e] = l_run[nt][e] * alpha[nt][e] + pv[e] + pv[2 + e];
+            m_run[nt][e] = m_new;
+          }
+          // P^T fragments: the S^T accumulator layout (token g, rows 2c..2c+1) is an
+          // 8x8 b16 tile per 8 tokens; transposing it gives (row g, tokens 2c..2c+1),
+          // which is exactly the B operand of O^T += V^T P^T.
+          pb[nt][0] = movmatrix_t(pack_p<KV>(pv[0], pv[1]));
+          pb[nt][1] = movmatrix_t(pack_p<KV>(pv[2], pv[3]));
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int nt = 0; nt < NTW; ++nt) {
+            o_acc[mt][nt][0] *= alpha[nt][0];
+            o_acc[mt][nt][1] *= alpha[nt][1];
+            o_acc[mt][nt][2] *= alpha[nt][0];
+            o_acc[mt][nt][3] *= alpha[nt][1];
+          }
+
+        // ---- O^T (head_size x rows) += V^T P^T ----
+        {
+          const int mi = lane >> 3;
+          if constexpr (!kFp8) {
+            const int tok = (lane & 7) + 8 * (mi >> 1);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+              const int ch = 2 * mt + (mi & 1);
+              uint32_t a0, a1, a2, a3;
+              ldsm_x4_t(vt + swz<RB>(tok * RB + ch * 16), a0, a1, a2, a3);
+#pragma unroll
+              for (int nt = 0; nt < NTW; ++nt)
+                mma_kv<KV>(o_acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+            }
+          } else {
+            const int tok = (lane & 7) + 8 * (mi & 1);
+#pragma unroll
+            for (int mp = 0; mp < MT / 2; ++mp) {
+              const int ch = 2 * mp + (mi >> 1);
+              uint32_t r0, r1, r2, r3;
+              ldsm_x4_t(vt + swz<RB>(tok * RB + ch * 16), r0, r1, r2, r3);
+              // Transposed load of byte pairs: register = {V[2c][2g], V[2c][2g+1],
+              // V[2c+1][2g], V[2c+1][2g+1]}; m-row g <-> d 2g, m-row g+8 <-> d 2g+1.
+              const uint32_t v0 = __byte_perm(r0, 0, 0x2404), v1 = __byte_perm(r0, 0, 0x3414);
+              const uint32_t v2 = __byte_perm(r1, 0, 0x2404), v3 = __byte_perm(r1, 0, 0x3414);
+              const uint32_t v4 = __byte_perm(r2, 0, 0x2404), v5 = __byte_perm(r2, 0, 0x3414);
+              const uint32_t v6 = __byte_perm(r3, 0, 0x2404), v7 = __byte_perm(r3, 0, 0x3414);
+#pragma unroll
+              for (int nt = 0; nt < NTW; ++nt) {
+                mma_f16(o_acc[2 * mp][nt], v0, v1, v2, v3, pb[nt][0], pb[nt][1]);
+                mma_f16(o_acc[2 * mp + 1][nt], v4, v5, v6, v7, pb[nt][0], pb[nt][1]);
+              }
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars + 8 * (stages + stage));
+    }
+    i += take;
+
+    // ---- merge the WB block streams of this piece ----
+#pragma unroll
+    for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float lsum = l_run[nt][e];
+        lsum += __shfl_xor_sync(0xffffffffu, lsum, 4);
+        lsum += __shfl_xor_sync(0xffffffffu, lsum, 8);
+        lsum += __shfl_xor_sync(0xffffffffu, lsum, 16);
+        if (g8 == 0) {
+          const int r = row_base + nt * 8 + 2 * c4 + e;
+          mrg_m[wb * R_pad + r] = m_run[nt][e];
+          mrg_l[wb * R_pad + r] = lsum;
+        }
+      }
+    {
+      float* mo = mrg_o + static_cast<size_t>(wb) * R_pad * (D + 4);
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        const int d_lo = kFp8 ? 16 * mt + 2 * g8 : 16 * mt + g8;
+        const int d_hi = kFp8 ? d_lo + 1 : d_lo + 8;
+#pragma unroll
+        for (int nt = 0; nt < NTW; ++nt) {
+          const int r0 = row_base + nt * 8 + 2 * c4;
+          mo[r0 * (D + 4) + d_lo] = o_acc[mt][nt][0];
+          mo[(r0 + 1) * (D + 4) + d_lo] = o_acc[mt][nt][1];
+          mo[r0 * (D + 4) + d_hi] = o_acc[mt][nt][2];
+          mo[(r0 + 1) * (D + 4) + d_hi] = o_acc[mt][nt][3];
+        }
+      }
+    }
+    named_bar_sync(2, nthr_c);
+    for (int idx = tid; idx < R * (D / 4); idx += nthr_c) {
+      const int r = idx / (D / 4), d4 = idx - (idx / (D / 4)) * (D / 4);
+      float M = kNegInf;
+      for (int w = 0; w < WB; ++w) M = fmaxf(M, mrg_m[w * R_pad + r]);
+      const float Mu = (M == kNegInf) ? 0.f : M;
+      float lsum = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int w = 0; w < WB; ++w) {
+        const float f = fast_exp2(mrg_m[w * R_pad + r] - Mu);
+        lsum += f * mrg_l[w * R_pad + r];
+        const float4 v =
+            *reinterpret_cast<const float4*>(mrg_o + static_cast<size_t>(w * R_pad + r) * (D + 4) + d4 * 4);
+        acc.x += f * v.x;
+        acc.y += f * v.y;
+        acc.z += f * v.z;
+        acc.w += f * v.w;
+      }
+      if (!split) {
+        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+        const int j = r / G, gi = r - j * G;
+        const size_t dst = (static_cast<size_t>(s * n + j) * Hq + h * G + gi) * D + d4 * 4;
+        uint2 pk;
+        pk.x = pack_p<KV>(acc.x * inv, acc.y * inv);
+        pk.y = pack_p<KV>(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + dst) = pk;
+      } else {
+        float* P = a.partials + static_cast<size_t>(u + cta) * a.slot_floats;
+        if (d4 == 0) {
+          P[r] = M;
+          P[R + r] = lsum;
+        }
+        *reinterpret_cast<float4*>(P + partial_o_offset(R) + r * D + d4 * 4) = acc;
+      }
+    }
+
+    // ---- advance the walk ----
+    gpos += take;
+    lb += take;
+    if (lb == nb) {
+      lb = 0;
+      if (++h == Hkv) {
+        h = 0;
+        ++s;
+        if (gpos < b1) {
+          ctx = a.context_lens[s];
+          nb = unit_blocks(ctx, mbs);
+        }
+      }
+    }
+  }
+}
+
+// Combine the partial pieces of every (sequence, KV head) unit that more than
+// one CTA covered: M = max m_c, L = sum l_c 2^(m_c - M), out = sum o_c 2^(m_c - M) / L.
+template <int KV>
+__global__ void __launch_bounds__(128) reduce_kernel(const ReduceArgs a) {
+  constexpr float kNegInf = -INFINITY;
+  pdl_wait_prior_grid();
+  const int u = blockIdx.x;
+  const int2 dsc = a.unit_desc[u];
+  if (dsc.x >= dsc.y) return;   // one CTA covered the unit and wrote its output
+  if (dsc.x < 0 || dsc.y >= a.num_ctas) {
+    // Only possible if the decode kernel gave up before describing this unit.
+    if (threadIdx.x == 0 && a.status) atomicOr(a.status, kDevTimeout);
+    return;
+  }
+  const int s = u / a.num_kv_heads, h = u - s * a.num_kv_heads;
+  const int R = a.rows, D = a.head_size, G = a.group;
+  const int ooff = partial_o_offset(R);
+  for (int idx = threadIdx.x; idx < R * (D / 4); idx += blockDim.x) {
+    const int r = idx / (D / 4), d4 = idx - r * (D / 4);
+    float M = kNegInf;
+    for (int c = dsc.x; c <= dsc.y; ++c) {
+      M = fmaxf(M, a.partials[static_cast<size_t>(u + c) * a.slot_floats + r]);
+    }
+    const float Mu = (M == kNegInf) ? 0.f : M;
+    float lsum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = dsc.x; c <= dsc.y; ++c) {
+      const float* P = a.partials + static_cast<size_t>(u + c) * a.slot_floats;
+      const float f = fast_exp2(P[r] - Mu);
+      lsum += f * P[R + r];
+      const float4 v = *reinterpret_cast<const float4*>(P + ooff + r * D + d4 * 4);
+      acc.x += f * v.x;
+      acc.y += f * v.y;
+      acc.z += f * v.z;
+      acc.w += f * v.w;
+    }
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    const int j = r / G, gi = r - j * G;
+    const size_t dst = (static_cast<size_t>(s * a.q_per_seq + j) * a.num_q_heads + h * G + gi) * D + d4 * 4;
+    uint2 pk;
+    pk.x = pack_p<KV>(acc.x * inv, acc.y * inv);
+    pk.y = pack_p<KV>(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + dst) = pk;
+  }
+}
+
+}  // namespace pkv

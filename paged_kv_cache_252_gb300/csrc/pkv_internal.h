@@ -1,0 +1,125 @@
+// Internal declarations shared by the library's translation units (host and
+// device). Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace pkv {
+
+constexpr int kBlockSize = 16;       // tokens per KV block
+constexpr int kMaxRows = 64;         // GQA group size x query tokens handled per CTA
+constexpr int kMaxCtasPerSm = 4;     // upper bound used to size the workspace
+constexpr int kKvF16 = 0, kKvBf16 = 1, kKvE5m2 = 2;
+
+// Device-status bits (mirror the public PKV_DEV_* values).
+constexpr int32_t kDevBadSlot = 0x1;
+constexpr int32_t kDevBadBlock = 0x2;
+constexpr int32_t kDevBadCtx = 0x4;
+constexpr int32_t kDevTimeout = 0x8;
+
+// Arguments of the decode kernel (passed by value).
+struct DecodeArgs {
+  void* out;                   // [S*n][Hq][D] fp16/bf16
+  const void* q;               // same layout
+  const int32_t* block_tables; // [S][max_blocks_per_seq]
+  const int32_t* context_lens; // [S]
+  float* partials;             // split-KV partial slots
+  int2* unit_desc;             // [S*Hkv]: (first CTA, last CTA) covering the unit
+  int32_t* status;             // optional device status word
+  int32_t num_seqs;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t q_per_seq;
+  int32_t group;               // Hq / Hkv
+  int32_t rows;                // group * q_per_seq (rows of one (seq, KV head) unit)
+  int32_t max_blocks_per_seq;
+  int32_t num_blocks;
+  int32_t warps_rows;          // consumer warps splitting the rows
+  int32_t warps_blocks;        // consumer warp groups splitting the blocks
+  int32_t stages;              // depth of the shared-memory ring
+  int32_t slot_floats;         // floats per partial slot
+  float scale_log2;            // softmax scale * log2(e)
+};
+
+struct ReduceArgs {
+  void* out;
+  const float* partials;
+  const int2* unit_desc;
+  int32_t num_kv_heads;
+  int32_t num_q_heads;
+  int32_t q_per_seq;
+  int32_t group;
+  int32_t rows;
+  int32_t head_size;
+  int32_t slot_floats;
+  int32_t num_ctas;            // grid of the decode launch (bounds the descriptor range)
+  int32_t* status;
+};
+
+// Shared-memory and launch geometry of one decode instantiation.
+struct DecodeGeometry {
+  int ntw;            // n-tiles (8 rows each) per consumer warp
+  int warps_rows;
+  int warps_blocks;
+  int stages;
+  int threads;
+  size_t smem_bytes;
+};
+
+// Sizes derived from (kv dtype, head size).
+__host__ __device__ constexpr int kv_elem_bytes(int kv) { return kv == kKvE5m2 ? 1 : 2; }
+__host__ __device__ constexpr int tile_row_bytes(int kv, int d) { return d * kv_elem_bytes(kv); }
+__host__ __device__ constexpr int tile_bytes(int kv, int d) { return kBlockSize * tile_row_bytes(kv, d); }
+
+// Floats in one split-KV partial slot: m[rows], l[rows] (padded to 4), o[rows][D].
+__host__ __device__ constexpr int partial_o_offset(int rows) { return ((2 * rows + 3) / 4) * 4; }
+__host__ __device__ constexpr int partial_slot_floats(int rows, int d) {
+  return partial_o_offset(rows) + rows * d;
+}
+
+// Shared-memory layout of the decode kernel, relative to a 1024-aligned base.
+struct DecodeSmem {
+  size_t ring, bars, qs, mrg_o, mrg_ml, misc, total;
+};
+__host__ __device__ inline DecodeSmem decode_smem_layout(int kv, int d, int ntw, int wr, int wb,
+                                                         int stages) {
+  DecodeSmem s{};
+  const int rows_pad = 8 * ntw * wr;
+  s.ring = 0;
+  s.bars = s.ring + (size_t)stages * 2 * tile_bytes(kv, d);
+  s.qs = s.bars + (size_t)stages * 2 * 8;
+  s.qs = (s.qs + 15) & ~(size_t)15;
+  s.mrg_o = s.qs + (size_t)rows_pad * (d * 2 + 16);
+  s.mrg_ml = s.mrg_o + (size_t)wb * rows_pad * (d + 4) * 4;
+  s.misc = s.mrg_ml + (size_t)wb * rows_pad * 2 * 4;
+  s.total = s.misc + 256;   // block-reduce scratch, CTA plan, abort flag
+  return s;
+}
+
+// Kernel entry points, one set per KV dtype translation unit (nullptr if the
+// head size / rows-per-warp combination is not instantiated).
+const void* decode_kernel_ptr_f16(int d, int ntw);
+const void* decode_kernel_ptr_bf16(int d, int ntw);
+const void* decode_kernel_ptr_e5m2(int d, int ntw);
+const void* reduce_kernel_ptr_f16();
+const void* reduce_kernel_ptr_bf16();
+const void* reduce_kernel_ptr_e5m2();
+const void* kv_cache_write_kernel_ptr();
+
+struct CacheWriteArgs {
+  const uint4* key;            // [T][Hkv][D] 16-bit elements, 8 per uint4
+  const uint4* value;
+  const int32_t* slot_mapping; // [T]
+  void* k_cache;
+  void* v_cache;
+  int32_t* status;
+  long long num_slots;         // num_blocks * 16
+  int32_t num_tokens;
+  int32_t num_kv_heads;
+  int32_t head_size;
+  int32_t kv;                  // kKvF16 / kKvBf16 / kKvE5m2
+};
+
+}  // namespace pkv

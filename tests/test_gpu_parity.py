@@ -1,0 +1,197 @@
+"""CUDA path vs the CPU oracle, through the C ABI (Python binding = marshalling only).
+
+Cache writes must match the oracle's cache image bit for bit; attention outputs
+must satisfy |gpu - oracle| <= 2e-3 + 1e-2*|oracle| element-wise (fp64 oracle;
+for E5M2 the oracle reads the same E5M2 bytes, which the cache check proves
+identical).
+"""
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_252_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    return torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module")
+def gpu(dev):
+    import _gpu
+    return _gpu
+
+
+# ------------------------------------------------------------------------------------
+# cache write
+# ------------------------------------------------------------------------------------
+
+def test_e5m2_cast_exhaustive_through_cache_write(orc, dev, gpu):
+    """All 65,536 fp16 patterns written through kv_cache_write into an E5M2 cache
+    equal the oracle's cast byte for byte (NaN, inf, saturation, subnormals, ties)."""
+    import paged_kv_cache_252_gb300 as pkv
+    T, Hkv, D = 512, 1, 128
+    pat = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(T, Hkv, D)
+    key = torch.from_numpy(pat.view(np.int16)).view(torch.float16).to(dev)
+    val = torch.from_numpy(pat[::-1].copy().view(np.int16)).view(torch.float16).to(dev)
+    slots = torch.from_numpy(np.random.default_rng(0).permutation(T).astype(np.int32)).to(dev)
+    kc, vc = pkv.alloc_kv_cache(T // 16, Hkv, D, "e5m2", dev)
+    pkv.kv_cache_write(key, val, slots, kc, vc)
+    torch.cuda.synchronize()
+    okc = np.zeros(kc.shape, np.uint8)
+    ovc = np.zeros(vc.shape, np.uint8)
+    assert orc.kv_cache_write(pat, pat[::-1].copy(), orc.FP16, slots.cpu().numpy(), okc, ovc, orc.E5M2) == 0
+    assert np.array_equal(gpu.cache_bytes(kc), okc)
+    assert np.array_equal(gpu.cache_bytes(vc), ovc)
+
+
+@pytest.mark.parametrize("kv", ["fp16", "bf16", "e5m2"])
+@pytest.mark.parametrize("D", [64, 128])
+def test_cache_write_bit_exact(orc, dev, gpu, kv, D):
+    w = wl.custom(num_seqs=5, num_q_heads=8, num_kv_heads=4, head_size=D, q_per_seq=1,
+                  kv_dtype=kv, context_lens=[1, 16, 17, 100, 333], seed=70 + D)
+    vals = wl.token_values(w)
+    kc, vc, _ = gpu.cuda_path(w, vals, dev)
+    okc, ovc = gpu.oracle_caches(orc, w, vals)
+    assert np.array_equal(gpu.cache_bytes(kc), okc)
+    assert np.array_equal(gpu.cache_bytes(vc), ovc)
+
+
+def test_cache_write_skips_minus_one_and_flags_bad_slots(orc, dev, gpu):
+    import paged_kv_cache_252_gb300 as pkv
+    key = torch.randn(4, 2, 64, device=dev).half()
+    slots = torch.tensor([-1, 5, 1 << 20, -7], dtype=torch.int32, device=dev)
+    kc, vc = pkv.alloc_kv_cache(4, 2, 64, "fp16", dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    pkv.kv_cache_write(key, key, slots, kc, vc, device_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 0x1
+    flat = kc.permute(0, 2, 1, 3).reshape(64, 2, 64)   # slot-major view
+    assert torch.equal(flat[5], key[1])
+    nz = (kc != 0).any(dim=-1).sum().item()
+    assert nz == 2                                      # only slot 5 (two heads) written
+
+
+# ------------------------------------------------------------------------------------
+# decode attention: small shapes, all dtypes, block edges, GQA groups, spec tokens
+# ------------------------------------------------------------------------------------
+
+EDGE_LENS = [1, 2, 15, 16, 17, 31, 32, 33, 48, 49, 64, 65, 127, 200]
+
+SHAPES = [
+    # (Hq, Hkv, n)   rows = Hq/Hkv * n
+    (4, 4, 1),     # GQA-H (MHA), rows 1
+    (8, 4, 1),     # rows 2
+    (8, 2, 1),     # rows 4
+    (8, 1, 1),     # GQA-1 (MQA), rows 8
+    (16, 2, 2),    # rows 16
+    (12, 4, 5),    # rows 15 (ragged tile)
+    (64, 8, 4),    # 70B verify, rows 32
+    (16, 1, 4),    # rows 64
+]
+
+
+@pytest.mark.parametrize("kv", ["fp16", "bf16", "e5m2"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("shape", SHAPES, ids=[f"Hq{a}-Hkv{b}-n{c}" for a, b, c in SHAPES])
+def test_decode_small_parity(orc, dev, gpu, kv, D, shape):
+    Hq, Hkv, n = shape
+    lens = [max(x, n) for x in EDGE_LENS]
+    w = wl.custom(num_seqs=len(lens), num_q_heads=Hq, num_kv_heads=Hkv, head_size=D, q_per_seq=n,
+                  kv_dtype=kv, context_lens=lens, seed=1000 + D + Hq * 7 + n)
+    gpu.full_check(orc, w, dev)
+
+
+def test_tiny_workload(orc, dev, gpu):
+    gpu.full_check(orc, wl.tiny(), dev)
+
+
+def test_decode_is_deterministic(orc, dev, gpu):
+    w = wl.custom(num_seqs=6, num_q_heads=32, num_kv_heads=8, head_size=128, q_per_seq=1,
+                  kv_dtype="fp16", context_lens=[700, 1, 64, 3000, 17, 999], seed=5)
+    vals = wl.token_values(w)
+    _, _, o1 = gpu.cuda_path(w, vals, dev)
+    _, _, o2 = gpu.cuda_path(w, vals, dev)
+    assert torch.equal(o1, o2)
+
+
+def test_scale_zero_gives_mean_of_v(orc, dev, gpu):
+    w = wl.custom(num_seqs=3, num_q_heads=8, num_kv_heads=2, head_size=128, q_per_seq=1,
+                  kv_dtype="bf16", context_lens=[5, 40, 300], seed=8, scale=0.0)
+    gpu.full_check(orc, w, dev)
+
+
+def test_bad_block_and_context_are_flagged_not_faulted(orc, dev, gpu):
+    import paged_kv_cache_252_gb300 as pkv
+    w = wl.custom(num_seqs=3, num_q_heads=4, num_kv_heads=2, head_size=64, q_per_seq=2,
+                  kv_dtype="fp16", context_lens=[20, 40, 9], seed=3)
+    vals = wl.token_values(w)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    kc, vc, _ = gpu.cuda_path(w, vals, dev, status=status)
+    assert int(status.item()) == 0
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    bt[0, 1] = w.num_blocks + 5          # out-of-range physical block
+    cl = torch.from_numpy(w.context_lens).to(dev)
+    cl[2] = 1                            # shorter than q_per_seq
+    q = vals["q"].to(dev)
+    out = torch.empty_like(q)
+    pkv.paged_attention_decode(out, q, kc, vc, bt, cl, 2, w.scale, device_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 0x2 and int(status.item()) & 0x4
+    assert torch.isfinite(out[2:4]).all()   # sequence 1 untouched by the bad inputs
+    okc, ovc = gpu.oracle_caches(orc, w, vals)
+    ref, _, _ = gpu.oracle_attention(orc, w, vals, okc, ovc, seqs=[1])
+    gpu.compare(out, ref, rows=[2, 3])
+
+
+def test_empty_batch_is_a_no_op(dev):
+    import paged_kv_cache_252_gb300 as pkv
+    kc, vc = pkv.alloc_kv_cache(4, 2, 64, "fp16", dev)
+    q = torch.empty(0, 4, 64, dtype=torch.float16, device=dev)
+    bt = torch.empty(0, 1, dtype=torch.int32, device=dev)
+    cl = torch.empty(0, dtype=torch.int32, device=dev)
+    pkv.paged_attention_decode(q, q, kc, vc, bt, cl, 1, 0.125)
+    pkv.kv_cache_write(q.view(0, 2, 128)[:, :, :64].contiguous(), q.view(0, 2, 128)[:, :, :64].contiguous(),
+                       cl, kc, vc)
+    torch.cuda.synchronize()
+
+
+# ------------------------------------------------------------------------------------
+# the five workloads: reduced sizes in full, full sizes on sampled sequences
+# ------------------------------------------------------------------------------------
+
+REDUCED = {
+    "8b": dict(num_seqs=6),
+    "8b_fp8": dict(num_seqs=6),
+    "long": dict(num_seqs=2, ctx_scale=0.06),
+    "70b_spec": dict(num_seqs=10),
+}
+
+
+@pytest.mark.parametrize("key", list(REDUCED))
+def test_workload_reduced_full_parity(orc, dev, gpu, key):
+    w = wl.reduced(wl.by_name(key), **REDUCED[key])
+    gpu.full_check(orc, w, dev)
+
+
+def _sample(w, k, seed=0):
+    lens = w.context_lens
+    rng = np.random.default_rng(seed)
+    pick = {int(np.argmax(lens)), int(np.argmin(lens))}
+    pick |= set(int(x) for x in rng.choice(w.num_seqs, size=min(k, w.num_seqs), replace=False))
+    return sorted(pick)
+
+
+@pytest.mark.parametrize("key,k", [("8b", 6), ("8b_fp8", 6), ("long", 1), ("70b_spec", 8)])
+def test_workload_full_size_sampled_parity(orc, dev, gpu, key, k):
+    """Full-size workload in the bench's launch configuration: every cache byte is
+    compared; outputs of sampled sequences (longest, shortest, random) against the oracle."""
+    w = wl.by_name(key)
+    gpu.full_check(orc, w, dev, seqs=_sample(w, k), values_device=dev)
