@@ -162,7 +162,11 @@ __global__ void __launch_bounds__(288)
     long long tot = 0;
     for (int w = 0; w < nwarps; ++w) tot += red[w];
     tot *= Hkv;
-    const long long b0 = cta * tot / ncta, b1 = (cta + 1) * tot / ncta;
+    // Only min(grid, total) CTAs take work, so every active CTA owns at least one
+    // block and every CTA between a unit's first and last owner wrote a piece of it.
+    const long long nact = ncta < tot ? ncta : tot;
+    const long long b0 = cta < nact ? cta * tot / nact : tot;
+    const long long b1 = cta < nact ? (cta + 1) * tot / nact : tot;
     __syncthreads();
     if (tid == 0) { plan[0] = tot; plan[1] = b0; plan[2] = b1; plan[3] = -1; plan[4] = 0; }
     if (b0 < b1) {
@@ -223,8 +227,9 @@ __global__ void __launch_bounds__(288)
       const int take = static_cast<int>(min(static_cast<long long>(nb - lb), b1 - gpos));
       if (lb == 0 && lane == 0) {
         // This CTA owns the unit's first block: record which CTAs cover the unit.
+        const long long nact = ncta < total ? ncta : total;
         const long long last_blk = gpos + nb - 1;
-        const int last_cta = static_cast<int>(((last_blk + 1) * ncta - 1) / total);
+        const int last_cta = static_cast<int>(((last_blk + 1) * nact - 1) / total);
         a.unit_desc[s * Hkv + h] = make_int2(static_cast<int>(cta), last_cta);
       }
       const int32_t* bt = a.block_tables + static_cast<size_t>(s) * mbs + lb;
@@ -429,6 +434,7 @@ __global__ void __launch_bounds__(288)
         const bool masked = tok0 + (kBlockSize - 1) > ctx_eff - n;
         const int p_lo = tok0 + g8, p_hi = p_lo + 8;
         uint32_t pb[NTW][2];
+        uint32_t pb_lo[NTW][2];   // bf16 only: P - bf16(P), a second bf16 term
         float alpha[NTW][2];
 #pragma unroll
         for (int nt = 0; nt < NTW; ++nt) {
@@ -456,8 +462,20 @@ __global__ void __launch_bounds__(288)
           // P^T fragments: the S^T accumulator layout (token g, rows 2c..2c+1) is an
           // 8x8 b16 tile per 8 tokens; transposing it gives (row g, tokens 2c..2c+1),
           // which is exactly the B operand of O^T += V^T P^T.
-          pb[nt][0] = movmatrix_t(pack_p<KV>(pv[0], pv[1]));
-          pb[nt][1] = movmatrix_t(pack_p<KV>(pv[2], pv[3]));
+          const uint32_t h01 = pack_p<KV>(pv[0], pv[1]);
+          const uint32_t h23 = pack_p<KV>(pv[2], pv[3]);
+          pb[nt][0] = movmatrix_t(h01);
+          pb[nt][1] = movmatrix_t(h23);
+          if constexpr (KV == kKvBf16) {
+            // bf16 keeps 8 significant bits; P = hi + lo with both in bf16 keeps
+            // about 16, so the P V product is as accurate as with an fp16 P.
+            const uint32_t l01 = pack_bf16x2(pv[0] - __uint_as_float(h01 << 16),
+                                             pv[1] - __uint_as_float(h01 & 0xFFFF0000u));
+            const uint32_t l23 = pack_bf16x2(pv[2] - __uint_as_float(h23 << 16),
+                                             pv[3] - __uint_as_float(h23 & 0xFFFF0000u));
+            pb_lo[nt][0] = movmatrix_t(l01);
+            pb_lo[nt][1] = movmatrix_t(l23);
+          }
         }
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
@@ -480,8 +498,11 @@ __global__ void __launch_bounds__(288)
               uint32_t a0, a1, a2, a3;
               ldsm_x4_t(vt + swz<RB>(tok * RB + ch * 16), a0, a1, a2, a3);
 #pragma unroll
-              for (int nt = 0; nt < NTW; ++nt)
+              for (int nt = 0; nt < NTW; ++nt) {
                 mma_kv<KV>(o_acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+                if constexpr (KV == kKvBf16)
+                  mma_kv<KV>(o_acc[mt][nt], a0, a1, a2, a3, pb_lo[nt][0], pb_lo[nt][1]);
+              }
             }
           } else {
             const int tok = (lane & 7) + 8 * (mi & 1);
