@@ -1,0 +1,483 @@
+#!/usr/bin/env python3
+"""Benchmark: paged decode attention on GB300 (one JSON line on rank 0).
+
+A step is one pass of the whole hot path over one batch: the cache write of
+the step's new tokens (fp16 -> E5M2 cast for an E5M2 cache) followed by paged
+decode attention over every sequence's blocks (decode kernel + split-KV reduce).
+
+    python bench.py [--config 8b] [--steps K] [--warmup W] [--gpus N]
+    python bench.py --impl reference ...   # the CPU oracle on the same workload
+
+Workloads (seeded, synthetic; see paged_kv_cache_252_gb300/workloads.py):
+  tiny, 8b (default: Llama-3-8B-shaped decode layer, batch 64, fp16 KV),
+  8b_fp8, long, 70b_spec.
+
+value  = algorithmic bytes of the step / device time per step (GB/s), inputs
+         resident in HBM. Algorithmic bytes: every visible token's K and V once,
+         q in, out out, plus the cache write's reads and writes.
+e2e    = the same metric through the public Python API with host buffers: the
+         step's q, new K/V tokens, slot mapping, block table and lengths copied
+         from pinned host memory, and the output copied back, inside the timing.
+Several KV pools are rotated so that one cycle touches more than 4x the L2.
+
+Multi-GPU: replicas only. Each rank runs the same workload on its own GPU;
+value = total bytes of all ranks / max elapsed over ranks (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode-attention HBM GB/s (% of GB300 peak) and seq-steps/s"
+
+
+# ---------------------------------------------------------------------------------
+# distributed helpers (replicas only)
+# ---------------------------------------------------------------------------------
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        if device is not None and device.type == "cuda":
+            torch.distributed.barrier(device_ids=[device.index])
+        else:
+            torch.distributed.barrier()
+
+
+def aggregate(elapsed_s: float, units: float, world: int, device=None):
+    """Whole-job view of a replicated run: max elapsed over ranks, total units."""
+    if world <= 1:
+        return elapsed_s, units
+    dev = device if (device is not None and device.type == "cuda") else torch.device("cpu")
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    torch.distributed.all_reduce(u, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# ---------------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, interval_ms: int = 20):
+        self.gpu_index = gpu_index
+        self.interval_ms = interval_ms
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms={self.interval_ms}"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)   # let the first sample land before the timed region
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        return summarize_clocks(open(self.path).read().splitlines())
+
+
+def summarize_clocks(lines):
+    """nvidia-smi CSV rows (noheader, nounits) -> median SM clock, max, reasons seen."""
+    rows = []
+    for line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            rows.append({"sm": float(parts[1]), "max": float(parts[2]), "power": float(parts[3]),
+                         "hw": parts[5], "hw_thermal": parts[6], "sw_thermal": parts[7],
+                         "sw_power": parts[8]})
+        except ValueError:
+            continue
+    if not rows:
+        return None
+    reasons = set()
+    for r in rows:
+        for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                          ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+            if r[key].lower().startswith("active"):
+                reasons.add(name)
+    return {"sm_mhz": float(np.median([r["sm"] for r in rows])),
+            "sm_max_mhz": float(max(r["max"] for r in rows)),
+            "power_w_max": float(max(r["power"] for r in rows)),
+            "samples": len(rows), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------------
+# roofline helpers
+# ---------------------------------------------------------------------------------
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def csrc_digest() -> str:
+    src = hashlib.sha256()
+    d = os.path.join(ROOT, "paged_kv_cache_252_gb300", "csrc")
+    for fn in sorted(os.listdir(d)):
+        with open(os.path.join(d, fn), "rb") as f:
+            src.update(fn.encode())
+            src.update(f.read())
+    return src.hexdigest()
+
+
+def profiled_traffic(config: str):
+    """DRAM bytes per decode launch from a committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    entry = d.get(config)
+    if not entry or entry.get("csrc_sha256") != csrc_digest():
+        return None
+    return float(entry["dram_bytes_per_launch"])
+
+
+# ---------------------------------------------------------------------------------
+# our implementation
+# ---------------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local):
+    import paged_kv_cache_252_gb300 as pkv
+    from paged_kv_cache_252_gb300 import workloads as wl
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pkv.load_library()
+    w = wl.by_name(args.config)
+    vals = wl.token_values(w, device=dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20))
+    kv_bytes = w.kv_bytes_read()
+    pools = args.pools or max(2, math.ceil(4 * l2 / kv_bytes))
+
+    caches = []
+    for _ in range(pools):
+        kc, vc = pkv.alloc_kv_cache(w.num_blocks, w.num_kv_heads, w.head_size, w.kv_dtype, dev)
+        pkv.kv_cache_write(vals["k_all"], vals["v_all"], vals["slot_all"], kc, vc)   # prefill
+        caches.append((kc, vc))
+    new_idx = vals["new_idx"]
+    k_new = vals["k_all"][new_idx].contiguous()
+    v_new = vals["v_all"][new_idx].contiguous()
+    s_new = vals["slot_all"][new_idx].contiguous()
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    cl = torch.from_numpy(w.context_lens).to(dev)
+    qs = [vals["q"].clone() for _ in range(pools)]
+    outs = [torch.empty_like(vals["q"]) for _ in range(pools)]
+    del vals
+    torch.cuda.synchronize(dev)
+
+    def step(i):
+        p = i % pools
+        kc, vc = caches[p]
+        pkv.kv_cache_write(k_new, v_new, s_new, kc, vc)
+        pkv.paged_attention_decode(outs[p], qs[p], kc, vc, bt, cl, w.q_per_seq, w.scale)
+
+    step_bytes = kv_bytes + w.q_out_bytes() + w.write_bytes()
+    attn_bytes = kv_bytes + w.q_out_bytes()
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    barrier(world, dev)
+
+    sampler = ClockSampler(local) if not args.no_clocks else None
+    if sampler:
+        sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record()
+    for i in range(args.steps):
+        step(i)
+    e1.record()
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop() if sampler else None
+    barrier(world, dev)
+    elapsed = e0.elapsed_time(e1) / 1e3
+    job_elapsed, job_bytes = aggregate(elapsed, step_bytes * args.steps, world, dev)
+
+    # Decode op alone (decode kernel + split-KV reduce), per-launch CUDA events on its stream.
+    n_r = max(args.steps, 50)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_r)]
+    for i in range(n_r):
+        p = i % pools
+        kc, vc = caches[p]
+        evs[i][0].record()
+        pkv.paged_attention_decode(outs[p], qs[p], kc, vc, bt, cl, w.q_per_seq, w.scale)
+        evs[i][1].record()
+    torch.cuda.synchronize(dev)
+    dec_s = float(np.mean([a.elapsed_time(b) for a, b in evs])) / 1e3
+
+    # End to end through the public API with pinned host buffers.
+    e2e = None
+    if not args.no_e2e:
+        host = {n: t.cpu().pin_memory() for n, t in
+                (("q", qs[0]), ("k_new", k_new), ("v_new", v_new), ("s_new", s_new), ("bt", bt), ("cl", cl))}
+        out_h = torch.empty(outs[0].shape, dtype=outs[0].dtype).pin_memory()
+        dq, dk, dv = torch.empty_like(qs[0]), torch.empty_like(k_new), torch.empty_like(v_new)
+        ds, dbt, dcl = torch.empty_like(s_new), torch.empty_like(bt), torch.empty_like(cl)
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_h.numel() * out_h.element_size()
+
+        def e2e_step(i):
+            p = i % pools
+            kc, vc = caches[p]
+            dq.copy_(host["q"], non_blocking=True)
+            dk.copy_(host["k_new"], non_blocking=True)
+            dv.copy_(host["v_new"], non_blocking=True)
+            ds.copy_(host["s_new"], non_blocking=True)
+            dbt.copy_(host["bt"], non_blocking=True)
+            dcl.copy_(host["cl"], non_blocking=True)
+            pkv.kv_cache_write(dk, dv, ds, kc, vc)
+            pkv.paged_attention_decode(outs[p], dq, kc, vc, dbt, dcl, w.q_per_seq, w.scale)
+            out_h.copy_(outs[p], non_blocking=True)
+
+        for i in range(args.warmup):
+            e2e_step(i)
+        torch.cuda.synchronize(dev)
+        barrier(world, dev)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record()
+        for i in range(args.steps):
+            e2e_step(i)
+        a1.record()
+        torch.cuda.synchronize(dev)
+        e2e_el = a0.elapsed_time(a1) / 1e3
+        e2e_job_el, e2e_job_bytes = aggregate(e2e_el, step_bytes * args.steps, world, dev)
+        e2e = {"value": round(e2e_job_bytes / e2e_job_el / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": round(e2e_el / args.steps * 1e3, 5)}
+
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peaks()
+    achieved = attn_bytes / dec_s / 1e9
+    cpu = None if (args.no_cpu_baseline or world > 1) else cpu_baseline(w, args.cpu_budget_s)
+    value = job_bytes / job_elapsed / 1e9
+    dtype = ("fp16 q / " + w.kv_dtype + " KV, fp32 accumulate") if w.q_dtype == "fp16" \
+        else "bf16 q / bf16 KV, fp32 accumulate"
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(elapsed / args.steps * 1e3, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": dtype,
+        "data": "synthetic (seeded N(0,1) K/V/q, shuffled block pool)",
+        "config": {**w.describe(), "l2_policy": f"{pools} KV pools rotated, "
+                   f"{pools * kv_bytes / 1e9:.2f} GB per cycle > 4x L2 ({l2 / 1e6:.0f} MB)",
+                   "parallelism": f"replicas x{world}"},
+        "seq_steps_per_s": round(w.num_seqs * world * args.steps / job_elapsed, 1),
+        "tokens_per_s": round(w.num_seqs * w.q_per_seq * world * args.steps / job_elapsed, 1),
+        "pct_of_hbm_peak": round(100 * value / peak, 2),
+        "roofline": {"bound": "hbm", "kernel": "paged_attention_decode (decode + split-KV reduce)",
+                     "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                     "traffic": profiled_traffic(args.config),
+                     "algorithmic_bytes_per_launch": int(attn_bytes),
+                     "us_per_launch": round(dec_s * 1e6, 3)},
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------
+# CPU oracle (baseline / reference arm)
+# ---------------------------------------------------------------------------------
+
+def _oracle_inputs(w, seqs):
+    """Host inputs for the oracle: cache images holding the sample's tokens."""
+    import oracle
+    from paged_kv_cache_252_gb300 import workloads as wl
+    vals = wl.token_values(w, device="cpu")
+    starts = w.seq_starts()
+    mask = np.zeros(w.num_tokens_total, dtype=bool)
+    for s in seqs:
+        mask[starts[s]:starts[s + 1]] = True
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    k_all, v_all = bits(vals["k_all"]), bits(vals["v_all"])
+    slots = vals["slot_all"].numpy()
+    new = np.zeros(w.num_tokens_total, dtype=bool)
+    new[w.new_token_index()] = True
+    pre, stp = mask & ~new, mask & new
+    dt = np.uint8 if w.kv_dtype == "e5m2" else np.uint16
+    shape = (w.num_blocks, w.num_kv_heads, 16, w.head_size)
+    kc, vc = np.zeros(shape, dt), np.zeros(shape, dt)
+    code = {"fp16": 0, "bf16": 1, "e5m2": 2}[w.kv_dtype]
+    src = 1 if w.kv_dtype == "bf16" else 0
+    oracle.kv_cache_write(k_all[pre], v_all[pre], src, slots[pre], kc, vc, code)
+    return {"kc": kc, "vc": vc, "q": bits(vals["q"]), "k_new": k_all[stp], "v_new": v_all[stp],
+            "s_new": slots[stp], "src": src, "code": code}
+
+
+def _oracle_step(w, inp, seqs, threads):
+    import oracle
+    oracle.kv_cache_write(inp["k_new"], inp["v_new"], inp["src"], inp["s_new"], inp["kc"], inp["vc"],
+                          inp["code"])
+    qcode = 1 if w.q_dtype == "bf16" else 0
+    _, _, rc = oracle.paged_attention(inp["q"], qcode, w.q_per_seq, inp["kc"], inp["vc"], inp["code"],
+                                      w.block_tables, w.context_lens, w.scale, seqs=seqs,
+                                      num_threads=threads)
+    assert rc == 0
+
+
+def _sample_bytes(w, seqs):
+    lens = w.context_lens[seqs].astype(np.int64)
+    kv = int(lens.sum()) * w.num_kv_heads * w.head_size * 2 * w.kv_elem_bytes
+    qo = 2 * len(seqs) * w.q_per_seq * w.num_q_heads * w.head_size * 2
+    t = len(seqs) * w.q_per_seq
+    wr = t * w.num_kv_heads * w.head_size * (4 + w.kv_elem_bytes) + 4 * t
+    return kv + qo + wr
+
+
+def _pick_sample(w, budget_s, threads):
+    """Leading sequences whose oracle step takes about budget_s on `threads` threads,
+    estimated from a one-sequence probe."""
+    probe = [0]
+    inp = _oracle_inputs(w, probe)
+    t0 = time.perf_counter()
+    _oracle_step(w, inp, probe, 1)
+    per_token = (time.perf_counter() - t0) / max(1, int(w.context_lens[0]))
+    total_tokens = budget_s * threads / max(per_token, 1e-9)
+    seqs, acc = [], 0
+    for s in range(w.num_seqs):
+        if seqs and acc + int(w.context_lens[s]) > total_tokens:
+            break
+        seqs.append(s)
+        acc += int(w.context_lens[s])
+    return seqs
+
+
+def cpu_baseline(w, budget_s):
+    import oracle
+    threads = oracle.hardware_threads()
+    seqs = _pick_sample(w, budget_s, threads)
+    inp = _oracle_inputs(w, seqs)
+    t0 = time.perf_counter()
+    _oracle_step(w, inp, seqs, threads)
+    el = time.perf_counter() - t0
+    return {"value": round(_sample_bytes(w, seqs) / el / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{len(seqs)} of {w.num_seqs} sequences (their new-token cache write + fp64 "
+                      f"decode attention), {el:.1f} s on {threads} threads"}
+
+
+def run_reference(args, rank, world, local):
+    """The CPU oracle as the reference arm: bounded sample per step, same metric."""
+    if rank != 0:
+        return
+    import oracle
+    from paged_kv_cache_252_gb300 import workloads as wl
+    oracle.build()
+    w = wl.by_name(args.config)
+    threads = oracle.hardware_threads()
+    per_step = max(1.0, args.cpu_budget_s / max(1, args.steps + args.warmup))
+    seqs = _pick_sample(w, per_step, threads)
+    inp = _oracle_inputs(w, seqs)
+    for _ in range(args.warmup):
+        _oracle_step(w, inp, seqs, threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(w, inp, seqs, threads)
+    el = time.perf_counter() - t0
+    v = _sample_bytes(w, seqs) * args.steps / el / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) K/V/q, shuffled block pool)",
+        "config": {**w.describe(), "parallelism": "cpu oracle"},
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{len(seqs)} of {w.num_seqs} sequences per step"},
+        "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default="8b", choices=["tiny", "8b", "8b_fp8", "long", "70b_spec"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--pools", type=int, default=0, help="KV pools to rotate (default: >4x L2)")
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world, local)
+        return
+    init_dist(world, "nccl")
+    try:
+        run_ours(args, rank, world, local)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
