@@ -85,28 +85,29 @@ const void* reduce_fn(int kv) {
 DecodeGeometry choose_geometry(int kv, int d, int rows) {
   DecodeGeometry g{};
   const int nt = (rows + 7) / 8;
-  if (nt <= 1) { g.ntw = 1; g.warps_rows = 1; g.warps_blocks = 4; }
+  if (nt <= 1) { g.ntw = 1; g.warps_rows = 1; g.warps_blocks = 8; }
   else if (nt <= 2) { g.ntw = 2; g.warps_rows = 1; g.warps_blocks = 4; }
   else if (nt <= 4) { g.ntw = 2; g.warps_rows = 2; g.warps_blocks = 2; }
   else { g.ntw = 2; g.warps_rows = 4; g.warps_blocks = 1; }
   g.threads = (g.warps_rows * g.warps_blocks + 1) * 32;
   const size_t target = 110 * 1024;
-  const size_t fixed = decode_smem_layout(kv, d, g.ntw, g.warps_rows, g.warps_blocks, 0).total + 1024;
+  const size_t fixed = decode_smem_layout(kv, d, g.ntw, g.warps_rows, g.warps_blocks, 0, rows).total + 1024;
   const size_t per_stage = 2 * static_cast<size_t>(tile_bytes(kv, d)) + 16;
   long long st = target > fixed ? static_cast<long long>((target - fixed) / per_stage) : 0;
   if (st < 4) st = 4;
   if (st > 16) st = 16;
   g.stages = static_cast<int>(st);
-  g.smem_bytes = decode_smem_layout(kv, d, g.ntw, g.warps_rows, g.warps_blocks, g.stages).total + 1024;
+  g.smem_bytes = decode_smem_layout(kv, d, g.ntw, g.warps_rows, g.warps_blocks, g.stages, rows).total + 1024;
   return g;
 }
 
 int get_geometry(DeviceState* st, int kv, int d, int rows, GeomEntry** out) {
   const DecodeGeometry g0 = choose_geometry(kv, d, rows);
   GeomEntry& e = st->geom[kv][d == 128 ? 1 : 0][g0.ntw == 2 ? 1 : 0];
-  // The entry depends on (kv, d, ntw, warps, stages); rows only pick ntw and the
-  // warp grid, so re-derive and compare.
-  if (!e.ready || e.geom.warps_rows != g0.warps_rows || e.geom.warps_blocks != g0.warps_blocks) {
+  // The cached entry is keyed by (kv, d, ntw); the row count also changes the
+  // warp grid and the merge-buffer size, so re-derive and compare.
+  if (!e.ready || e.geom.warps_rows != g0.warps_rows || e.geom.warps_blocks != g0.warps_blocks ||
+      e.geom.stages != g0.stages || e.geom.smem_bytes != g0.smem_bytes) {
     const void* fn = decode_fn(kv, d, g0.ntw);
     if (!fn) return PKV_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -130,7 +131,8 @@ int get_geometry(DeviceState* st, int kv, int d, int rows, GeomEntry** out) {
   return PKV_OK;
 }
 
-int encode_cache_map(CUtensorMap* map, const void* base, int kv, int d, long long total_rows) {
+int encode_cache_map(CUtensorMap* map, const void* base, int kv, int d, long long total_rows,
+                     int half) {
   std::call_once(g_encode_once, [] {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q{};
@@ -145,27 +147,20 @@ int encode_cache_map(CUtensorMap* map, const void* base, int kv, int d, long lon
   const int rb = tile_row_bytes(kv, d);
   const int esz = kv_elem_bytes(kv);
   const CUtensorMapDataType dt = esz == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
-  CUresult r;
-  if (rb == 256) {
-    // 256-byte token rows: view each row as 2 x 128 bytes so the 128-byte swizzle
-    // applies; the box [16][2][64] is the dense [16][128] tile.
-    cuuint64_t dims[3] = {64, 2, static_cast<cuuint64_t>(total_rows)};
-    cuuint64_t strides[2] = {128, 256};
-    cuuint32_t box[3] = {64, 2, static_cast<cuuint32_t>(kBlockSize)};
-    cuuint32_t es[3] = {1, 1, 1};
-    r = g_encode(map, dt, 3, const_cast<void*>(base), dims, strides, box, es,
-                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  } else {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(rb / esz), static_cast<cuuint64_t>(total_rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(rb)};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(rb / esz), static_cast<cuuint32_t>(kBlockSize)};
-    cuuint32_t es[2] = {1, 1};
-    r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, es,
-                 CU_TENSOR_MAP_INTERLEAVE_NONE,
-                 rb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  }
+  // Every map is 2-D: [total_rows][row bytes] with a box of 16 token rows. A
+  // 256-byte row (16-bit elements, head size 128) is covered by two maps, one per
+  // 128-byte half (base + half*128, row stride 256), so every box is at most 128
+  // bytes wide and takes the 128-byte swizzle (64-byte for 64-byte rows).
+  const int box_bytes = rb > 128 ? 128 : rb;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(box_bytes / esz), static_cast<cuuint64_t>(total_rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(rb)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_bytes / esz), static_cast<cuuint32_t>(kBlockSize)};
+  cuuint32_t es[2] = {1, 1};
+  const char* ptr = static_cast<const char*>(base) + half * 128;
+  const CUresult r = g_encode(map, dt, 2, const_cast<char*>(ptr), dims, strides, box, es,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
 }
 
@@ -318,9 +313,16 @@ int pkv_paged_attention_decode(void* out, const void* q, int32_t num_seqs, int32
   const DecodeGeometry& g = ge->geom;
 
   const long long total_rows = static_cast<long long>(cache->num_blocks) * cache->num_kv_heads * kBlockSize;
-  CUtensorMap tmk, tmv;
-  if (int rc = encode_cache_map(&tmk, k_cache, kv, d, total_rows)) return rc;
-  if (int rc = encode_cache_map(&tmv, v_cache, kv, d, total_rows)) return rc;
+  CUtensorMap tmk, tmv, tmk1, tmv1;
+  if (int rc = encode_cache_map(&tmk, k_cache, kv, d, total_rows, 0)) return rc;
+  if (int rc = encode_cache_map(&tmv, v_cache, kv, d, total_rows, 0)) return rc;
+  if (tile_row_bytes(kv, d) > 128) {
+    if (int rc = encode_cache_map(&tmk1, k_cache, kv, d, total_rows, 1)) return rc;
+    if (int rc = encode_cache_map(&tmv1, v_cache, kv, d, total_rows, 1)) return rc;
+  } else {
+    tmk1 = tmk;
+    tmv1 = tmv;
+  }
 
   // One wave: every CTA resident at once; never more CTAs than blocks could exist.
   long long grid = static_cast<long long>(st->sm_count) * ge->ctas_per_sm;
@@ -352,7 +354,7 @@ int pkv_paged_attention_decode(void* out, const void* q, int32_t num_seqs, int32
   a.scale_log2 = scale * 1.4426950408889634f;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  void* dargs[3] = {&tmk, &tmv, &a};
+  void* dargs[5] = {&tmk, &tmv, &tmk1, &tmv1, &a};
   cudaError_t e = launch(decode_fn(kv, d, g.ntw), dim3(static_cast<unsigned>(grid)), dim3(g.threads),
                          g.smem_bytes, s, dargs);
   if (e != cudaSuccess) {

@@ -12,8 +12,8 @@
 //
 // Structure of one CTA
 //   warp NC (the last) : producer. Walks the CTA's block range, reads physical
-//                        block ids from the block table and issues one TMA copy
-//                        for the K tile and one for the V tile of each block.
+//                        block ids from the block table and issues the TMA copies
+//                        of the K tile and the V tile of each block.
 //   warps 0..NC-1      : consumers, a WR x WB grid. Row-group wr owns 8*NTW of
 //                        the unit's G*n query rows; block-stream wb takes every
 //                        WB-th block. Per block: S^T = K Q^T and O^T += V^T P^T on
@@ -24,9 +24,10 @@
 //   shared memory; a piece covering a whole unit writes the normalised output,
 //   a partial piece writes (m, l, o) to its workspace slot for the reduce kernel.
 //
-// Tile layout in shared memory: the TMA box of a (block, head) tile is the
-// dense [16 tokens][head_size] array with the 128-byte (or 64-byte) swizzle
-// applied, so ldmatrix reads of 8 token rows hit 8 different bank groups.
+// Tile layout in shared memory: a (block, head) tile is [16 tokens][row bytes]
+// (split into two [16][128-byte] halves when a row is 256 bytes) with the
+// 128-byte (or 64-byte) TMA swizzle applied, so ldmatrix reads of 8 token rows
+// hit 8 different bank groups.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -36,6 +37,19 @@
 #include "pkv_ptx.cuh"
 
 namespace pkv {
+
+// Unswizzled byte offset of 16-byte chunk `ch` of token `tok` inside a tile.
+// 256-byte token rows (16-bit elements, head size 128) arrive as two TMA boxes
+// of [16 tokens][128 bytes], one per half row, so that 8 consecutive tokens fall
+// on 8 consecutive 128-byte lines and the swizzle spreads them over all banks.
+template <int RB>
+__device__ __forceinline__ uint32_t tile_off(int tok, int ch) {
+  if constexpr (RB == 256) {
+    return static_cast<uint32_t>((ch >> 3) * (kBlockSize * 128) + tok * 128 + (ch & 7) * 16);
+  } else {
+    return static_cast<uint32_t>(tok * RB + ch * 16);
+  }
+}
 
 template <int RB>
 __device__ __forceinline__ uint32_t swz(uint32_t off) {
@@ -97,8 +111,9 @@ __device__ __forceinline__ void mma_kv(float (&d)[4], uint32_t a0, uint32_t a1, 
 }
 
 template <int KV, int D, int NTW>
-__global__ void __launch_bounds__(288)
+__global__ void __launch_bounds__(NTW == 1 ? 288 : 160, 2)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ CUtensorMap tm_k1, const __grid_constant__ CUtensorMap tm_v1,
                   const DecodeArgs a) {
   constexpr int RB = tile_row_bytes(KV, D);   // bytes of one token row of a tile
   constexpr int TILE = tile_bytes(KV, D);     // bytes of one (block, head) tile
@@ -113,13 +128,13 @@ __global__ void __launch_bounds__(288)
                                              ~static_cast<uintptr_t>(1023));
   const int WR = a.warps_rows, WB = a.warps_blocks, NC = WR * WB, stages = a.stages;
   const int R = a.rows, R_pad = 8 * NTW * WR;
-  const DecodeSmem lay = decode_smem_layout(KV, D, NTW, WR, WB, stages);
+  const DecodeSmem lay = decode_smem_layout(KV, D, NTW, WR, WB, stages, R);
   const uint32_t ring = smem_addr(smem + lay.ring);
   const uint32_t bars = smem_addr(smem + lay.bars);   // full[k]: +8k, empty[k]: +8(stages+k)
   uint8_t* qs = smem + lay.qs;
   float* mrg_o = reinterpret_cast<float*>(smem + lay.mrg_o);
   float* mrg_m = reinterpret_cast<float*>(smem + lay.mrg_ml);
-  float* mrg_l = mrg_m + WB * R_pad;
+  float* mrg_l = mrg_m + WB * R;
   long long* red = reinterpret_cast<long long*>(smem + lay.misc);   // [10] block-reduce scratch
   long long* plan = red + 10;                                      // total, b0, b1, s0, cum0
   volatile int* abort_flag = reinterpret_cast<volatile int*>(plan + 5);
@@ -139,6 +154,10 @@ __global__ void __launch_bounds__(288)
   if (is_producer && lane == 0) {
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
+    if constexpr (RB == 256) {
+      prefetch_tensormap(&tm_k1);
+      prefetch_tensormap(&tm_v1);
+    }
   }
   // Padding rows of the query tile stay zero for the whole kernel.
   for (int idx = tid; idx < (R_pad - R) * (QS / 16); idx += blockDim.x) {
@@ -257,8 +276,11 @@ __global__ void __launch_bounds__(288)
               const uint32_t kdst = ring + stage * 2 * TILE;
               mbar_arrive_expect_tx(full, 2 * TILE);
               if constexpr (RB == 256) {
-                tma_load_3d(kdst, &tm_k, 0, 0, row, full, pol);
-                tma_load_3d(kdst + TILE, &tm_v, 0, 0, row, full, pol);
+                // Two 2-D maps per cache, one per 128-byte half of a token row.
+                tma_load_2d(kdst, &tm_k, 0, row, full, pol);
+                tma_load_2d(kdst + TILE / 2, &tm_k1, 0, row, full, pol);
+                tma_load_2d(kdst + TILE, &tm_v, 0, row, full, pol);
+                tma_load_2d(kdst + TILE + TILE / 2, &tm_v1, 0, row, full, pol);
               } else {
                 tma_load_2d(kdst, &tm_k, 0, row, full, pol);
                 tma_load_2d(kdst + TILE, &tm_v, 0, row, full, pol);
@@ -383,9 +405,10 @@ __global__ void __launch_bounds__(288)
           // Positions >= ctx are not part of the sequence; their V rows may hold
           // anything (even NaN), so zero them before P V (their weight is 0).
           const int tv = ctx_eff - tok0 > 0 ? ctx_eff - tok0 : 0;
-          uint4* vt_ptr = reinterpret_cast<uint4*>(smem + lay.ring + stage * 2 * TILE + TILE);
-          for (int idx = tv * (RB / 16) + lane; idx < kBlockSize * (RB / 16); idx += 32) {
-            vt_ptr[idx] = make_uint4(0, 0, 0, 0);
+          uint8_t* vt_ptr = smem + lay.ring + stage * 2 * TILE + TILE;
+          for (int idx = lane; idx < (kBlockSize - tv) * (RB / 16); idx += 32) {
+            const int t = tv + idx / (RB / 16), ch = idx % (RB / 16);
+            *reinterpret_cast<uint4*>(vt_ptr + tile_off<RB>(t, ch)) = make_uint4(0, 0, 0, 0);
           }
           __syncwarp();
           fence_proxy_async_smem();
@@ -405,7 +428,7 @@ __global__ void __launch_bounds__(288)
             for (int ks = 0; ks < KS; ++ks) {
               const int ch = 2 * ks + (mi >> 1);
               uint32_t a0, a1, a2, a3;
-              ldsm_x4(kt + swz<RB>(tok * RB + ch * 16), a0, a1, a2, a3);
+              ldsm_x4(kt + swz<RB>(tile_off<RB>(tok, ch)), a0, a1, a2, a3);
 #pragma unroll
               for (int nt = 0; nt < NTW; ++nt)
                 mma_kv<KV>(sa[ks & 1][nt], a0, a1, a2, a3, qf[nt][ks][0], qf[nt][ks][1]);
@@ -415,7 +438,7 @@ __global__ void __launch_bounds__(288)
             for (int kp = 0; kp < KS / 2; ++kp) {
               const int ch = 2 * kp + (mi >> 1);
               uint32_t r0, r1, r2, r3;
-              ldsm_x4(kt + swz<RB>(tok * RB + ch * 16), r0, r1, r2, r3);
+              ldsm_x4(kt + swz<RB>(tile_off<RB>(tok, ch)), r0, r1, r2, r3);
               // E5M2 byte b is the fp16 pattern b << 8: widen with byte permutes.
               const uint32_t k0 = __byte_perm(r0, 0, 0x1404), k2 = __byte_perm(r0, 0, 0x3424);
               const uint32_t k1 = __byte_perm(r1, 0, 0x1404), k3 = __byte_perm(r1, 0, 0x3424);
@@ -496,7 +519,7 @@ __global__ void __launch_bounds__(288)
             for (int mt = 0; mt < MT; ++mt) {
               const int ch = 2 * mt + (mi & 1);
               uint32_t a0, a1, a2, a3;
-              ldsm_x4_t(vt + swz<RB>(tok * RB + ch * 16), a0, a1, a2, a3);
+              ldsm_x4_t(vt + swz<RB>(tile_off<RB>(tok, ch)), a0, a1, a2, a3);
 #pragma unroll
               for (int nt = 0; nt < NTW; ++nt) {
                 mma_kv<KV>(o_acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
@@ -510,7 +533,7 @@ __global__ void __launch_bounds__(288)
             for (int mp = 0; mp < MT / 2; ++mp) {
               const int ch = 2 * mp + (mi >> 1);
               uint32_t r0, r1, r2, r3;
-              ldsm_x4_t(vt + swz<RB>(tok * RB + ch * 16), r0, r1, r2, r3);
+              ldsm_x4_t(vt + swz<RB>(tile_off<RB>(tok, ch)), r0, r1, r2, r3);
               // Transposed load of byte pairs: register = {V[2c][2g], V[2c][2g+1],
               // V[2c+1][2g], V[2c+1][2g+1]}; m-row g <-> d 2g, m-row g+8 <-> d 2g+1.
               const uint32_t v0 = __byte_perm(r0, 0, 0x2404), v1 = __byte_perm(r0, 0, 0x3414);
@@ -540,14 +563,14 @@ __global__ void __launch_bounds__(288)
         lsum += __shfl_xor_sync(0xffffffffu, lsum, 4);
         lsum += __shfl_xor_sync(0xffffffffu, lsum, 8);
         lsum += __shfl_xor_sync(0xffffffffu, lsum, 16);
-        if (g8 == 0) {
-          const int r = row_base + nt * 8 + 2 * c4 + e;
-          mrg_m[wb * R_pad + r] = m_run[nt][e];
-          mrg_l[wb * R_pad + r] = lsum;
+        const int r = row_base + nt * 8 + 2 * c4 + e;
+        if (g8 == 0 && r < R) {
+          mrg_m[wb * R + r] = m_run[nt][e];
+          mrg_l[wb * R + r] = lsum;
         }
       }
     {
-      float* mo = mrg_o + static_cast<size_t>(wb) * R_pad * (D + 4);
+      float* mo = mrg_o + static_cast<size_t>(wb) * R * (D + 4);
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
         const int d_lo = kFp8 ? 16 * mt + 2 * g8 : 16 * mt + g8;
@@ -555,10 +578,14 @@ __global__ void __launch_bounds__(288)
 #pragma unroll
         for (int nt = 0; nt < NTW; ++nt) {
           const int r0 = row_base + nt * 8 + 2 * c4;
-          mo[r0 * (D + 4) + d_lo] = o_acc[mt][nt][0];
-          mo[(r0 + 1) * (D + 4) + d_lo] = o_acc[mt][nt][1];
-          mo[r0 * (D + 4) + d_hi] = o_acc[mt][nt][2];
-          mo[(r0 + 1) * (D + 4) + d_hi] = o_acc[mt][nt][3];
+          if (r0 < R) {
+            mo[r0 * (D + 4) + d_lo] = o_acc[mt][nt][0];
+            mo[r0 * (D + 4) + d_hi] = o_acc[mt][nt][2];
+          }
+          if (r0 + 1 < R) {
+            mo[(r0 + 1) * (D + 4) + d_lo] = o_acc[mt][nt][1];
+            mo[(r0 + 1) * (D + 4) + d_hi] = o_acc[mt][nt][3];
+          }
         }
       }
     }
@@ -566,15 +593,15 @@ __global__ void __launch_bounds__(288)
     for (int idx = tid; idx < R * (D / 4); idx += nthr_c) {
       const int r = idx / (D / 4), d4 = idx - (idx / (D / 4)) * (D / 4);
       float M = kNegInf;
-      for (int w = 0; w < WB; ++w) M = fmaxf(M, mrg_m[w * R_pad + r]);
+      for (int w = 0; w < WB; ++w) M = fmaxf(M, mrg_m[w * R + r]);
       const float Mu = (M == kNegInf) ? 0.f : M;
       float lsum = 0.f;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int w = 0; w < WB; ++w) {
-        const float f = fast_exp2(mrg_m[w * R_pad + r] - Mu);
-        lsum += f * mrg_l[w * R_pad + r];
+        const float f = fast_exp2(mrg_m[w * R + r] - Mu);
+        lsum += f * mrg_l[w * R + r];
         const float4 v =
-            *reinterpret_cast<const float4*>(mrg_o + static_cast<size_t>(w * R_pad + r) * (D + 4) + d4 * 4);
+            *reinterpret_cast<const float4*>(mrg_o + static_cast<size_t>(w * R + r) * (D + 4) + d4 * 4);
         acc.x += f * v.x;
         acc.y += f * v.y;
         acc.z += f * v.z;

@@ -83,8 +83,9 @@ __host__ __device__ constexpr int partial_slot_floats(int rows, int d) {
 struct DecodeSmem {
   size_t ring, bars, qs, mrg_o, mrg_ml, misc, total;
 };
+// The merge buffers hold only the unit's real rows (rows <= 8*ntw*wr).
 __host__ __device__ inline DecodeSmem decode_smem_layout(int kv, int d, int ntw, int wr, int wb,
-                                                         int stages) {
+                                                         int stages, int rows) {
   DecodeSmem s{};
   const int rows_pad = 8 * ntw * wr;
   s.ring = 0;
@@ -92,8 +93,8 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int kv, int d, int ntw,
   s.qs = s.bars + (size_t)stages * 2 * 8;
   s.qs = (s.qs + 15) & ~(size_t)15;
   s.mrg_o = s.qs + (size_t)rows_pad * (d * 2 + 16);
-  s.mrg_ml = s.mrg_o + (size_t)wb * rows_pad * (d + 4) * 4;
-  s.misc = s.mrg_ml + (size_t)wb * rows_pad * 2 * 4;
+  s.mrg_ml = s.mrg_o + (size_t)wb * rows * (d + 4) * 4;
+  s.misc = s.mrg_ml + (size_t)((wb * rows * 2 * 4 + 15) & ~15);
   s.total = s.misc + 256;   // block-reduce scratch, CTA plan, abort flag
   return s;
 }
