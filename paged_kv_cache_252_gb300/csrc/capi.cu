@@ -94,8 +94,15 @@ DecodeGeometry choose_geometry(int kv, int d, int rows) {
   const size_t fixed = decode_smem_layout(kv, d, g.ntw, g.warps_rows, g.warps_blocks, 0, rows).total + 1024;
   const size_t per_stage = 2 * static_cast<size_t>(tile_bytes(kv, d)) + 16;
   long long st = target > fixed ? static_cast<long long>((target - fixed) / per_stage) : 0;
-  if (st < 4) st = 4;
   if (st > 16) st = 16;
+  // The ring depth must be a multiple of the block-stream count: then stage k is
+  // only ever consumed by block-stream (k mod WB), which waits for its phases in
+  // order. With any other depth a stream can reach a stage whose previous use
+  // (another stream's block) has not landed yet, and the parity test of the
+  // mbarrier wait cannot tell that older phase from the one it wants.
+  st -= st % g.warps_blocks;
+  if (st < g.warps_blocks) st = g.warps_blocks;
+  if (st < 4) st = (4 + g.warps_blocks - 1) / g.warps_blocks * g.warps_blocks;
   g.stages = static_cast<int>(st);
   g.smem_bytes = decode_smem_layout(kv, d, g.ntw, g.warps_rows, g.warps_blocks, g.stages, rows).total + 1024;
   return g;

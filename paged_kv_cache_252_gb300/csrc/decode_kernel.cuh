@@ -20,6 +20,9 @@
 //                        tensor cores (mma.sync m16n8k16, fp32 accumulate), online
 //                        softmax in base 2 with quad shuffles. E5M2 tiles are
 //                        widened to fp16 in registers (byte << 8 is exact).
+//   Block i of the CTA goes to ring stage i mod STAGES and to block-stream
+//   i mod WB; STAGES is a multiple of WB, so each stage has a single consumer
+//   stream and every wait on its mbarrier is for the next phase in order.
 //   At the end of each (sequence, KV head) piece the block streams are merged in
 //   shared memory; a piece covering a whole unit writes the normalised output,
 //   a partial piece writes (m, l, o) to its workspace slot for the reduce kernel.
