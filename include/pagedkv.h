@@ -140,6 +140,42 @@ int pkv_paged_attention_decode(void* out, const void* q, int32_t num_seqs,
                                float scale, void* workspace, size_t workspace_bytes,
                                int32_t* device_status, void* stream);
 
+/*
+ * pkv_paged_attention_decode_noalloc — the same decode attention as
+ * pkv_paged_attention_decode, for callers that cannot allocate device memory
+ * when they run it (for example code running inside a custom allocator's
+ * callbacks, or engines that hand the whole device to the KV pool up front and
+ * forbid later cudaMalloc calls). The pages describe no such entry point; it
+ * is a deployment convenience of this library.
+ *
+ *   Arguments, layouts and results are those of pkv_paged_attention_decode,
+ *   without the workspace: the split-KV scratch comes from a buffer of
+ *   PKV_NOALLOC_SCRATCH_BYTES built into the library. Inputs and outputs are
+ *   still the caller's. The call itself allocates nothing.
+ *   - Limit: a problem whose pkv_decode_workspace_bytes(...) exceeds
+ *     PKV_NOALLOC_SCRATCH_BYTES is rejected with PKV_ERR_WORKSPACE_TOO_SMALL
+ *     before anything is launched (use pkv_paged_attention_decode with your own
+ *     workspace for it).
+ *   - The buffer occupies PKV_NOALLOC_SCRATCH_BYTES of device memory on every
+ *     device where the library's module holding it is loaded, until the process
+ *     exits.
+ *   - The first call on a device looks up the buffer's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call shares the one buffer and keeps the previous call's contents
+ *     in it (nothing in it needs to start at zero). Calls whose kernels overlap
+ *     on the GPU (different streams, or concurrent host threads) race on it;
+ *     serialise them.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+int pkv_paged_attention_decode_noalloc(void* out, const void* q, int32_t num_seqs,
+                                       int32_t num_q_heads, int32_t q_per_seq,
+                                       const void* k_cache, const void* v_cache,
+                                       pkv_dtype kv_dtype, const pkv_cache_desc* cache,
+                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t* context_lens, float scale,
+                                       int32_t* device_status, void* stream);
+
 /* Static description of a status code. Never NULL. */
 const char* pkv_error_string(int code);
 

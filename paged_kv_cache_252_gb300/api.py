@@ -59,6 +59,10 @@ def load_library():
             vp, vp, i32, i32, i32, vp, vp, ctypes.c_int, P(_CacheDesc), vp, i32, vp,
             ctypes.c_float, vp, ctypes.c_size_t, vp, vp]
         lib.pkv_paged_attention_decode.restype = ctypes.c_int
+        lib.pkv_paged_attention_decode_noalloc.argtypes = [
+            vp, vp, i32, i32, i32, vp, vp, ctypes.c_int, P(_CacheDesc), vp, i32, vp,
+            ctypes.c_float, vp, vp]
+        lib.pkv_paged_attention_decode_noalloc.restype = ctypes.c_int
         lib.pkv_error_string.argtypes = [ctypes.c_int]
         lib.pkv_error_string.restype = ctypes.c_char_p
         lib.pkv_version.restype = ctypes.c_int
@@ -182,4 +186,30 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
             float(scale), _ptr(workspace), int(workspace.numel() * workspace.element_size()),
             _ptr(device_status), _stream_handle(stream, q.device))
     _check(rc, "paged_attention_decode")
+    return out
+
+
+def paged_attention_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens,
+                                   q_per_seq: int, scale: float, kv_dtype=None, *,
+                                   device_status=None, stream=None):
+    """Same as :func:`paged_attention_decode`, but the split-KV scratch comes from a
+    fixed buffer inside the library, so neither this call nor the library allocates
+    device memory (for callers that cannot allocate at this point). Problems too
+    large for that buffer raise PagedKVError ("workspace too small"). Calls that
+    overlap on the GPU share the buffer and must be serialised."""
+    for n, t in (("out", out), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
+                 ("block_tables", block_tables), ("context_lens", context_lens)):
+        _need_cuda_contig(n, t)
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise PagedKVError("block_tables and context_lens must be int32")
+    if out.dtype != q.dtype:
+        raise PagedKVError("out and q must share a dtype")
+    d = _desc(k_cache)
+    with torch.cuda.device(q.device):
+        rc = load_library().pkv_paged_attention_decode_noalloc(
+            _ptr(out), _ptr(q), int(context_lens.shape[0]), int(q.shape[1]), int(q_per_seq),
+            _ptr(k_cache), _ptr(v_cache), _kv_code(kv_dtype, k_cache), ctypes.byref(d),
+            _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens), float(scale),
+            _ptr(device_status), _stream_handle(stream, q.device))
+    _check(rc, "paged_attention_decode_noalloc")
     return out

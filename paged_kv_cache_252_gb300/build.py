@@ -23,7 +23,8 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpagedkv.so")
 
-SOURCES = ["capi.cu", "kv_cache_write.cu", "decode_f16.cu", "decode_bf16.cu", "decode_e5m2.cu"]
+SOURCES = ["capi.cu", "kv_cache_write.cu", "decode_f16.cu", "decode_bf16.cu", "decode_e5m2.cu",
+           "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
