@@ -80,17 +80,19 @@ const void* reduce_fn(int kv) {
 
 // Warp layout and ring depth for a unit of `rows` query rows. Consumers form a
 // WR x WB grid: WR warps split the rows (8*NTW each), WB warp groups take turns
-// on blocks. The ring gets as many stages as fit in about half of an SM's
-// shared memory, so that two CTAs share each SM.
+// on blocks. Each CTA has one producer thread issuing the TMA copies, and that
+// thread is the limit when few CTAs share an SM, so units of at most 8 rows run
+// small CTAs (2 consumer warps, ~44 KB of shared memory) five to an SM; wider
+// units keep two larger CTAs per SM (their warps need ~168 registers).
 DecodeGeometry choose_geometry(int kv, int d, int rows) {
   DecodeGeometry g{};
   const int nt = (rows + 7) / 8;
-  if (nt <= 1) { g.ntw = 1; g.warps_rows = 1; g.warps_blocks = 8; }
+  size_t target = 110 * 1024;
+  if (nt <= 1) { g.ntw = 1; g.warps_rows = 1; g.warps_blocks = 2; target = 44 * 1024; }
   else if (nt <= 2) { g.ntw = 2; g.warps_rows = 1; g.warps_blocks = 4; }
   else if (nt <= 4) { g.ntw = 2; g.warps_rows = 2; g.warps_blocks = 2; }
   else { g.ntw = 2; g.warps_rows = 4; g.warps_blocks = 1; }
   g.threads = (g.warps_rows * g.warps_blocks + 1) * 32;
-  const size_t target = 110 * 1024;
   const size_t fixed = decode_smem_layout(kv, d, g.ntw, g.warps_rows, g.warps_blocks, 0, rows).total + 1024;
   const size_t per_stage = 2 * static_cast<size_t>(tile_bytes(kv, d)) + 16;
   long long st = target > fixed ? static_cast<long long>((target - fixed) / per_stage) : 0;
@@ -183,8 +185,10 @@ bool valid_cache(const pkv_cache_desc* c) {
 // Workspace layout: [unit descriptors, 256-aligned][partial slots].
 size_t desc_bytes(long long units) { return static_cast<size_t>((units * 8 + 255) / 256 * 256); }
 
-size_t workspace_bytes_for(long long units, int sm_count, int rows, int d) {
-  const long long slots = units + static_cast<long long>(sm_count) * kMaxCtasPerSm;
+// The decode grid has at most sm_count * ctas_per_sm CTAs, and a split unit's
+// pieces use slots unit + cta, so units + grid slots suffice.
+size_t workspace_bytes_for(long long units, int sm_count, int ctas_per_sm, int rows, int d) {
+  const long long slots = units + static_cast<long long>(sm_count) * ctas_per_sm;
   return desc_bytes(units) + static_cast<size_t>(slots) * partial_slot_floats(rows, d) * sizeof(float);
 }
 
@@ -271,11 +275,20 @@ size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t
   if (num_q_heads % cache->num_kv_heads != 0) return 0;
   const int rows = (num_q_heads / cache->num_kv_heads) * q_per_seq;
   if (rows > kMaxRows) return 0;
+  if (cache->head_size != 64 && cache->head_size != 128) return 0;
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState* st = nullptr;
   if (current_device_state(&st)) return 0;
   const long long units = static_cast<long long>(num_seqs) * cache->num_kv_heads;
-  return workspace_bytes_for(units, st->sm_count, rows, cache->head_size);
+  // The grid follows the kv dtype's occupancy; size for the largest over the
+  // supported dtypes so that one workspace serves any of them.
+  int ctas = 1;
+  for (int kv = kKvF16; kv <= kKvE5m2; ++kv) {
+    GeomEntry* ge = nullptr;
+    if (get_geometry(st, kv, cache->head_size, rows, &ge)) return 0;
+    if (ge->ctas_per_sm > ctas) ctas = ge->ctas_per_sm;
+  }
+  return workspace_bytes_for(units, st->sm_count, ctas, rows, cache->head_size);
 }
 
 int pkv_paged_attention_decode(void* out, const void* q, int32_t num_seqs, int32_t num_q_heads,
@@ -313,11 +326,11 @@ int pkv_paged_attention_decode(void* out, const void* q, int32_t num_seqs, int32
   DeviceState* st = nullptr;
   if (int rc = current_device_state(&st)) return rc;
   const long long units = static_cast<long long>(num_seqs) * cache->num_kv_heads;
-  if (workspace_bytes < workspace_bytes_for(units, st->sm_count, rows, d)) return PKV_ERR_WORKSPACE_TOO_SMALL;
-
   GeomEntry* ge = nullptr;
   if (int rc = get_geometry(st, kv, d, rows, &ge)) return rc;
   const DecodeGeometry& g = ge->geom;
+  if (workspace_bytes < workspace_bytes_for(units, st->sm_count, ge->ctas_per_sm, rows, d))
+    return PKV_ERR_WORKSPACE_TOO_SMALL;
 
   const long long total_rows = static_cast<long long>(cache->num_blocks) * cache->num_kv_heads * kBlockSize;
   CUtensorMap tmk, tmv, tmk1, tmv1;

@@ -114,7 +114,7 @@ __device__ __forceinline__ void mma_kv(float (&d)[4], uint32_t a0, uint32_t a1, 
 }
 
 template <int KV, int D, int NTW>
-__global__ void __launch_bounds__(NTW == 1 ? 288 : 160, 2)
+__global__ void __launch_bounds__(NTW == 1 ? 96 : 160, NTW == 1 ? 5 : 2)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_k1, const __grid_constant__ CUtensorMap tm_v1,
                   const DecodeArgs a) {

@@ -10,7 +10,7 @@ namespace pkv {
 
 constexpr int kBlockSize = 16;       // tokens per KV block
 constexpr int kMaxRows = 64;         // GQA group size x query tokens handled per CTA
-constexpr int kMaxCtasPerSm = 4;     // upper bound used to size the workspace
+constexpr int kMaxCtasPerSm = 8;     // upper bound on resident decode CTAs per SM
 constexpr int kKvF16 = 0, kKvBf16 = 1, kKvE5m2 = 2;
 
 // Device-status bits (mirror the public PKV_DEV_* values).
