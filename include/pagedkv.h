@@ -102,7 +102,7 @@ int pkv_kv_cache_write(const void* key, const void* value, pkv_dtype src_dtype,
 /*
  * pkv_decode_workspace_bytes — size of the scratch buffer paged attention needs
  * on the CURRENT device for this problem shape (split-KV partial results and a
- * per-(sequence, KV head) descriptor). It depends only on the arguments and the
+ * per-(sequence, KV head) counter of finished pieces). It depends only on the arguments and the
  * device's multiprocessor count; any buffer at least this large works, and it
  * needs no initialisation. Returns 0 on invalid arguments.
  */
@@ -123,7 +123,8 @@ size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t
  *                 q_per_seq query tokens, which are its last q_per_seq positions.
  *   scale         softmax scale (typically 1/sqrt(head_size)).
  *   workspace     device scratch of at least pkv_decode_workspace_bytes(...)
- *                 bytes, 16-byte aligned; contents need no initialisation.
+ *                 bytes, 16-byte aligned; contents need no initialisation. Two
+ *                 calls in flight at the same time must not share a workspace.
  *
  *   For each sequence s, query head hq (KV head h = hq / (num_q_heads/num_kv_heads))
  *   and query token j, with L = context_lens[s] - q_per_seq + j + 1:

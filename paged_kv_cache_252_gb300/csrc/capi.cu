@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -35,6 +36,7 @@ std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
+std::atomic<uint32_t> g_call_epoch{0};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -65,15 +67,6 @@ const void* decode_fn(int kv, int d, int ntw) {
     case kKvF16: return decode_kernel_ptr_f16(d, ntw);
     case kKvBf16: return decode_kernel_ptr_bf16(d, ntw);
     case kKvE5m2: return decode_kernel_ptr_e5m2(d, ntw);
-    default: return nullptr;
-  }
-}
-
-const void* reduce_fn(int kv) {
-  switch (kv) {
-    case kKvF16: return reduce_kernel_ptr_f16();
-    case kKvBf16: return reduce_kernel_ptr_bf16();
-    case kKvE5m2: return reduce_kernel_ptr_e5m2();
     default: return nullptr;
   }
 }
@@ -182,7 +175,7 @@ bool valid_cache(const pkv_cache_desc* c) {
   return rows < (1ll << 31) - kBlockSize;
 }
 
-// Workspace layout: [unit descriptors, 256-aligned][partial slots].
+// Workspace layout: [per-unit piece counters, 8 bytes each, 256-aligned][partial slots].
 size_t desc_bytes(long long units) { return static_cast<size_t>((units * 8 + 255) / 256 * 256); }
 
 // The decode grid has at most sm_count * ctas_per_sm CTAs, and a split unit's
@@ -356,7 +349,7 @@ int pkv_paged_attention_decode(void* out, const void* q, int32_t num_seqs, int32
   a.q = q;
   a.block_tables = block_tables;
   a.context_lens = context_lens;
-  a.unit_desc = reinterpret_cast<int2*>(ws);
+  a.piece_counts = reinterpret_cast<unsigned long long*>(ws);
   a.partials = reinterpret_cast<float*>(ws + desc_bytes(units));
   a.status = device_status;
   a.num_seqs = num_seqs;
@@ -372,35 +365,21 @@ int pkv_paged_attention_decode(void* out, const void* q, int32_t num_seqs, int32
   a.stages = g.stages;
   a.slot_floats = partial_slot_floats(rows, d);
   a.scale_log2 = scale * 1.4426950408889634f;
+  // Counters from an earlier call carry an older epoch and count as zero, so the
+  // workspace never needs clearing. (0 is skipped so a zeroed buffer is stale too.)
+  uint32_t ep = ++g_call_epoch;
+  if (ep == 0) ep = ++g_call_epoch;
+  a.epoch = ep;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   void* dargs[5] = {&tmk, &tmv, &tmk1, &tmv1, &a};
-  cudaError_t e = launch(decode_fn(kv, d, g.ntw), dim3(static_cast<unsigned>(grid)), dim3(g.threads),
+  const cudaError_t e = launch(decode_fn(kv, d, g.ntw), dim3(static_cast<unsigned>(grid)), dim3(g.threads),
                          g.smem_bytes, s, dargs);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return PKV_ERR_CUDA;
   }
 
-  ReduceArgs r{};
-  r.out = out;
-  r.partials = a.partials;
-  r.unit_desc = a.unit_desc;
-  r.num_kv_heads = cache->num_kv_heads;
-  r.num_q_heads = num_q_heads;
-  r.q_per_seq = q_per_seq;
-  r.group = group;
-  r.rows = rows;
-  r.head_size = d;
-  r.slot_floats = a.slot_floats;
-  r.num_ctas = static_cast<int32_t>(grid);
-  r.status = device_status;
-  void* rargs[1] = {&r};
-  e = launch(reduce_fn(kv), dim3(static_cast<unsigned>(units)), dim3(128), 0, s, rargs);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return PKV_ERR_CUDA;
-  }
   return PKV_OK;
 }
 

@@ -1,4 +1,4 @@
-// Instantiations of the decode and reduce kernels for the e5m2 KV cache.
+// Instantiations of the decode kernel for the e5m2 KV cache.
 #include "decode_kernel.cuh"
 
 namespace pkv {
@@ -11,6 +11,5 @@ const void* decode_kernel_ptr_e5m2(int d, int ntw) {
   return nullptr;
 }
 
-const void* reduce_kernel_ptr_e5m2() { return reinterpret_cast<const void*>(&reduce_kernel<2>); }
 
 }  // namespace pkv

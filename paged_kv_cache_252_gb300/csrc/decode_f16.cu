@@ -1,4 +1,4 @@
-// Instantiations of the decode and reduce kernels for the f16 KV cache.
+// Instantiations of the decode kernel for the f16 KV cache.
 #include "decode_kernel.cuh"
 
 namespace pkv {
@@ -11,6 +11,5 @@ const void* decode_kernel_ptr_f16(int d, int ntw) {
   return nullptr;
 }
 
-const void* reduce_kernel_ptr_f16() { return reinterpret_cast<const void*>(&reduce_kernel<0>); }
 
 }  // namespace pkv

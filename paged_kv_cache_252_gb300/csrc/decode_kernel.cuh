@@ -25,7 +25,10 @@
 //   stream and every wait on its mbarrier is for the next phase in order.
 //   At the end of each (sequence, KV head) piece the block streams are merged in
 //   shared memory; a piece covering a whole unit writes the normalised output,
-//   a partial piece writes (m, l, o) to its workspace slot for the reduce kernel.
+//   a partial piece writes (m, l, o) to its workspace slot and counts itself on
+//   the unit's counter; the CTA that finishes the unit's last piece combines all
+//   pieces (M = max m, L = sum l 2^(m-M), out = sum o 2^(m-M) / L) and writes
+//   the output, so no separate reduce launch is needed.
 //
 // Tile layout in shared memory: a (block, head) tile is [16 tokens][row bytes]
 // (split into two [16][128-byte] halves when a row is 256 bytes) with the
@@ -141,6 +144,7 @@ __global__ void __launch_bounds__(NTW == 1 ? 96 : 160, NTW == 1 ? 5 : 2)
   long long* red = reinterpret_cast<long long*>(smem + lay.misc);   // [10] block-reduce scratch
   long long* plan = red + 10;                                      // total, b0, b1, s0, cum0
   volatile int* abort_flag = reinterpret_cast<volatile int*>(plan + 5);
+  volatile int* fin = reinterpret_cast<volatile int*>(plan + 6);   // is_last, first CTA, last CTA
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nwarps = blockDim.x >> 5;
@@ -247,13 +251,6 @@ __global__ void __launch_bounds__(NTW == 1 ? 96 : 160, NTW == 1 ? 5 : 2)
     bool ok = true;
     while (gpos < b1 && ok) {
       const int take = static_cast<int>(min(static_cast<long long>(nb - lb), b1 - gpos));
-      if (lb == 0 && lane == 0) {
-        // This CTA owns the unit's first block: record which CTAs cover the unit.
-        const long long nact = ncta < total ? ncta : total;
-        const long long last_blk = gpos + nb - 1;
-        const int last_cta = static_cast<int>(((last_blk + 1) * nact - 1) / total);
-        a.unit_desc[s * Hkv + h] = make_int2(static_cast<int>(cta), last_cta);
-      }
       const int32_t* bt = a.block_tables + static_cast<size_t>(s) * mbs + lb;
       int nxt = (lane < take) ? bt[lane] : 0;
       for (int k0 = 0; k0 < take && ok; k0 += 32) {
@@ -628,6 +625,64 @@ __global__ void __launch_bounds__(NTW == 1 ? 96 : 160, NTW == 1 ? 5 : 2)
       }
     }
 
+    if (split) {
+      // Count this piece; the CTA finishing the unit's last piece combines them.
+      __threadfence();
+      named_bar_sync(3, nthr_c);
+      if (tid == 0) {
+        const long long nact = ncta < total ? ncta : total;
+        const long long ustart = gpos - lb;                       // unit's first global block
+        const int c_first = static_cast<int>(((ustart + 1) * nact - 1) / total);
+        const int c_last = static_cast<int>(((ustart + nb) * nact - 1) / total);
+        unsigned long long* ctr = a.piece_counts + u;
+        unsigned long long cur = atomicAdd(ctr, 0ull);
+        unsigned long long want;
+        for (;;) {
+          want = (static_cast<uint32_t>(cur >> 32) == a.epoch)
+                     ? cur + 1ull
+                     : ((static_cast<unsigned long long>(a.epoch) << 32) | 1ull);
+          const unsigned long long prev = atomicCAS(ctr, cur, want);
+          if (prev == cur) break;
+          cur = prev;
+        }
+        fin[0] = (static_cast<int>(want & 0xffffffffull) == c_last - c_first + 1) ? 1 : 0;
+        fin[1] = c_first;
+        fin[2] = c_last;
+        __threadfence();
+      }
+      named_bar_sync(3, nthr_c);
+      if (fin[0]) {
+        const int c_first = fin[1], c_last = fin[2];
+        const int ooff = partial_o_offset(R);
+        for (int idx = tid; idx < R * (D / 4); idx += nthr_c) {
+          const int r = idx / (D / 4), d4 = idx - (idx / (D / 4)) * (D / 4);
+          float M = kNegInf;
+          for (int c = c_first; c <= c_last; ++c)
+            M = fmaxf(M, __ldcg(a.partials + static_cast<size_t>(u + c) * a.slot_floats + r));
+          const float Mu = (M == kNegInf) ? 0.f : M;
+          float lsum = 0.f;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int c = c_first; c <= c_last; ++c) {
+            const float* P = a.partials + static_cast<size_t>(u + c) * a.slot_floats;
+            const float f = fast_exp2(__ldcg(P + r) - Mu);
+            lsum += f * __ldcg(P + R + r);
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(P + ooff + r * D + d4 * 4));
+            acc.x += f * v.x;
+            acc.y += f * v.y;
+            acc.z += f * v.z;
+            acc.w += f * v.w;
+          }
+          const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+          const int j = r / G, gi = r - j * G;
+          const size_t dst = (static_cast<size_t>(s * n + j) * Hq + h * G + gi) * D + d4 * 4;
+          uint2 pk;
+          pk.x = pack_p<KV>(acc.x * inv, acc.y * inv);
+          pk.y = pack_p<KV>(acc.z * inv, acc.w * inv);
+          *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + dst) = pk;
+        }
+      }
+    }
+
     // ---- advance the walk ----
     gpos += take;
     lb += take;
@@ -642,52 +697,6 @@ __global__ void __launch_bounds__(NTW == 1 ? 96 : 160, NTW == 1 ? 5 : 2)
         }
       }
     }
-  }
-}
-
-// Combine the partial pieces of every (sequence, KV head) unit that more than
-// one CTA covered: M = max m_c, L = sum l_c 2^(m_c - M), out = sum o_c 2^(m_c - M) / L.
-template <int KV>
-__global__ void __launch_bounds__(128) reduce_kernel(const ReduceArgs a) {
-  constexpr float kNegInf = -INFINITY;
-  pdl_wait_prior_grid();
-  const int u = blockIdx.x;
-  const int2 dsc = a.unit_desc[u];
-  if (dsc.x >= dsc.y) return;   // one CTA covered the unit and wrote its output
-  if (dsc.x < 0 || dsc.y >= a.num_ctas) {
-    // Only possible if the decode kernel gave up before describing this unit.
-    if (threadIdx.x == 0 && a.status) atomicOr(a.status, kDevTimeout);
-    return;
-  }
-  const int s = u / a.num_kv_heads, h = u - s * a.num_kv_heads;
-  const int R = a.rows, D = a.head_size, G = a.group;
-  const int ooff = partial_o_offset(R);
-  for (int idx = threadIdx.x; idx < R * (D / 4); idx += blockDim.x) {
-    const int r = idx / (D / 4), d4 = idx - r * (D / 4);
-    float M = kNegInf;
-    for (int c = dsc.x; c <= dsc.y; ++c) {
-      M = fmaxf(M, a.partials[static_cast<size_t>(u + c) * a.slot_floats + r]);
-    }
-    const float Mu = (M == kNegInf) ? 0.f : M;
-    float lsum = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c = dsc.x; c <= dsc.y; ++c) {
-      const float* P = a.partials + static_cast<size_t>(u + c) * a.slot_floats;
-      const float f = fast_exp2(P[r] - Mu);
-      lsum += f * P[R + r];
-      const float4 v = *reinterpret_cast<const float4*>(P + ooff + r * D + d4 * 4);
-      acc.x += f * v.x;
-      acc.y += f * v.y;
-      acc.z += f * v.z;
-      acc.w += f * v.w;
-    }
-    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-    const int j = r / G, gi = r - j * G;
-    const size_t dst = (static_cast<size_t>(s * a.q_per_seq + j) * a.num_q_heads + h * G + gi) * D + d4 * 4;
-    uint2 pk;
-    pk.x = pack_p<KV>(acc.x * inv, acc.y * inv);
-    pk.y = pack_p<KV>(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + dst) = pk;
   }
 }
 

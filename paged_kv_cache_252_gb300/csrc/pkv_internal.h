@@ -26,7 +26,7 @@ struct DecodeArgs {
   const int32_t* block_tables; // [S][max_blocks_per_seq]
   const int32_t* context_lens; // [S]
   float* partials;             // split-KV partial slots
-  int2* unit_desc;             // [S*Hkv]: (first CTA, last CTA) covering the unit
+  unsigned long long* piece_counts;  // [S*Hkv]: (call epoch << 32) | pieces finished
   int32_t* status;             // optional device status word
   int32_t num_seqs;
   int32_t num_q_heads;
@@ -41,22 +41,9 @@ struct DecodeArgs {
   int32_t stages;              // depth of the shared-memory ring
   int32_t slot_floats;         // floats per partial slot
   float scale_log2;            // softmax scale * log2(e)
+  uint32_t epoch;              // distinct for every call (tags the piece counters)
 };
 
-struct ReduceArgs {
-  void* out;
-  const float* partials;
-  const int2* unit_desc;
-  int32_t num_kv_heads;
-  int32_t num_q_heads;
-  int32_t q_per_seq;
-  int32_t group;
-  int32_t rows;
-  int32_t head_size;
-  int32_t slot_floats;
-  int32_t num_ctas;            // grid of the decode launch (bounds the descriptor range)
-  int32_t* status;
-};
 
 // Shared-memory and launch geometry of one decode instantiation.
 struct DecodeGeometry {
@@ -104,9 +91,6 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int kv, int d, int ntw,
 const void* decode_kernel_ptr_f16(int d, int ntw);
 const void* decode_kernel_ptr_bf16(int d, int ntw);
 const void* decode_kernel_ptr_e5m2(int d, int ntw);
-const void* reduce_kernel_ptr_f16();
-const void* reduce_kernel_ptr_bf16();
-const void* reduce_kernel_ptr_e5m2();
 const void* kv_cache_write_kernel_ptr();
 
 struct CacheWriteArgs {
