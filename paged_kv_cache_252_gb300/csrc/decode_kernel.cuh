@@ -500,15 +500,22 @@ __global__ void __launch_bounds__(NTW == 1 ? 96 : 160, NTW == 1 ? 5 : 2)
             pb_lo[nt][1] = movmatrix_t(l23);
           }
         }
+        // alpha is exactly 1 for a row whose running max did not change; once the
+        // max settles that holds for the whole warp and the rescale is skipped.
+        bool rescale = false;
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
+        for (int nt = 0; nt < NTW; ++nt) rescale |= (alpha[nt][0] != 1.f) | (alpha[nt][1] != 1.f);
+        if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-          for (int nt = 0; nt < NTW; ++nt) {
-            o_acc[mt][nt][0] *= alpha[nt][0];
-            o_acc[mt][nt][1] *= alpha[nt][1];
-            o_acc[mt][nt][2] *= alpha[nt][0];
-            o_acc[mt][nt][3] *= alpha[nt][1];
-          }
+          for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NTW; ++nt) {
+              o_acc[mt][nt][0] *= alpha[nt][0];
+              o_acc[mt][nt][1] *= alpha[nt][1];
+              o_acc[mt][nt][2] *= alpha[nt][0];
+              o_acc[mt][nt][3] *= alpha[nt][1];
+            }
+        }
 
         // ---- O^T (head_size x rows) += V^T P^T ----
         {
@@ -627,9 +634,11 @@ __global__ void __launch_bounds__(NTW == 1 ? 96 : 160, NTW == 1 ? 5 : 2)
 
     if (split) {
       // Count this piece; the CTA finishing the unit's last piece combines them.
-      __threadfence();
+      // The barrier orders every consumer thread's slot writes before thread 0's
+      // device-scope fence, which makes them visible before the counter update.
       named_bar_sync(3, nthr_c);
       if (tid == 0) {
+        __threadfence();
         const long long nact = ncta < total ? ncta : total;
         const long long ustart = gpos - lb;                       // unit's first global block
         const int c_first = static_cast<int>(((ustart + 1) * nact - 1) / total);
