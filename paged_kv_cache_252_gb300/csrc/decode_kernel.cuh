@@ -179,51 +179,49 @@ __global__ void __launch_bounds__(NTW == 1 ? 96 : 160, NTW == 1 ? 5 : 2)
   const long long ncta = gridDim.x, cta = blockIdx.x;
 
   // ---- plan: this CTA's share [b0, b1) of all (sequence, head, block) triples ----
+  // One pass over context_lens: thread t owns a contiguous run of sequences,
+  // a block-wide scan of the runs' block counts gives the total and every run's
+  // offset, and the thread whose run holds block b0 finds its sequence.
   {
-    long long local = 0;
-    for (int s = tid; s < S; s += blockDim.x) local += unit_blocks(a.context_lens[s], mbs);
-    local = warp_sum_ll(local);
-    if (lane == 0) red[warp] = local;
+    const int per = (S + blockDim.x - 1) / blockDim.x;
+    const int s_lo = tid * per;
+    const int s_hi = s_lo + per < S ? s_lo + per : S;
+    long long mine = 0;
+    for (int s = s_lo; s < s_hi; ++s) mine += unit_blocks(a.context_lens[s], mbs);
+    mine *= Hkv;
+    long long v = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long t = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += t;
+    }
+    if (lane == 31) red[warp] = v;
+    if (tid == 0) plan[3] = -1;
     __syncthreads();
-    long long tot = 0;
-    for (int w = 0; w < nwarps; ++w) tot += red[w];
-    tot *= Hkv;
+    long long pre = 0, tot = 0;
+    for (int w = 0; w < nwarps; ++w) {
+      if (w < warp) pre += red[w];
+      tot += red[w];
+    }
+    const long long excl = pre + v - mine;
     // Only min(grid, total) CTAs take work, so every active CTA owns at least one
     // block and every CTA between a unit's first and last owner wrote a piece of it.
     const long long nact = ncta < tot ? ncta : tot;
     const long long b0 = cta < nact ? cta * tot / nact : tot;
     const long long b1 = cta < nact ? (cta + 1) * tot / nact : tot;
-    __syncthreads();
-    if (tid == 0) { plan[0] = tot; plan[1] = b0; plan[2] = b1; plan[3] = -1; plan[4] = 0; }
-    if (b0 < b1) {
-      // Locate the sequence holding global block b0 with a block-wide scan.
-      long long carry = 0;
-      for (int base = 0; base < S; base += blockDim.x) {
-        const int s = base + tid;
-        const long long wblk = (s < S) ? (long long)Hkv * unit_blocks(a.context_lens[s], mbs) : 0;
-        long long v = wblk;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const long long t = __shfl_up_sync(0xffffffffu, v, o);
-          if (lane >= o) v += t;
-        }
-        if (lane == 31) red[warp] = v;
-        __syncthreads();
-        long long pre = 0, all = 0;
-        for (int w = 0; w < nwarps; ++w) {
-          if (w < warp) pre += red[w];
-          all += red[w];
-        }
-        const long long incl = v + pre, excl = incl - wblk;
-        if (s < S && carry + excl <= b0 && b0 < carry + incl) {
+    if (b0 < b1 && excl <= b0 && b0 < excl + mine) {
+      long long cum = excl;
+      for (int s = s_lo; s < s_hi; ++s) {
+        const long long wblk = static_cast<long long>(Hkv) * unit_blocks(a.context_lens[s], mbs);
+        if (b0 < cum + wblk) {
           plan[3] = s;
-          plan[4] = (carry + excl) / Hkv;
+          plan[4] = cum / Hkv;
+          break;
         }
-        carry += all;
-        __syncthreads();
-        if (carry > b0) break;
+        cum += wblk;
       }
     }
+    if (tid == 0) { plan[0] = tot; plan[1] = b0; plan[2] = b1; }
     __syncthreads();
   }
   pdl_launch_dependents();
