@@ -10,7 +10,7 @@ decode attention over every sequence's blocks (decode kernel + split-KV reduce).
 
 Workloads (seeded, synthetic; see paged_kv_cache_252_gb300/workloads.py):
   tiny, 8b (default: Llama-3-8B-shaped decode layer, batch 64, fp16 KV),
-  8b_fp8, long, 70b_spec.
+  8b_fp8, long, 70b_spec, mixed (decode + 4-token verify rows packed together).
 
 value  = algorithmic bytes of the step / device time per step (GB/s), inputs
          resident in HBM. Algorithmic bytes: every visible token's K and V once,
@@ -212,16 +212,23 @@ def run_ours(args, rank, world, local):
     s_new = vals["slot_all"][new_idx].contiguous()
     bt = torch.from_numpy(w.block_tables).to(dev)
     cl = torch.from_numpy(w.context_lens).to(dev)
+    cu = torch.from_numpy(w.cu_q_lens()).to(dev) if w.q_lens is not None else None
     qs = [vals["q"].clone() for _ in range(pools)]
     outs = [torch.empty_like(vals["q"]) for _ in range(pools)]
     del vals
     torch.cuda.synchronize(dev)
 
+    def decode(o, q, kc, vc, bt_, cl_, cu_):
+        if cu_ is not None:
+            pkv.paged_attention_decode_varlen(o, q, cu_, kc, vc, bt_, cl_, w.q_per_seq, w.scale)
+        else:
+            pkv.paged_attention_decode(o, q, kc, vc, bt_, cl_, w.q_per_seq, w.scale)
+
     def step(i):
         p = i % pools
         kc, vc = caches[p]
         pkv.kv_cache_write(k_new, v_new, s_new, kc, vc)
-        pkv.paged_attention_decode(outs[p], qs[p], kc, vc, bt, cl, w.q_per_seq, w.scale)
+        decode(outs[p], qs[p], kc, vc, bt, cl, cu)
 
     step_bytes = kv_bytes + w.q_out_bytes() + w.write_bytes()
     attn_bytes = kv_bytes + w.q_out_bytes()
@@ -253,7 +260,7 @@ def run_ours(args, rank, world, local):
         p = i % pools
         kc, vc = caches[p]
         evs[i][0].record()
-        pkv.paged_attention_decode(outs[p], qs[p], kc, vc, bt, cl, w.q_per_seq, w.scale)
+        decode(outs[p], qs[p], kc, vc, bt, cl, cu)
         evs[i][1].record()
     torch.cuda.synchronize(dev)
     dec_s = float(np.mean([a.elapsed_time(b) for a, b in evs])) / 1e3
@@ -261,11 +268,14 @@ def run_ours(args, rank, world, local):
     # End to end through the public API with pinned host buffers.
     e2e = None
     if not args.no_e2e:
-        host = {n: t.cpu().pin_memory() for n, t in
-                (("q", qs[0]), ("k_new", k_new), ("v_new", v_new), ("s_new", s_new), ("bt", bt), ("cl", cl))}
+        named = [("q", qs[0]), ("k_new", k_new), ("v_new", v_new), ("s_new", s_new), ("bt", bt), ("cl", cl)]
+        if cu is not None:
+            named.append(("cu", cu))
+        host = {n: t.cpu().pin_memory() for n, t in named}
         out_h = torch.empty(outs[0].shape, dtype=outs[0].dtype).pin_memory()
         dq, dk, dv = torch.empty_like(qs[0]), torch.empty_like(k_new), torch.empty_like(v_new)
         ds, dbt, dcl = torch.empty_like(s_new), torch.empty_like(bt), torch.empty_like(cl)
+        dcu = torch.empty_like(cu) if cu is not None else None
         h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = out_h.numel() * out_h.element_size()
 
@@ -278,8 +288,10 @@ def run_ours(args, rank, world, local):
             ds.copy_(host["s_new"], non_blocking=True)
             dbt.copy_(host["bt"], non_blocking=True)
             dcl.copy_(host["cl"], non_blocking=True)
+            if dcu is not None:
+                dcu.copy_(host["cu"], non_blocking=True)
             pkv.kv_cache_write(dk, dv, ds, kc, vc)
-            pkv.paged_attention_decode(outs[p], dq, kc, vc, dbt, dcl, w.q_per_seq, w.scale)
+            decode(outs[p], dq, kc, vc, dbt, dcl, dcu)
             out_h.copy_(outs[p], non_blocking=True)
 
         for i in range(args.warmup):
@@ -323,7 +335,7 @@ def run_ours(args, rank, world, local):
                    f"{pools * kv_bytes / 1e9:.2f} GB per cycle > 4x L2 ({l2 / 1e6:.0f} MB)",
                    "parallelism": f"replicas x{world}"},
         "seq_steps_per_s": round(w.num_seqs * world * args.steps / job_elapsed, 1),
-        "tokens_per_s": round(w.num_seqs * w.q_per_seq * world * args.steps / job_elapsed, 1),
+        "tokens_per_s": round(w.num_new_tokens * world * args.steps / job_elapsed, 1),
         "pct_of_hbm_peak": round(100 * value / peak, 2),
         "roofline": {"bound": "hbm", "kernel": "paged_attention_decode (decode + split-KV reduce)",
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
@@ -375,15 +387,16 @@ def _oracle_step(w, inp, seqs, threads):
     qcode = 1 if w.q_dtype == "bf16" else 0
     _, _, rc = oracle.paged_attention(inp["q"], qcode, w.q_per_seq, inp["kc"], inp["vc"], inp["code"],
                                       w.block_tables, w.context_lens, w.scale, seqs=seqs,
-                                      num_threads=threads)
+                                      num_threads=threads,
+                                      cu_q_lens=w.cu_q_lens() if w.q_lens is not None else None)
     assert rc == 0
 
 
 def _sample_bytes(w, seqs):
     lens = w.context_lens[seqs].astype(np.int64)
     kv = int(lens.sum()) * w.num_kv_heads * w.head_size * 2 * w.kv_elem_bytes
-    qo = 2 * len(seqs) * w.q_per_seq * w.num_q_heads * w.head_size * 2
-    t = len(seqs) * w.q_per_seq
+    t = int(w.query_lens()[seqs].sum())
+    qo = 2 * t * w.num_q_heads * w.head_size * 2
     wr = t * w.num_kv_heads * w.head_size * (4 + w.kv_elem_bytes) + 4 * t
     return kv + qo + wr
 
@@ -457,7 +470,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--config", default="8b", choices=["tiny", "8b", "8b_fp8", "long", "70b_spec"])
+    ap.add_argument("--config", default="8b", choices=["tiny", "8b", "8b_fp8", "long", "70b_spec", "mixed"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--pools", type=int, default=0, help="KV pools to rotate (default: >4x L2)")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)

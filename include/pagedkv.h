@@ -142,6 +142,33 @@ int pkv_paged_attention_decode(void* out, const void* q, int32_t num_seqs,
                                int32_t* device_status, void* stream);
 
 /*
+ * pkv_paged_attention_decode_varlen — the same attention for a batch whose
+ * sequences carry different numbers of query tokens: plain decode (1 token),
+ * speculative verify (several draft tokens) and short prefill chunks mixed in one
+ * launch, with the tokens packed without padding ("nopadding" 1-D input of the
+ * Continuous Batching section of the Colossal-Inference release page).
+ *
+ *   cu_q_lens     [num_seqs + 1] int32, device: sequence s owns query/output rows
+ *                 cu_q_lens[s] .. cu_q_lens[s+1]-1 (cu_q_lens[0] = 0); its
+ *                 n_s = cu_q_lens[s+1] - cu_q_lens[s] must be in [1, max_q_per_seq].
+ *                 A sequence outside that range gets no output rows and sets
+ *                 PKV_DEV_BAD_CTX.
+ *   out, q        [cu_q_lens[num_seqs]][num_q_heads][head_size].
+ *   max_q_per_seq sizes the per-unit row capacity: (num_q_heads/num_kv_heads) *
+ *                 max_q_per_seq <= 64; pkv_decode_workspace_bytes(num_seqs,
+ *                 num_q_heads, max_q_per_seq, cache) sizes the workspace.
+ *   Query token j of sequence s sees positions p <= context_lens[s] - n_s + j.
+ *   Everything else is as for pkv_paged_attention_decode.
+ */
+int pkv_paged_attention_decode_varlen(void* out, const void* q, const int32_t* cu_q_lens,
+                                      int32_t num_seqs, int32_t num_q_heads, int32_t max_q_per_seq,
+                                      const void* k_cache, const void* v_cache, pkv_dtype kv_dtype,
+                                      const pkv_cache_desc* cache, const int32_t* block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                      float scale, void* workspace, size_t workspace_bytes,
+                                      int32_t* device_status, void* stream);
+
+/*
  * pkv_paged_attention_decode_noalloc — the same decode attention as
  * pkv_paged_attention_decode, for callers that cannot allocate device memory
  * when they run it (for example code running inside a custom allocator's

@@ -265,8 +265,10 @@ int orc_kv_cache_write(const uint16_t* key, const uint16_t* value, int src_dtype
 
 // Paged decode attention, fp64.
 //
-// q: [num_seqs * q_per_seq][num_q_heads][head_size] in q_dtype (fp16/bf16);
-//    row s*q_per_seq + j is query token j of sequence s.
+// q: [rows][num_q_heads][head_size] in q_dtype (fp16/bf16). With cu_q_lens NULL,
+//    sequence s has q_per_seq query tokens in rows s*q_per_seq + j; otherwise it
+//    has cu_q_lens[s+1] - cu_q_lens[s] tokens in rows cu_q_lens[s] + j (the
+//    unpadded mixed batch of the Colossal-Inference Continuous Batching section).
 // out: same layout, fp64, unnormalised nothing: out = sum_p w_p V_p.
 // weights (optional, may be NULL): [num_seqs*q_per_seq][num_q_heads][weights_stride],
 //    w_p for p < limit, 0 elsewhere.
@@ -281,10 +283,13 @@ int orc_paged_attention(double* out, double* weights, int64_t weights_stride,
                         int kv_dtype, int num_blocks, int block_size, int num_kv_heads,
                         int head_size, const int32_t* block_tables,
                         int max_blocks_per_seq, const int32_t* context_lens, double scale,
-                        const int32_t* seq_subset, int n_subset, int num_threads) {
+                        const int32_t* seq_subset, int n_subset, int num_threads,
+                        const int32_t* cu_q_lens) {
   if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return -1;
   const int group = num_q_heads / num_kv_heads;
-  const int n = q_per_seq;
+  // Query tokens and first query row of sequence s.
+  auto tokens_of = [&](int s) { return cu_q_lens ? cu_q_lens[s + 1] - cu_q_lens[s] : q_per_seq; };
+  auto first_row = [&](int s) { return cu_q_lens ? (int64_t)cu_q_lens[s] : (int64_t)s * q_per_seq; };
 
   std::vector<int32_t> seqs;
   if (seq_subset) {
@@ -296,7 +301,7 @@ int orc_paged_attention(double* out, double* weights, int64_t weights_stride,
   struct Row { int s, j, hq; };
   std::vector<Row> rows;
   for (int s : seqs)
-    for (int j = 0; j < n; ++j)
+    for (int j = 0; j < tokens_of(s); ++j)
       for (int hq = 0; hq < num_q_heads; ++hq) rows.push_back({s, j, hq});
 
   std::vector<int> bad(std::max(1, num_threads), 0);
@@ -307,7 +312,8 @@ int orc_paged_attention(double* out, double* weights, int64_t weights_stride,
       const int s = r.s, j = r.j, hq = r.hq;
       const int h = hq / group;  // KV head of this query head
       const int ctx = context_lens[s];
-      const int64_t qrow = ((int64_t)s * n + j) * num_q_heads + hq;
+      const int n = tokens_of(s);
+      const int64_t qrow = (first_row(s) + j) * num_q_heads + hq;
       double* o = out + qrow * head_size;
       // Query token j is position ctx - n + j; it sees positions 0..ctx-n+j.
       const int limit = ctx - n + j + 1;

@@ -59,6 +59,10 @@ def load_library():
             vp, vp, i32, i32, i32, vp, vp, ctypes.c_int, P(_CacheDesc), vp, i32, vp,
             ctypes.c_float, vp, ctypes.c_size_t, vp, vp]
         lib.pkv_paged_attention_decode.restype = ctypes.c_int
+        lib.pkv_paged_attention_decode_varlen.argtypes = [
+            vp, vp, vp, i32, i32, i32, vp, vp, ctypes.c_int, P(_CacheDesc), vp, i32, vp,
+            ctypes.c_float, vp, ctypes.c_size_t, vp, vp]
+        lib.pkv_paged_attention_decode_varlen.restype = ctypes.c_int
         lib.pkv_paged_attention_decode_noalloc.argtypes = [
             vp, vp, i32, i32, i32, vp, vp, ctypes.c_int, P(_CacheDesc), vp, i32, vp,
             ctypes.c_float, vp, vp]
@@ -212,4 +216,38 @@ def paged_attention_decode_noalloc(out, q, k_cache, v_cache, block_tables, conte
             _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens), float(scale),
             _ptr(device_status), _stream_handle(stream, q.device))
     _check(rc, "paged_attention_decode_noalloc")
+    return out
+
+
+def paged_attention_decode_varlen(out, q, cu_q_lens, k_cache, v_cache, block_tables, context_lens,
+                                  max_q_per_seq: int, scale: float, kv_dtype=None, *,
+                                  workspace=None, device_status=None, stream=None):
+    """Decode attention for a batch whose sequences carry different numbers of query
+    tokens, packed without padding: sequence s owns rows cu_q_lens[s]..cu_q_lens[s+1]-1
+    of q/out ([total_rows, Hq, D]), 1 <= n_s <= max_q_per_seq, causal among its tokens."""
+    for nm, t in (("out", out), ("q", q), ("cu_q_lens", cu_q_lens), ("k_cache", k_cache),
+                  ("v_cache", v_cache), ("block_tables", block_tables), ("context_lens", context_lens)):
+        _need_cuda_contig(nm, t)
+    if (block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32
+            or cu_q_lens.dtype != torch.int32):
+        raise PagedKVError("block_tables, context_lens and cu_q_lens must be int32")
+    if out.dtype != q.dtype:
+        raise PagedKVError("out and q must share a dtype")
+    S = int(context_lens.shape[0])
+    if int(cu_q_lens.shape[0]) != S + 1:
+        raise PagedKVError("cu_q_lens must have num_seqs + 1 entries")
+    Hq = int(q.shape[1])
+    d = _desc(k_cache)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        need = int(lib.pkv_decode_workspace_bytes(S, Hq, int(max_q_per_seq), ctypes.byref(d)))
+        if workspace is None:
+            workspace = _workspace(need, q.device)
+        rc = lib.pkv_paged_attention_decode_varlen(
+            _ptr(out), _ptr(q), _ptr(cu_q_lens), S, Hq, int(max_q_per_seq), _ptr(k_cache),
+            _ptr(v_cache), _kv_code(kv_dtype, k_cache), ctypes.byref(d), _ptr(block_tables),
+            int(block_tables.shape[1]), _ptr(context_lens), float(scale), _ptr(workspace),
+            int(workspace.numel() * workspace.element_size()), _ptr(device_status),
+            _stream_handle(stream, q.device))
+    _check(rc, "paged_attention_decode_varlen")
     return out

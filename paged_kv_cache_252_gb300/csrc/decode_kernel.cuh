@@ -327,16 +327,28 @@ __global__ void __launch_bounds__(NTW == 1 ? 96 : 160, NTW == 1 ? 5 : 2)
     const int u = s * Hkv + h;
     const int cap = mbs * kBlockSize;
     const int ctx_eff = ctx < cap ? ctx : cap;
-    if (first && warp == 0 && lane == 0 && (ctx < n || ctx > cap) && a.status) {
+    // Query tokens of sequence s: n_s of them, rows qb.. of q/out ("nopadding"
+    // packed tokens). With cu_q_lens a sequence may carry fewer than q_per_seq;
+    // a count outside [1, q_per_seq] is flagged and the sequence gets no rows.
+    int n_s = n, qb = s * n;
+    if (a.cu_q_lens) {
+      qb = a.cu_q_lens[s];
+      n_s = a.cu_q_lens[s + 1] - qb;
+    }
+    const bool rows_ok = n_s >= 1 && n_s <= n;
+    const int Rs = rows_ok ? G * n_s : 0;          // real rows of this unit
+    if (!rows_ok) n_s = 1;
+    if (first && warp == 0 && lane == 0 && (!rows_ok || ctx < n_s || ctx > cap) && a.status) {
       atomicOr(a.status, kDevBadCtx);
     }
 
     // Query rows of this unit -> shared memory. Row r = j*G + gi is query token j,
-    // query head h*G + gi.
-    for (int idx = tid; idx < R * (D / 8); idx += nthr_c) {
+    // query head h*G + gi. Rows past Rs keep stale finite values; every row is an
+    // independent column of S and O, and only rows below Rs are written out.
+    for (int idx = tid; idx < Rs * (D / 8); idx += nthr_c) {
       const int r = idx / (D / 8), ch = idx % (D / 8);
       const int j = r / G, gi = r - j * G;
-      const size_t src = (static_cast<size_t>(s * n + j) * Hq + h * G + gi) * D + ch * 8;
+      const size_t src = (static_cast<size_t>(qb + j) * Hq + h * G + gi) * D + ch * 8;
       *reinterpret_cast<uint4*>(qs + r * QS + ch * 16) =
           *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) + src);
     }
@@ -377,7 +389,7 @@ __global__ void __launch_bounds__(NTW == 1 ? 96 : 160, NTW == 1 ? 5 : 2)
         l_run[nt][e] = 0.f;
         const int r = row_base + nt * 8 + 2 * c4 + e;
         const int j = r / G;
-        const int lj = ctx_eff - n + j;             // last visible position of token j
+        const int lj = ctx_eff - n_s + j;           // last visible position of token j
         lim[nt][e] = lj < ctx_eff - 1 ? lj : ctx_eff - 1;
       }
 #pragma unroll
@@ -452,7 +464,7 @@ __global__ void __launch_bounds__(NTW == 1 ? 96 : 160, NTW == 1 ? 5 : 2)
         }
 
         // ---- online softmax (base 2) over this block ----
-        const bool masked = tok0 + (kBlockSize - 1) > ctx_eff - n;
+        const bool masked = tok0 + (kBlockSize - 1) > ctx_eff - n_s;
         const int p_lo = tok0 + g8, p_hi = p_lo + 8;
         uint32_t pb[NTW][2];
         uint32_t pb_lo[NTW][2];   // bf16 only: P - bf16(P), a second bf16 term
@@ -595,7 +607,7 @@ __global__ void __launch_bounds__(NTW == 1 ? 96 : 160, NTW == 1 ? 5 : 2)
       }
     }
     named_bar_sync(2, nthr_c);
-    for (int idx = tid; idx < R * (D / 4); idx += nthr_c) {
+    for (int idx = tid; idx < Rs * (D / 4); idx += nthr_c) {
       const int r = idx / (D / 4), d4 = idx - (idx / (D / 4)) * (D / 4);
       float M = kNegInf;
       for (int w = 0; w < WB; ++w) M = fmaxf(M, mrg_m[w * R + r]);
@@ -615,7 +627,7 @@ __global__ void __launch_bounds__(NTW == 1 ? 96 : 160, NTW == 1 ? 5 : 2)
       if (!split) {
         const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
         const int j = r / G, gi = r - j * G;
-        const size_t dst = (static_cast<size_t>(s * n + j) * Hq + h * G + gi) * D + d4 * 4;
+        const size_t dst = (static_cast<size_t>(qb + j) * Hq + h * G + gi) * D + d4 * 4;
         uint2 pk;
         pk.x = pack_p<KV>(acc.x * inv, acc.y * inv);
         pk.y = pack_p<KV>(acc.z * inv, acc.w * inv);
@@ -661,7 +673,7 @@ __global__ void __launch_bounds__(NTW == 1 ? 96 : 160, NTW == 1 ? 5 : 2)
       if (fin[0]) {
         const int c_first = fin[1], c_last = fin[2];
         const int ooff = partial_o_offset(R);
-        for (int idx = tid; idx < R * (D / 4); idx += nthr_c) {
+        for (int idx = tid; idx < Rs * (D / 4); idx += nthr_c) {
           const int r = idx / (D / 4), d4 = idx - (idx / (D / 4)) * (D / 4);
           float M = kNegInf;
           for (int c = c_first; c <= c_last; ++c)
@@ -681,7 +693,7 @@ __global__ void __launch_bounds__(NTW == 1 ? 96 : 160, NTW == 1 ? 5 : 2)
           }
           const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
           const int j = r / G, gi = r - j * G;
-          const size_t dst = (static_cast<size_t>(s * n + j) * Hq + h * G + gi) * D + d4 * 4;
+          const size_t dst = (static_cast<size_t>(qb + j) * Hq + h * G + gi) * D + d4 * 4;
           uint2 pk;
           pk.x = pack_p<KV>(acc.x * inv, acc.y * inv);
           pk.y = pack_p<KV>(acc.z * inv, acc.w * inv);

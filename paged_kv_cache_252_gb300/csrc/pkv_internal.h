@@ -25,15 +25,16 @@ struct DecodeArgs {
   const void* q;               // same layout
   const int32_t* block_tables; // [S][max_blocks_per_seq]
   const int32_t* context_lens; // [S]
+  const int32_t* cu_q_lens;    // [S+1] query-token offsets, or null: q_per_seq tokens each
   float* partials;             // split-KV partial slots
   unsigned long long* piece_counts;  // [S*Hkv]: (call epoch << 32) | pieces finished
   int32_t* status;             // optional device status word
   int32_t num_seqs;
   int32_t num_q_heads;
   int32_t num_kv_heads;
-  int32_t q_per_seq;
+  int32_t q_per_seq;           // query tokens per sequence (the maximum when cu_q_lens is set)
   int32_t group;               // Hq / Hkv
-  int32_t rows;                // group * q_per_seq (rows of one (seq, KV head) unit)
+  int32_t rows;                // group * q_per_seq (row capacity of one (seq, KV head) unit)
   int32_t max_blocks_per_seq;
   int32_t num_blocks;
   int32_t warps_rows;          // consumer warps splitting the rows

@@ -34,9 +34,14 @@ def main(argv=None):
     cl = torch.from_numpy(w.context_lens).to(dev)
     out = torch.empty_like(vals["q"])
     status = torch.zeros(1, dtype=torch.int32, device=dev)
+    cu = torch.from_numpy(w.cu_q_lens()).to(dev) if w.q_lens is not None else None
     for _ in range(args.iters):
-        api.paged_attention_decode(out, vals["q"], kc, vc, bt, cl, w.q_per_seq, w.scale,
-                                   device_status=status)
+        if cu is not None:
+            api.paged_attention_decode_varlen(out, vals["q"], cu, kc, vc, bt, cl, w.q_per_seq,
+                                              w.scale, device_status=status)
+        else:
+            api.paged_attention_decode(out, vals["q"], kc, vc, bt, cl, w.q_per_seq, w.scale,
+                                       device_status=status)
     torch.cuda.synchronize()
     print(f"{w.name}: {w.num_seqs} seqs, {w.kv_bytes_read() / 1e6:.1f} MB KV per call, "
           f"status {int(status.item())}")

@@ -44,6 +44,7 @@ class Workload:
     block_tables: np.ndarray            # int32 [S, max_blocks]; -1 past a sequence's blocks
     notes: str = ""
     extra: dict = field(default_factory=dict)
+    q_lens: np.ndarray | None = None    # int32 [S] query tokens per sequence (None: q_per_seq each)
 
     # ---- derived --------------------------------------------------------------
     @property
@@ -72,7 +73,19 @@ class Workload:
 
     @property
     def num_new_tokens(self) -> int:
-        return self.num_seqs * self.q_per_seq
+        return int(self.query_lens().sum())
+
+    def query_lens(self) -> np.ndarray:
+        """Query tokens of every sequence (q_per_seq each unless q_lens is set)."""
+        if self.q_lens is not None:
+            return self.q_lens.astype(np.int32)
+        return np.full(self.num_seqs, self.q_per_seq, dtype=np.int32)
+
+    def cu_q_lens(self) -> np.ndarray:
+        """Row offsets of each sequence's query tokens in the packed q/out ([S+1])."""
+        c = np.zeros(self.num_seqs + 1, dtype=np.int32)
+        np.cumsum(self.query_lens(), out=c[1:])
+        return c
 
     def seq_starts(self) -> np.ndarray:
         """Start of each sequence in the packed all-token arrays."""
@@ -96,10 +109,11 @@ class Workload:
         return out
 
     def new_token_index(self) -> np.ndarray:
-        """Indices (into the packed all-token arrays) of the q_per_seq newest tokens of each sequence."""
+        """Indices (into the packed all-token arrays) of each sequence's newest tokens
+        (its query tokens, which the step writes into the cache)."""
         starts = self.seq_starts()
-        n = self.q_per_seq
-        idx = [np.arange(starts[s + 1] - n, starts[s + 1]) for s in range(self.num_seqs)]
+        ql = self.query_lens()
+        idx = [np.arange(starts[s + 1] - ql[s], starts[s + 1]) for s in range(self.num_seqs)]
         return np.concatenate(idx).astype(np.int64)
 
     def kv_bytes_read(self) -> int:
@@ -107,7 +121,7 @@ class Workload:
         return int(self.num_tokens_total * self.num_kv_heads * self.head_size * 2 * self.kv_elem_bytes)
 
     def q_out_bytes(self) -> int:
-        return int(2 * self.num_seqs * self.q_per_seq * self.num_q_heads * self.head_size * 2)
+        return int(2 * self.num_new_tokens * self.num_q_heads * self.head_size * 2)
 
     def write_bytes(self) -> int:
         """Algorithmic bytes of the per-step cache write (read new K/V, write cache slots)."""
@@ -130,6 +144,7 @@ class Workload:
             "context_len_mean": float(self.context_lens.mean()),
             "context_len_min": int(self.context_lens.min()),
             "context_len_max": int(self.context_lens.max()),
+            "query_tokens": int(self.num_new_tokens),
             "num_blocks": self.num_blocks,
             "seed": self.seed,
         }
@@ -153,13 +168,18 @@ def _pool_and_tables(rng: np.random.Generator, context_lens: np.ndarray, pool_fa
 def make_workload(name: str, *, num_seqs: int, num_q_heads: int, num_kv_heads: int,
                   head_size: int, q_per_seq: int, kv_dtype: str, scale: float, seed: int,
                   context_lens, pool_factor: float = 1.25, min_pool: int = 0,
-                  notes: str = "") -> Workload:
+                  notes: str = "", q_lens=None) -> Workload:
     assert kv_dtype in KV_DTYPES
     rng = np.random.Generator(np.random.PCG64(seed + 7919))
     context_lens = np.asarray(context_lens, dtype=np.int32)
     num_blocks, tables = _pool_and_tables(rng, context_lens, pool_factor, min_pool)
+    if q_lens is not None:
+        q_lens = np.asarray(q_lens, dtype=np.int32)
+        assert q_lens.shape == (num_seqs,) and q_lens.min() >= 1
+        assert np.all(q_lens <= context_lens)
+        q_per_seq = int(q_lens.max())
     return Workload(name, num_seqs, num_q_heads, num_kv_heads, head_size, q_per_seq, kv_dtype,
-                    float(scale), seed, context_lens, num_blocks, tables, notes)
+                    float(scale), seed, context_lens, num_blocks, tables, notes, q_lens=q_lens)
 
 
 def _uniform_lens(seed, n, lo, hi):
@@ -225,12 +245,26 @@ def llama3_70b_spec4_e5m2(num_seqs: int = 128) -> Workload:
                          context_lens=_lognormal_lens(seed, num_seqs, 1024.0, 1.0, 4, 16384))
 
 
+def mixed_8b_decode_verify(num_seqs: int = 64) -> Workload:
+    """Continuous-batching mix on the 8B decode layer: each sequence carries 1 query
+    token (plain decode) or 4 (speculative verify), 3:1, packed without padding;
+    lengths uniform in [512, 2048], fp16 KV."""
+    seed = 258
+    rng = np.random.Generator(np.random.PCG64(seed))
+    q_lens = rng.choice(np.array([1, 1, 1, 4], dtype=np.int32), size=num_seqs)
+    return make_workload("mixed_8b_decode_verify_fp16", num_seqs=num_seqs, num_q_heads=32,
+                         num_kv_heads=8, head_size=128, q_per_seq=4, kv_dtype="fp16",
+                         scale=1.0 / math.sqrt(128), seed=seed,
+                         context_lens=_uniform_lens(seed, num_seqs, 512, 2048), q_lens=q_lens)
+
+
 NAMED = {
     "tiny": tiny,
     "8b": llama3_8b_bs64_fp16,
     "8b_fp8": llama3_8b_bs256_e5m2,
     "long": long_bs8_bf16,
     "70b_spec": llama3_70b_spec4_e5m2,
+    "mixed": mixed_8b_decode_verify,
 }
 
 
@@ -248,21 +282,22 @@ def reduced(w: Workload, *, num_seqs: int | None = None, ctx_scale: float = 1.0,
     if ctx_cap is not None:
         lens = np.minimum(lens, ctx_cap)
     lens = np.maximum(lens, w.q_per_seq).astype(np.int32)
+    q_lens = None if w.q_lens is None else w.q_lens[:S]
     return make_workload(w.name + name_suffix, num_seqs=S, num_q_heads=w.num_q_heads,
                          num_kv_heads=w.num_kv_heads, head_size=w.head_size,
                          q_per_seq=w.q_per_seq, kv_dtype=w.kv_dtype, scale=w.scale,
-                         seed=w.seed, context_lens=lens)
+                         seed=w.seed, context_lens=lens, q_lens=q_lens)
 
 
 def custom(*, num_seqs, num_q_heads, num_kv_heads, head_size, q_per_seq, kv_dtype,
            context_lens, seed=1000, scale=None, pool_factor=1.25, min_pool=0,
-           name="custom") -> Workload:
+           name="custom", q_lens=None) -> Workload:
     if scale is None:
         scale = 1.0 / math.sqrt(head_size)
     return make_workload(name, num_seqs=num_seqs, num_q_heads=num_q_heads,
                          num_kv_heads=num_kv_heads, head_size=head_size, q_per_seq=q_per_seq,
                          kv_dtype=kv_dtype, scale=scale, seed=seed, context_lens=context_lens,
-                         pool_factor=pool_factor, min_pool=min_pool)
+                         pool_factor=pool_factor, min_pool=min_pool, q_lens=q_lens)
 
 
 # ---- values ---------------------------------------------------------------------------
@@ -276,9 +311,9 @@ def token_values(w: Workload, device="cpu", *, chunk_tokens: int = 1 << 20):
 
     Returns a dict of torch tensors on ``device``:
       k_all, v_all : [T_total, Hkv, D]  source dtype (fp16, or bf16 for a bf16 cache)
-      q            : [S*n, Hq, D]        query dtype
+      q            : [rows, Hq, D]       query dtype (S*n rows, or sum(q_lens))
       slot_all     : [T_total] int32     physical slots (sequences packed in order)
-      new_idx      : [S*n] int64         which of the packed tokens are the step's new ones
+      new_idx      : [rows] int64        which of the packed tokens are the step's new ones
     """
     device = torch.device(device)
     gen = torch.Generator(device=device)
@@ -292,7 +327,7 @@ def token_values(w: Workload, device="cpu", *, chunk_tokens: int = 1 << 20):
         t1 = min(T, t0 + chunk_tokens)
         k_all[t0:t1] = _randn(gen, (t1 - t0, Hkv, D), device, src)
         v_all[t0:t1] = _randn(gen, (t1 - t0, Hkv, D), device, src)
-    q = _randn(gen, (w.num_seqs * w.q_per_seq, w.num_q_heads, D), device, w.torch_q_dtype)
+    q = _randn(gen, (w.num_new_tokens, w.num_q_heads, D), device, w.torch_q_dtype)
     slot_all = torch.from_numpy(w.slot_mapping_all()).to(device)
     new_idx = torch.from_numpy(w.new_token_index()).to(device)
     return {"k_all": k_all, "v_all": v_all, "q": q, "slot_all": slot_all, "new_idx": new_idx}

@@ -7,7 +7,7 @@ import torch
 
 import paged_kv_cache_252_gb300 as pkv
 from paged_kv_cache_252_gb300 import workloads as wl
-from _helpers import bits16, oracle_caches, oracle_attention
+from _helpers import bits16, oracle_caches, oracle_attention, query_rows
 
 ATOL, RTOL = 2e-3, 1e-2
 
@@ -31,7 +31,12 @@ def cuda_path(w, vals, dev, *, split_write=True, status=None):
     out = torch.full_like(q, float("nan"))
     bt = torch.from_numpy(w.block_tables).to(dev)
     cl = torch.from_numpy(w.context_lens).to(dev)
-    pkv.paged_attention_decode(out, q, kc, vc, bt, cl, w.q_per_seq, w.scale, device_status=status)
+    if w.q_lens is not None:
+        cu = torch.from_numpy(w.cu_q_lens()).to(dev)
+        pkv.paged_attention_decode_varlen(out, q, cu, kc, vc, bt, cl, w.q_per_seq, w.scale,
+                                          device_status=status)
+    else:
+        pkv.paged_attention_decode(out, q, kc, vc, bt, cl, w.q_per_seq, w.scale, device_status=status)
     torch.cuda.synchronize(dev)
     return kc, vc, out
 
@@ -76,6 +81,5 @@ def full_check(orc, w, dev, *, seqs=None, values_device="cpu", check_cache=True,
     assert rc == 0
     rows = None
     if seqs is not None:
-        n = w.q_per_seq
-        rows = np.concatenate([np.arange(s * n, (s + 1) * n) for s in seqs])
+        rows = query_rows(w, seqs)
     return compare(out, ref, rows)

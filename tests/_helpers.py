@@ -38,8 +38,16 @@ def oracle_caches(orc, w, vals, *, token_mask=None):
 
 def oracle_attention(orc, w, vals, kc, vc, **kw):
     q = bits16(vals["q"])
+    if w.q_lens is not None:
+        kw.setdefault("cu_q_lens", w.cu_q_lens())
     return orc.paged_attention(q, Q_CODE[w.q_dtype], w.q_per_seq, kc, vc, KV_CODE[w.kv_dtype],
                                w.block_tables, w.context_lens, w.scale, **kw)
+
+
+def query_rows(w, seqs):
+    """Rows of q/out that belong to the given sequences."""
+    cu = w.cu_q_lens()
+    return np.concatenate([np.arange(cu[s], cu[s + 1]) for s in seqs])
 
 
 def dense_kv_f64(w, vals, s):
@@ -56,10 +64,12 @@ def dense_kv_f64(w, vals, s):
 def sdpa_reference(w, vals, s):
     """Library reference for sequence s: torch SDPA in fp64 on contiguous K/V, GQA by
     repeating each KV head over its G query heads, causal among the n query tokens."""
-    n, G = w.q_per_seq, w.group
+    G = w.group
+    cu = w.cu_q_lens()
+    n = int(cu[s + 1] - cu[s])
     ctx = int(w.context_lens[s])
     k, v = dense_kv_f64(w, vals, s)                          # [ctx, Hkv, D]
-    q = vals["q"][s * n:(s + 1) * n].cpu().to(torch.float64)  # [n, Hq, D]
+    q = vals["q"][cu[s]:cu[s + 1]].cpu().to(torch.float64)   # [n, Hq, D]
     k = k.repeat_interleave(G, dim=1).permute(1, 0, 2)[None]  # [1, Hq, ctx, D]
     v = v.repeat_interleave(G, dim=1).permute(1, 0, 2)[None]
     qq = q.permute(1, 0, 2)[None]                              # [1, Hq, n, D]

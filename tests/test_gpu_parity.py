@@ -195,3 +195,54 @@ def test_workload_full_size_sampled_parity(orc, dev, gpu, key, k):
     compared; outputs of sampled sequences (longest, shortest, random) against the oracle."""
     w = wl.by_name(key)
     gpu.full_check(orc, w, dev, seqs=_sample(w, k), values_device=dev)
+
+
+# ------------------------------------------------------------------------------------
+# mixed batches (per-sequence query-token counts)
+# ------------------------------------------------------------------------------------
+
+VARLEN = [
+    # (kv, D, Hq, Hkv, q_lens)
+    ("fp16", 128, 32, 8, [1, 4, 1, 1, 4, 2, 1, 3]),
+    ("bf16", 64, 16, 4, [2, 1, 4, 1, 1, 3]),
+    ("e5m2", 128, 64, 8, [4, 1, 2, 4, 1]),
+    ("fp16", 64, 8, 1, [1, 8, 3, 1, 5, 2]),
+]
+
+
+@pytest.mark.parametrize("case", VARLEN, ids=[f"{c[0]}-D{c[1]}-G{c[2] // c[3]}" for c in VARLEN])
+def test_varlen_parity(orc, dev, gpu, case):
+    kv, D, Hq, Hkv, q_lens = case
+    lens = [max(l, ql) for l, ql in zip([1, 17, 300, 16, 64, 1000, 33, 129], q_lens)]
+    w = wl.custom(num_seqs=len(q_lens), num_q_heads=Hq, num_kv_heads=Hkv, head_size=D,
+                  q_per_seq=max(q_lens), kv_dtype=kv, context_lens=lens, seed=300 + D + Hq,
+                  q_lens=q_lens)
+    gpu.full_check(orc, w, dev)
+
+
+def test_mixed_workload_reduced(orc, dev, gpu):
+    gpu.full_check(orc, wl.reduced(wl.by_name("mixed"), num_seqs=12), dev)
+
+
+def test_mixed_workload_full_size_sampled(orc, dev, gpu):
+    w = wl.by_name("mixed")
+    gpu.full_check(orc, w, dev, seqs=_sample(w, 6), values_device=dev)
+
+
+def test_varlen_rejects_bad_counts_without_faulting(orc, dev, gpu):
+    import paged_kv_cache_252_gb300 as pkv
+    w = wl.custom(num_seqs=3, num_q_heads=4, num_kv_heads=2, head_size=64, q_per_seq=2,
+                  kv_dtype="fp16", context_lens=[20, 40, 9], seed=3, q_lens=[1, 2, 2])
+    vals = wl.token_values(w)
+    kc, vc, out = gpu.cuda_path(w, vals, dev)
+    cu = torch.tensor([0, 1, 4, 5], dtype=torch.int32, device=dev)   # sequence 1 claims 3 > max 2
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    q = vals["q"].to(dev)
+    out2 = torch.full_like(q, float("nan"))
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    cl = torch.from_numpy(w.context_lens).to(dev)
+    pkv.paged_attention_decode_varlen(out2, q, cu, kc, vc, bt, cl, 2, w.scale, device_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 0x4
+    assert torch.equal(out2[0], out[0])           # sequence 0 unaffected
+    assert torch.isnan(out2[1:4]).all()           # sequence 1 got no output rows

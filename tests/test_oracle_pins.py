@@ -379,3 +379,40 @@ def test_threads_do_not_change_results(orc):
     o1, _, _ = oracle_attention(orc, w, vals, kc, vc, num_threads=1)
     o4, _, _ = oracle_attention(orc, w, vals, kc, vc, num_threads=4)
     assert np.array_equal(o1, o4)
+
+
+# ---------------------------------------------------------------------------------
+# mixed batches: per-sequence query-token counts, packed without padding
+# ---------------------------------------------------------------------------------
+
+def test_varlen_matches_sdpa_and_per_sequence_runs(orc):
+    """A packed mixed batch (1..5 query tokens per sequence) equals torch SDPA per
+    sequence, and each sequence's rows equal a uniform run with its own token count."""
+    q_lens = [1, 5, 2, 1, 3]
+    w = wl.custom(num_seqs=5, num_q_heads=8, num_kv_heads=2, head_size=64, q_per_seq=5,
+                  kv_dtype="e5m2", context_lens=[7, 40, 16, 1, 90], seed=17, q_lens=q_lens)
+    vals = wl.token_values(w)
+    assert vals["q"].shape[0] == sum(q_lens)
+    kc, vc = oracle_caches(orc, w, vals)
+    out, _, rc = oracle_attention(orc, w, vals, kc, vc)
+    assert rc == 0
+    cu = w.cu_q_lens()
+    q = bits16(vals["q"])
+    for s in range(w.num_seqs):
+        np.testing.assert_allclose(out[cu[s]:cu[s + 1]], sdpa_reference(w, vals, s), rtol=1e-10, atol=1e-12)
+        one, _, rc = orc.paged_attention(np.ascontiguousarray(q[cu[s]:cu[s + 1]]), 0, q_lens[s], kc, vc,
+                                         KV_CODE["e5m2"], w.block_tables[s:s + 1], w.context_lens[s:s + 1],
+                                         w.scale)
+        assert rc == 0
+        assert np.array_equal(out[cu[s]:cu[s + 1]], one)
+
+
+def test_varlen_with_equal_counts_is_the_uniform_batch(orc):
+    w = wl.custom(num_seqs=3, num_q_heads=4, num_kv_heads=2, head_size=64, q_per_seq=2,
+                  kv_dtype="fp16", context_lens=[5, 33, 18], seed=23)
+    vals = wl.token_values(w)
+    kc, vc = oracle_caches(orc, w, vals)
+    uni, _, _ = oracle_attention(orc, w, vals, kc, vc)
+    var, _, rc = oracle_attention(orc, w, vals, kc, vc, cu_q_lens=np.array([0, 2, 4, 6], np.int32))
+    assert rc == 0
+    assert np.array_equal(uni, var)
