@@ -75,14 +75,15 @@ const void* decode_fn(int kv, int d, int ntw) {
 // WR x WB grid: WR warps split the rows (8*NTW each), WB warp groups take turns
 // on blocks. Each CTA has one producer thread issuing the TMA copies, and that
 // thread is the limit when few CTAs share an SM, so units of at most 8 rows run
-// small CTAs (2 consumer warps, ~44 KB of shared memory) five to an SM; wider
+// small CTAs (2 consumer warps, ~44 KB of shared memory) five to an SM; units of
+// up to 16 rows split their rows over two such warps (three CTAs per SM); wider
 // units keep two larger CTAs per SM (their warps need ~168 registers).
 DecodeGeometry choose_geometry(int kv, int d, int rows) {
   DecodeGeometry g{};
   const int nt = (rows + 7) / 8;
   size_t target = 110 * 1024;
   if (nt <= 1) { g.ntw = 1; g.warps_rows = 1; g.warps_blocks = 2; target = 44 * 1024; }
-  else if (nt <= 2) { g.ntw = 2; g.warps_rows = 1; g.warps_blocks = 4; }
+  else if (nt <= 2) { g.ntw = 1; g.warps_rows = 2; g.warps_blocks = 2; target = 72 * 1024; }
   else if (nt <= 4) { g.ntw = 2; g.warps_rows = 2; g.warps_blocks = 2; }
   else { g.ntw = 2; g.warps_rows = 4; g.warps_blocks = 1; }
   g.threads = (g.warps_rows * g.warps_blocks + 1) * 32;

@@ -117,7 +117,7 @@ __device__ __forceinline__ void mma_kv(float (&d)[4], uint32_t a0, uint32_t a1, 
 }
 
 template <int KV, int D, int NTW>
-__global__ void __launch_bounds__(NTW == 1 ? 96 : 160, NTW == 1 ? 5 : 2)
+__global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_k1, const __grid_constant__ CUtensorMap tm_v1,
                   const DecodeArgs a) {
@@ -409,7 +409,9 @@ __global__ void __launch_bounds__(NTW == 1 ? 96 : 160, NTW == 1 ? 5 : 2)
         *abort_flag = 1;
         if (lane == 0 && a.status) atomicOr(a.status, kDevTimeout);
       }
-      if (alive) {
+      // A warp whose rows are all padding for this sequence (fewer query tokens
+      // than the unit's row capacity) only waits for and releases its stages.
+      if (alive && row_base < Rs) {
         const int tok0 = (lb + k) * kBlockSize;
         if (tok0 + kBlockSize > ctx_eff) {
           // Positions >= ctx are not part of the sequence; their V rows may hold
