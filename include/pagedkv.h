@@ -169,6 +169,32 @@ int pkv_paged_attention_decode_varlen(void* out, const void* q, const int32_t* c
                                       int32_t* device_status, void* stream);
 
 /*
+ * pkv_paged_attention_decode_tree — speculative verify of a token TREE: the n_s
+ * query tokens of a sequence are candidate continuations organised as a tree
+ * (the token-tree verification of FlexFlow Serve, nxhydt survey of inference
+ * frameworks, section FlexFlow), and each query token may attend only to the
+ * context before the drafts and to its own ancestors.
+ *
+ *   tree_masks    [total query rows] uint64, device, 8-byte aligned: bit i of the
+ *                 mask of query token j of sequence s is set when j may attend to
+ *                 draft token i, i.e. position context_lens[s] - n_s + i. A token
+ *                 normally sees itself (bit j). A row that sees no position gets
+ *                 output 0. The causal chain is mask (2 << j) - 1.
+ *   cu_q_lens     may be NULL: then every sequence has max_q_per_seq tokens
+ *                 (rows s*max_q_per_seq + j); otherwise as for the _varlen call.
+ *   max_q_per_seq <= 64 (one mask bit per draft token).
+ *   Everything else is as for pkv_paged_attention_decode_varlen.
+ */
+int pkv_paged_attention_decode_tree(void* out, const void* q, const int32_t* cu_q_lens,
+                                    const uint64_t* tree_masks, int32_t num_seqs,
+                                    int32_t num_q_heads, int32_t max_q_per_seq,
+                                    const void* k_cache, const void* v_cache, pkv_dtype kv_dtype,
+                                    const pkv_cache_desc* cache, const int32_t* block_tables,
+                                    int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                    float scale, void* workspace, size_t workspace_bytes,
+                                    int32_t* device_status, void* stream);
+
+/*
  * pkv_paged_attention_decode_noalloc — the same decode attention as
  * pkv_paged_attention_decode, for callers that cannot allocate device memory
  * when they run it (for example code running inside a custom allocator's

@@ -77,7 +77,7 @@ def load():
             P(dbl), P(dbl), i64, P(ctypes.c_uint16), ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_int, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_int, P(i32), ctypes.c_int, P(i32), dbl, P(i32), ctypes.c_int, ctypes.c_int,
-            P(i32)]
+            P(i32), P(ctypes.c_uint64)]
         lib.orc_paged_attention.restype = ctypes.c_int
         lib.orc_hardware_threads.restype = ctypes.c_int
         assert lib.orc_version() == 1
@@ -156,19 +156,21 @@ def kv_cache_write(key, value, src_dtype: int, slot_mapping, k_cache, v_cache,
 def paged_attention(q, q_dtype: int, q_per_seq: int, k_cache, v_cache, kv_dtype: int,
                     block_tables, context_lens, scale: float, *, block_size: int = 16,
                     seqs=None, num_threads: int = 1, want_weights: bool = False,
-                    out=None, cu_q_lens=None):
+                    out=None, cu_q_lens=None, tree_masks=None):
     """fp64 paged decode attention.
 
     q: [rows, Hq, D] uint16 patterns: S*q_per_seq rows, or cu_q_lens[S] rows when
     cu_q_lens (int32 [S+1]) gives each sequence its own number of query tokens.
     Caches: [NB, Hkv, block_size, D]. Returns (out_f64 [rows, Hq, D], weights or
-    None, rc). Only the rows of ``seqs`` are computed when given.
+    None, rc). Only the rows of ``seqs`` are computed when given. tree_masks (uint64,
+    one per query row) replaces the causal rule: bit i lets a token see draft token i.
     """
     q = _u16(q)
     SN, Hq, D = q.shape
     context_lens = np.ascontiguousarray(context_lens, dtype=np.int32)
     S = context_lens.shape[0] if cu_q_lens is not None else SN // q_per_seq
     cu = None if cu_q_lens is None else np.ascontiguousarray(cu_q_lens, dtype=np.int32)
+    tm = None if tree_masks is None else np.ascontiguousarray(tree_masks, dtype=np.uint64)
     NB, Hkv = k_cache.shape[0], k_cache.shape[1]
     block_tables = np.ascontiguousarray(block_tables, dtype=np.int32)
     mbs = block_tables.shape[1]
@@ -190,7 +192,7 @@ def paged_attention(q, q_dtype: int, q_per_seq: int, k_cache, v_cache, kv_dtype:
         k_cache.ctypes.data_as(ctypes.c_void_p), v_cache.ctypes.data_as(ctypes.c_void_p),
         kv_dtype, NB, block_size, Hkv, D, _p(block_tables, ctypes.c_int32), mbs,
         _p(context_lens, ctypes.c_int32), float(scale), _p(subset, ctypes.c_int32), nsub,
-        int(num_threads), _p(cu, ctypes.c_int32))
+        int(num_threads), _p(cu, ctypes.c_int32), _p(tm, ctypes.c_uint64))
     return out, weights, rc
 
 

@@ -284,7 +284,7 @@ int orc_paged_attention(double* out, double* weights, int64_t weights_stride,
                         int head_size, const int32_t* block_tables,
                         int max_blocks_per_seq, const int32_t* context_lens, double scale,
                         const int32_t* seq_subset, int n_subset, int num_threads,
-                        const int32_t* cu_q_lens) {
+                        const int32_t* cu_q_lens, const uint64_t* tree_masks) {
   if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return -1;
   const int group = num_q_heads / num_kv_heads;
   // Query tokens and first query row of sequence s.
@@ -315,9 +315,20 @@ int orc_paged_attention(double* out, double* weights, int64_t weights_stride,
       const int n = tokens_of(s);
       const int64_t qrow = (first_row(s) + j) * num_q_heads + hq;
       double* o = out + qrow * head_size;
-      // Query token j is position ctx - n + j; it sees positions 0..ctx-n+j.
-      const int limit = ctx - n + j + 1;
-      if (limit <= 0 || limit > max_blocks_per_seq * block_size) {
+      // Query token j is position ctx - n + j. The context before the n query
+      // (draft) tokens is visible to all of them; draft token i (position
+      // ctx - n + i) is visible to token j when bit i of j's tree mask is set —
+      // without tree masks, when i <= j (causal among the query tokens).
+      const int base = ctx - n;
+      const uint64_t mask = tree_masks ? tree_masks[first_row(s) + j]
+                                       : (j >= 63 ? ~0ull : ((2ull << j) - 1ull));
+      auto visible = [&](int p) {
+        if (p < base) return true;
+        const int i = p - base;
+        return i < 64 && ((mask >> i) & 1ull) != 0;
+      };
+      const int limit = ctx;   // positions 0 .. ctx-1 exist
+      if (base < 0 || ctx > max_blocks_per_seq * block_size) {
         for (int d = 0; d < head_size; ++d) o[d] = NAN;
         bad[tid] = 1;
         continue;
@@ -332,11 +343,12 @@ int orc_paged_attention(double* out, double* weights, int64_t weights_stride,
       logits.assign(limit, 0.0);
       bool ok = true;
       for (int p = 0; p < limit && ok; ++p) {
-        int64_t base;
-        if (!kv_index(p, &base)) { ok = false; break; }
+        if (!visible(p)) continue;
+        int64_t kbase;
+        if (!kv_index(p, &kbase)) { ok = false; break; }
         double dot = 0.0;
         for (int d = 0; d < head_size; ++d) {
-          dot += src_value(q, q_dtype, qrow * head_size + d) * kv_value(k_cache, kv_dtype, base + d);
+          dot += src_value(q, q_dtype, qrow * head_size + d) * kv_value(k_cache, kv_dtype, kbase + d);
         }
         logits[p] = scale * dot;
       }
@@ -345,21 +357,22 @@ int orc_paged_attention(double* out, double* weights, int64_t weights_stride,
         bad[tid] = 1;
         continue;
       }
-      // softmax over the visible positions
+      // softmax over the visible positions (a row that sees none gets output 0)
       double mx = -INFINITY;
-      for (int p = 0; p < limit; ++p) mx = std::max(mx, logits[p]);
+      for (int p = 0; p < limit; ++p) if (visible(p)) mx = std::max(mx, logits[p]);
       double denom = 0.0;
-      for (int p = 0; p < limit; ++p) denom += std::exp(logits[p] - mx);
+      for (int p = 0; p < limit; ++p) if (visible(p)) denom += std::exp(logits[p] - mx);
       for (int d = 0; d < head_size; ++d) o[d] = 0.0;
+      if (weights) {
+        for (int64_t p = 0; p < weights_stride; ++p) weights[qrow * weights_stride + p] = 0.0;
+      }
       for (int p = 0; p < limit; ++p) {
+        if (!visible(p)) continue;
         const double w = std::exp(logits[p] - mx) / denom;
         if (weights) weights[qrow * weights_stride + p] = w;
-        int64_t base;
-        kv_index(p, &base);
-        for (int d = 0; d < head_size; ++d) o[d] += w * kv_value(v_cache, kv_dtype, base + d);
-      }
-      if (weights) {
-        for (int64_t p = limit; p < weights_stride; ++p) weights[qrow * weights_stride + p] = 0.0;
+        int64_t vbase;
+        kv_index(p, &vbase);
+        for (int d = 0; d < head_size; ++d) o[d] += w * kv_value(v_cache, kv_dtype, vbase + d);
       }
     }
   };

@@ -63,6 +63,10 @@ def load_library():
             vp, vp, vp, i32, i32, i32, vp, vp, ctypes.c_int, P(_CacheDesc), vp, i32, vp,
             ctypes.c_float, vp, ctypes.c_size_t, vp, vp]
         lib.pkv_paged_attention_decode_varlen.restype = ctypes.c_int
+        lib.pkv_paged_attention_decode_tree.argtypes = [
+            vp, vp, vp, vp, i32, i32, i32, vp, vp, ctypes.c_int, P(_CacheDesc), vp, i32, vp,
+            ctypes.c_float, vp, ctypes.c_size_t, vp, vp]
+        lib.pkv_paged_attention_decode_tree.restype = ctypes.c_int
         lib.pkv_paged_attention_decode_noalloc.argtypes = [
             vp, vp, i32, i32, i32, vp, vp, ctypes.c_int, P(_CacheDesc), vp, i32, vp,
             ctypes.c_float, vp, vp]
@@ -250,4 +254,38 @@ def paged_attention_decode_varlen(out, q, cu_q_lens, k_cache, v_cache, block_tab
             int(workspace.numel() * workspace.element_size()), _ptr(device_status),
             _stream_handle(stream, q.device))
     _check(rc, "paged_attention_decode_varlen")
+    return out
+
+
+def paged_attention_decode_tree(out, q, tree_masks, k_cache, v_cache, block_tables, context_lens,
+                                max_q_per_seq: int, scale: float, kv_dtype=None, *, cu_q_lens=None,
+                                workspace=None, device_status=None, stream=None):
+    """Speculative verify of a token tree: tree_masks (int64/uint64, one per query row)
+    bit i lets a query token attend to its sequence's draft token i; the context before
+    the drafts is always visible. cu_q_lens as for paged_attention_decode_varlen, or
+    None for max_q_per_seq tokens per sequence."""
+    for nm, t in (("out", out), ("q", q), ("tree_masks", tree_masks), ("k_cache", k_cache),
+                  ("v_cache", v_cache), ("block_tables", block_tables), ("context_lens", context_lens)):
+        _need_cuda_contig(nm, t)
+    if tree_masks.dtype not in (torch.int64, torch.uint64):
+        raise PagedKVError("tree_masks must be 64-bit")
+    if cu_q_lens is not None:
+        _need_cuda_contig("cu_q_lens", cu_q_lens)
+    if out.dtype != q.dtype:
+        raise PagedKVError("out and q must share a dtype")
+    S = int(context_lens.shape[0])
+    Hq = int(q.shape[1])
+    d = _desc(k_cache)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        need = int(lib.pkv_decode_workspace_bytes(S, Hq, int(max_q_per_seq), ctypes.byref(d)))
+        if workspace is None:
+            workspace = _workspace(need, q.device)
+        rc = lib.pkv_paged_attention_decode_tree(
+            _ptr(out), _ptr(q), _ptr(cu_q_lens), _ptr(tree_masks), S, Hq, int(max_q_per_seq),
+            _ptr(k_cache), _ptr(v_cache), _kv_code(kv_dtype, k_cache), ctypes.byref(d),
+            _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens), float(scale),
+            _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+            _ptr(device_status), _stream_handle(stream, q.device))
+    _check(rc, "paged_attention_decode_tree")
     return out

@@ -291,7 +291,8 @@ namespace {
 
 // Shared body of the decode entry points; cu_q_lens null means q_per_seq query
 // tokens for every sequence.
-int decode_impl(void* out, const void* q, const int32_t* cu_q_lens, int32_t num_seqs,
+int decode_impl(void* out, const void* q, const int32_t* cu_q_lens,
+                const unsigned long long* tree_masks, int32_t num_seqs,
                 int32_t num_q_heads, int32_t q_per_seq, const void* k_cache, const void* v_cache,
                 pkv_dtype kv_dtype, const pkv_cache_desc* cache, const int32_t* block_tables,
                 int32_t max_blocks_per_seq, const int32_t* context_lens, float scale,
@@ -315,6 +316,7 @@ int decode_impl(void* out, const void* q, const int32_t* cu_q_lens, int32_t num_
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace)
     return PKV_ERR_INVALID_ARGUMENT;
   if (cu_q_lens && !aligned4(cu_q_lens)) return PKV_ERR_INVALID_ARGUMENT;
+  if (tree_masks && (reinterpret_cast<uintptr_t>(tree_masks) & 7u)) return PKV_ERR_INVALID_ARGUMENT;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
       !aligned16(workspace) || !aligned4(block_tables) || !aligned4(context_lens) ||
       (device_status && !aligned4(device_status)))
@@ -357,6 +359,7 @@ int decode_impl(void* out, const void* q, const int32_t* cu_q_lens, int32_t num_
   a.block_tables = block_tables;
   a.context_lens = context_lens;
   a.cu_q_lens = cu_q_lens;
+  a.tree_masks = tree_masks;
   a.piece_counts = reinterpret_cast<unsigned long long*>(ws);
   a.partials = reinterpret_cast<float*>(ws + desc_bytes(units));
   a.status = device_status;
@@ -401,7 +404,7 @@ int pkv_paged_attention_decode(void* out, const void* q, int32_t num_seqs, int32
                                const int32_t* block_tables, int32_t max_blocks_per_seq,
                                const int32_t* context_lens, float scale, void* workspace,
                                size_t workspace_bytes, int32_t* device_status, void* stream) {
-  return decode_impl(out, q, nullptr, num_seqs, num_q_heads, q_per_seq, k_cache, v_cache, kv_dtype,
+  return decode_impl(out, q, nullptr, nullptr, num_seqs, num_q_heads, q_per_seq, k_cache, v_cache, kv_dtype,
                      cache, block_tables, max_blocks_per_seq, context_lens, scale, workspace,
                      workspace_bytes, device_status, stream);
 }
@@ -414,9 +417,25 @@ int pkv_paged_attention_decode_varlen(void* out, const void* q, const int32_t* c
                                       float scale, void* workspace, size_t workspace_bytes,
                                       int32_t* device_status, void* stream) {
   if (num_seqs > 0 && !cu_q_lens) return PKV_ERR_INVALID_ARGUMENT;
-  return decode_impl(out, q, cu_q_lens, num_seqs, num_q_heads, max_q_per_seq, k_cache, v_cache,
+  return decode_impl(out, q, cu_q_lens, nullptr, num_seqs, num_q_heads, max_q_per_seq, k_cache, v_cache,
                      kv_dtype, cache, block_tables, max_blocks_per_seq, context_lens, scale,
                      workspace, workspace_bytes, device_status, stream);
+}
+
+int pkv_paged_attention_decode_tree(void* out, const void* q, const int32_t* cu_q_lens,
+                                    const uint64_t* tree_masks, int32_t num_seqs,
+                                    int32_t num_q_heads, int32_t max_q_per_seq,
+                                    const void* k_cache, const void* v_cache, pkv_dtype kv_dtype,
+                                    const pkv_cache_desc* cache, const int32_t* block_tables,
+                                    int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                    float scale, void* workspace, size_t workspace_bytes,
+                                    int32_t* device_status, void* stream) {
+  if (num_seqs > 0 && !tree_masks) return PKV_ERR_INVALID_ARGUMENT;
+  if (max_q_per_seq > 64) return PKV_ERR_UNSUPPORTED;
+  return decode_impl(out, q, cu_q_lens, reinterpret_cast<const unsigned long long*>(tree_masks),
+                     num_seqs, num_q_heads, max_q_per_seq, k_cache, v_cache, kv_dtype, cache,
+                     block_tables, max_blocks_per_seq, context_lens, scale, workspace,
+                     workspace_bytes, device_status, stream);
 }
 
 }  // extern "C"

@@ -380,7 +380,12 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
 
     float m_run[NTW][2], l_run[NTW][2];
     float o_acc[MT][NTW][4];
-    int lim[NTW][2];
+    // Visibility of the n_s query (draft) tokens: the context before them,
+    // positions < cb, is visible to every row; draft token i (position cb + i) is
+    // visible to query token j when bit i of j's mask is set. Without tree masks
+    // the mask is the causal chain, bits 0..j.
+    const int cb = ctx_eff - n_s;
+    unsigned long long vis[NTW][2];
 #pragma unroll
     for (int nt = 0; nt < NTW; ++nt) {
 #pragma unroll
@@ -389,8 +394,11 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
         l_run[nt][e] = 0.f;
         const int r = row_base + nt * 8 + 2 * c4 + e;
         const int j = r / G;
-        const int lj = ctx_eff - n_s + j;           // last visible position of token j
-        lim[nt][e] = lj < ctx_eff - 1 ? lj : ctx_eff - 1;
+        if (a.tree_masks && r < Rs) {
+          vis[nt][e] = a.tree_masks[qb + j];
+        } else {
+          vis[nt][e] = (j >= 63) ? ~0ull : ((2ull << j) - 1ull);
+        }
       }
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
@@ -466,7 +474,7 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
         }
 
         // ---- online softmax (base 2) over this block ----
-        const bool masked = tok0 + (kBlockSize - 1) > ctx_eff - n_s;
+        const bool masked = tok0 + (kBlockSize - 1) >= cb;
         const int p_lo = tok0 + g8, p_hi = p_lo + 8;
         uint32_t pb[NTW][2];
         uint32_t pb_lo[NTW][2];   // bf16 only: P - bf16(P), a second bf16 term
@@ -479,8 +487,12 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
             float x_lo = (sa[0][nt][e] + sa[1][nt][e]) * a.scale_log2;
             float x_hi = (sa[0][nt][2 + e] + sa[1][nt][2 + e]) * a.scale_log2;
             if (masked) {
-              x_lo = (p_lo <= lim[nt][e]) ? x_lo : kNegInf;
-              x_hi = (p_hi <= lim[nt][e]) ? x_hi : kNegInf;
+              const bool v_lo = p_lo < cb || (p_lo < ctx_eff && p_lo - cb < 64 &&
+                                               ((vis[nt][e] >> (p_lo - cb)) & 1ull));
+              const bool v_hi = p_hi < cb || (p_hi < ctx_eff && p_hi - cb < 64 &&
+                                               ((vis[nt][e] >> (p_hi - cb)) & 1ull));
+              x_lo = v_lo ? x_lo : kNegInf;
+              x_hi = v_hi ? x_hi : kNegInf;
             }
             float mx = fmaxf(x_lo, x_hi);
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));

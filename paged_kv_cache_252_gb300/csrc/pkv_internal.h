@@ -26,6 +26,7 @@ struct DecodeArgs {
   const int32_t* block_tables; // [S][max_blocks_per_seq]
   const int32_t* context_lens; // [S]
   const int32_t* cu_q_lens;    // [S+1] query-token offsets, or null: q_per_seq tokens each
+  const unsigned long long* tree_masks;  // [rows] draft tokens visible to each query token, or null: causal
   float* partials;             // split-KV partial slots
   unsigned long long* piece_counts;  // [S*Hkv]: (call epoch << 32) | pieces finished
   int32_t* status;             // optional device status word

@@ -338,3 +338,19 @@ def prefill_mask(w: Workload) -> np.ndarray:
     m = np.ones(w.num_tokens_total, dtype=bool)
     m[w.new_token_index()] = False
     return m
+
+
+def random_tree_masks(q_lens, seed: int) -> np.ndarray:
+    """Seeded token trees for speculative verify: in each sequence, draft token i
+    (i = 0..n_s-1) has a parent drawn uniformly from {context, draft 0..i-1}; its
+    mask holds its ancestors' bits and its own. Returns uint64 [sum(q_lens)]."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = []
+    for n in np.asarray(q_lens, dtype=np.int64):
+        masks = []
+        for i in range(int(n)):
+            parent = int(rng.integers(-1, i)) if i > 0 else -1
+            m = (masks[parent] if parent >= 0 else 0) | (1 << i)
+            masks.append(m)
+        out.extend(masks)
+    return np.array(out, dtype=np.uint64)

@@ -61,7 +61,7 @@ def dense_kv_f64(w, vals, s):
     return k.to(torch.float64), v.to(torch.float64)
 
 
-def sdpa_reference(w, vals, s):
+def sdpa_reference(w, vals, s, tree_masks=None):
     """Library reference for sequence s: torch SDPA in fp64 on contiguous K/V, GQA by
     repeating each KV head over its G query heads, causal among the n query tokens."""
     G = w.group
@@ -74,7 +74,16 @@ def sdpa_reference(w, vals, s):
     v = v.repeat_interleave(G, dim=1).permute(1, 0, 2)[None]
     qq = q.permute(1, 0, 2)[None]                              # [1, Hq, n, D]
     pos = torch.arange(ctx)[None, :]
-    lim = (ctx - n + torch.arange(n))[:, None]
-    mask = pos <= lim                                          # [n, ctx]
+    if tree_masks is None:
+        lim = (ctx - n + torch.arange(n))[:, None]
+        mask = pos <= lim                                      # [n, ctx]
+    else:
+        base = ctx - n
+        mask = torch.zeros(n, ctx, dtype=torch.bool)
+        mask[:, :base] = True
+        for j in range(n):
+            m = int(tree_masks[cu[s] + j])
+            for i in range(n):
+                mask[j, base + i] = bool((m >> i) & 1)
     o = torch.nn.functional.scaled_dot_product_attention(qq, k, v, attn_mask=mask, scale=w.scale)
     return o[0].permute(1, 0, 2).numpy()                       # [n, Hq, D]

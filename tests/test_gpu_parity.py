@@ -246,3 +246,48 @@ def test_varlen_rejects_bad_counts_without_faulting(orc, dev, gpu):
     assert int(status.item()) & 0x4
     assert torch.equal(out2[0], out[0])           # sequence 0 unaffected
     assert torch.isnan(out2[1:4]).all()           # sequence 1 got no output rows
+
+
+# ------------------------------------------------------------------------------------
+# token-tree verify
+# ------------------------------------------------------------------------------------
+
+TREES = [
+    # (kv, D, Hq, Hkv, q_lens or uniform n)
+    ("e5m2", 128, 64, 8, 4),
+    ("fp16", 128, 32, 8, [5, 1, 8, 3, 2]),
+    ("bf16", 64, 8, 4, [16, 3, 9]),
+    ("fp16", 64, 4, 4, 16),
+]
+
+
+@pytest.mark.parametrize("case", TREES, ids=[f"{c[0]}-D{c[1]}-G{c[2] // c[3]}" for c in TREES])
+def test_tree_verify_parity(orc, dev, gpu, case):
+    import paged_kv_cache_252_gb300 as pkv
+    kv, D, Hq, Hkv, ql = case
+    S = 5 if isinstance(ql, int) else len(ql)
+    q_lens = [ql] * S if isinstance(ql, int) else ql
+    lens = [max(l, n) for l, n in zip([20, 1, 300, 33, 1200], q_lens)]
+    w = wl.custom(num_seqs=S, num_q_heads=Hq, num_kv_heads=Hkv, head_size=D, q_per_seq=max(q_lens),
+                  kv_dtype=kv, context_lens=lens, seed=500 + D, q_lens=None if isinstance(ql, int) else q_lens)
+    masks = wl.random_tree_masks(q_lens, seed=11 + D)
+    vals = wl.token_values(w)
+    kc, vc, _ = gpu.cuda_path(w, vals, dev)
+    q = vals["q"].to(dev)
+    out = torch.full_like(q, float("nan"))
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    cl = torch.from_numpy(w.context_lens).to(dev)
+    tm = torch.from_numpy(masks.view(np.int64)).to(dev)
+    cu = torch.from_numpy(w.cu_q_lens()).to(dev) if w.q_lens is not None else None
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    pkv.paged_attention_decode_tree(out, q, tm, kc, vc, bt, cl, w.q_per_seq, w.scale, cu_q_lens=cu,
+                                    device_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    okc, ovc = gpu.oracle_caches(orc, w, vals)
+    kw = {"tree_masks": masks}
+    if w.q_lens is None:
+        kw["cu_q_lens"] = w.cu_q_lens()
+    ref, _, rc = gpu.oracle_attention(orc, w, vals, okc, ovc, **kw)
+    assert rc == 0
+    gpu.compare(out, ref)

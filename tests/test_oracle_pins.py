@@ -416,3 +416,47 @@ def test_varlen_with_equal_counts_is_the_uniform_batch(orc):
     var, _, rc = oracle_attention(orc, w, vals, kc, vc, cu_q_lens=np.array([0, 2, 4, 6], np.int32))
     assert rc == 0
     assert np.array_equal(uni, var)
+
+
+# ---------------------------------------------------------------------------------
+# token-tree verify (FlexFlow Serve, token-tree verification)
+# ---------------------------------------------------------------------------------
+
+def test_tree_masks_match_sdpa_with_the_tree_mask(orc):
+    q_lens = [4, 6, 1, 3]
+    w = wl.custom(num_seqs=4, num_q_heads=8, num_kv_heads=2, head_size=64, q_per_seq=6,
+                  kv_dtype="fp16", context_lens=[10, 40, 5, 17], seed=44, q_lens=q_lens)
+    vals = wl.token_values(w)
+    masks = wl.random_tree_masks(q_lens, seed=7)
+    kc, vc = oracle_caches(orc, w, vals)
+    out, _, rc = oracle_attention(orc, w, vals, kc, vc, tree_masks=masks)
+    assert rc == 0
+    cu = w.cu_q_lens()
+    for s in range(w.num_seqs):
+        ref = sdpa_reference(w, vals, s, tree_masks=masks)
+        np.testing.assert_allclose(out[cu[s]:cu[s + 1]], ref, rtol=1e-10, atol=1e-12)
+
+
+def test_chain_tree_is_the_causal_verify(orc):
+    w = wl.custom(num_seqs=3, num_q_heads=8, num_kv_heads=2, head_size=64, q_per_seq=4,
+                  kv_dtype="bf16", context_lens=[4, 33, 70], seed=45)
+    vals = wl.token_values(w)
+    kc, vc = oracle_caches(orc, w, vals)
+    causal, _, _ = oracle_attention(orc, w, vals, kc, vc)
+    chain = np.array([(2 << j) - 1 for _ in range(3) for j in range(4)], dtype=np.uint64)
+    tree, _, rc = oracle_attention(orc, w, vals, kc, vc, tree_masks=chain)
+    assert rc == 0
+    assert np.array_equal(causal, tree)
+
+
+def test_random_tree_masks_are_ancestor_closed():
+    masks = wl.random_tree_masks([7, 1, 5], seed=3)
+    off = 0
+    for n in (7, 1, 5):
+        m = [int(x) for x in masks[off:off + n]]
+        for i in range(n):
+            assert (m[i] >> i) & 1 and m[i] < (1 << (i + 1))
+            for a in range(i):
+                if (m[i] >> a) & 1:
+                    assert m[a] & m[i] == m[a]     # every ancestor's ancestors are visible too
+        off += n
