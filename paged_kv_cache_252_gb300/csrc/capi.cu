@@ -22,6 +22,7 @@ struct GeomEntry {
   bool ready = false;
   DecodeGeometry geom{};
   int ctas_per_sm = 0;
+  const void* fn = nullptr;
 };
 
 struct DeviceState {
@@ -30,6 +31,8 @@ struct DeviceState {
   bool write_attr_done = false;
   // [kv][d==128][ntw==2]
   GeomEntry geom[3][2][2];
+  // tcgen05 kernel, [rc - 1]
+  GeomEntry tc_geom[2];
 };
 
 std::mutex g_mu;
@@ -104,14 +107,35 @@ DecodeGeometry choose_geometry(int kv, int d, int rows) {
   return g;
 }
 
+// Units wider than 16 rows over an E5M2 cache with head size 128 run on the
+// tcgen05 kernel: one 192-thread CTA per SM holding the widened K/V chunk
+// buffers, P^T, two query tiles and a ring of as many 32 KB chunk buffers
+// (2..4) as fit in the 227 KB a CTA may use.
+bool use_tc(int kv, int d, int rows) { return kv == kKvE5m2 && d == 128 && rows > 16; }
+
+DecodeGeometry choose_tc_geometry(int rows) {
+  DecodeGeometry g{};
+  g.tc = 1;
+  g.rc = rows > 32 ? 2 : 1;
+  g.threads = kTcThreads;
+  const size_t limit = 227 * 1024;
+  int nbuf = 4;
+  while (nbuf > 2 && tc_smem_layout(32 * g.rc, nbuf).total + 1024 > limit) --nbuf;
+  g.stages = nbuf;
+  g.smem_bytes = tc_smem_layout(32 * g.rc, nbuf).total + 1024;
+  return g;
+}
+
 int get_geometry(DeviceState* st, int kv, int d, int rows, GeomEntry** out) {
-  const DecodeGeometry g0 = choose_geometry(kv, d, rows);
-  GeomEntry& e = st->geom[kv][d == 128 ? 1 : 0][g0.ntw == 2 ? 1 : 0];
+  const bool tc = use_tc(kv, d, rows);
+  const DecodeGeometry g0 = tc ? choose_tc_geometry(rows) : choose_geometry(kv, d, rows);
+  GeomEntry& e = tc ? st->tc_geom[g0.rc - 1] : st->geom[kv][d == 128 ? 1 : 0][g0.ntw == 2 ? 1 : 0];
   // The cached entry is keyed by (kv, d, ntw); the row count also changes the
   // warp grid and the merge-buffer size, so re-derive and compare.
   if (!e.ready || e.geom.warps_rows != g0.warps_rows || e.geom.warps_blocks != g0.warps_blocks ||
-      e.geom.stages != g0.stages || e.geom.smem_bytes != g0.smem_bytes) {
-    const void* fn = decode_fn(kv, d, g0.ntw);
+      e.geom.stages != g0.stages || e.geom.smem_bytes != g0.smem_bytes || e.geom.tc != g0.tc ||
+      e.geom.rc != g0.rc) {
+    const void* fn = tc ? decode_tc_kernel_ptr(kv, g0.rc) : decode_fn(kv, d, g0.ntw);
     if (!fn) return PKV_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(g0.smem_bytes)) != cudaSuccess) {
@@ -127,6 +151,7 @@ int get_geometry(DeviceState* st, int kv, int d, int rows, GeomEntry** out) {
       return PKV_ERR_CUDA;
     }
     e.geom = g0;
+    e.fn = fn;
     e.ctas_per_sm = nblk < kMaxCtasPerSm ? nblk : kMaxCtasPerSm;
     e.ready = true;
   }
@@ -384,8 +409,9 @@ int decode_impl(void* out, const void* q, const int32_t* cu_q_lens,
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   void* dargs[5] = {&tmk, &tmv, &tmk1, &tmv1, &a};
-  const cudaError_t e = launch(decode_fn(kv, d, g.ntw), dim3(static_cast<unsigned>(grid)), dim3(g.threads),
-                         g.smem_bytes, s, dargs);
+  void* dargs_tc[3] = {&tmk, &tmv, &a};
+  const cudaError_t e = launch(ge->fn, dim3(static_cast<unsigned>(grid)), dim3(g.threads), g.smem_bytes, s,
+                               g.tc ? dargs_tc : dargs);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return PKV_ERR_CUDA;

@@ -39,6 +39,7 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include "decode_common.cuh"
 #include "pkv_internal.h"
 #include "pkv_ptx.cuh"
 
@@ -63,46 +64,6 @@ __device__ __forceinline__ uint32_t swz(uint32_t off) {
     return off ^ ((off >> 3) & 0x70u);   // 16-byte chunk ^= 128-byte line index (mod 8)
   } else {
     return off ^ ((off >> 3) & 0x30u);   // 64-byte swizzle
-  }
-}
-
-// Blocks of one (sequence, KV head) unit. A context length outside
-// [1, max_blocks*16] is clamped so that every unit owns at least one block (and
-// so gets its output written) and never reads past its block-table row.
-__device__ __forceinline__ int unit_blocks(int ctx, int mbs) {
-  int c = ctx < 1 ? 1 : ctx;
-  const int cap = mbs * kBlockSize;
-  c = c > cap ? cap : c;
-  return (c + kBlockSize - 1) / kBlockSize;
-}
-
-__device__ __forceinline__ long long warp_sum_ll(long long v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-// Wait for an mbarrier phase; gives up after kWaitLimitNs or when another warp
-// of the CTA has already given up (abort flag in shared memory).
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
-                                              volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0u) {
-      if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) return false;
-    }
-  }
-}
-
-template <int KV>
-__device__ __forceinline__ uint32_t pack_p(float lo, float hi) {
-  if constexpr (KV == kKvBf16) {
-    return pack_bf16x2(lo, hi);
-  } else {
-    return pack_f16x2(lo, hi);
   }
 }
 
@@ -147,7 +108,6 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
   volatile int* fin = reinterpret_cast<volatile int*>(plan + 6);   // is_last, first CTA, last CTA
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nwarps = blockDim.x >> 5;
   const bool is_producer = (warp == NC);
 
   if (tid == 0) {
@@ -174,56 +134,11 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
   // Everything below reads inputs a previous kernel in the stream may write.
   pdl_wait_prior_grid();
 
-  const int S = a.num_seqs, Hkv = a.num_kv_heads, mbs = a.max_blocks_per_seq;
+  const int Hkv = a.num_kv_heads, mbs = a.max_blocks_per_seq;
   const int n = a.q_per_seq, G = a.group, Hq = a.num_q_heads;
   const long long ncta = gridDim.x, cta = blockIdx.x;
 
-  // ---- plan: this CTA's share [b0, b1) of all (sequence, head, block) triples ----
-  // One pass over context_lens: thread t owns a contiguous run of sequences,
-  // a block-wide scan of the runs' block counts gives the total and every run's
-  // offset, and the thread whose run holds block b0 finds its sequence.
-  {
-    const int per = (S + blockDim.x - 1) / blockDim.x;
-    const int s_lo = tid * per;
-    const int s_hi = s_lo + per < S ? s_lo + per : S;
-    long long mine = 0;
-    for (int s = s_lo; s < s_hi; ++s) mine += unit_blocks(a.context_lens[s], mbs);
-    mine *= Hkv;
-    long long v = mine;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const long long t = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) v += t;
-    }
-    if (lane == 31) red[warp] = v;
-    if (tid == 0) plan[3] = -1;
-    __syncthreads();
-    long long pre = 0, tot = 0;
-    for (int w = 0; w < nwarps; ++w) {
-      if (w < warp) pre += red[w];
-      tot += red[w];
-    }
-    const long long excl = pre + v - mine;
-    // Only min(grid, total) CTAs take work, so every active CTA owns at least one
-    // block and every CTA between a unit's first and last owner wrote a piece of it.
-    const long long nact = ncta < tot ? ncta : tot;
-    const long long b0 = cta < nact ? cta * tot / nact : tot;
-    const long long b1 = cta < nact ? (cta + 1) * tot / nact : tot;
-    if (b0 < b1 && excl <= b0 && b0 < excl + mine) {
-      long long cum = excl;
-      for (int s = s_lo; s < s_hi; ++s) {
-        const long long wblk = static_cast<long long>(Hkv) * unit_blocks(a.context_lens[s], mbs);
-        if (b0 < cum + wblk) {
-          plan[3] = s;
-          plan[4] = cum / Hkv;
-          break;
-        }
-        cum += wblk;
-      }
-    }
-    if (tid == 0) { plan[0] = tot; plan[1] = b0; plan[2] = b1; }
-    __syncthreads();
-  }
+  plan_cta_share(a, red, plan);
   pdl_launch_dependents();
 
   const long long total = plan[0], b0 = plan[1], b1 = plan[2];
@@ -657,63 +572,7 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
     }
 
     if (split) {
-      // Count this piece; the CTA finishing the unit's last piece combines them.
-      // The barrier orders every consumer thread's slot writes before thread 0's
-      // device-scope fence, which makes them visible before the counter update.
-      named_bar_sync(3, nthr_c);
-      if (tid == 0) {
-        __threadfence();
-        const long long nact = ncta < total ? ncta : total;
-        const long long ustart = gpos - lb;                       // unit's first global block
-        const int c_first = static_cast<int>(((ustart + 1) * nact - 1) / total);
-        const int c_last = static_cast<int>(((ustart + nb) * nact - 1) / total);
-        unsigned long long* ctr = a.piece_counts + u;
-        unsigned long long cur = atomicAdd(ctr, 0ull);
-        unsigned long long want;
-        for (;;) {
-          want = (static_cast<uint32_t>(cur >> 32) == a.epoch)
-                     ? cur + 1ull
-                     : ((static_cast<unsigned long long>(a.epoch) << 32) | 1ull);
-          const unsigned long long prev = atomicCAS(ctr, cur, want);
-          if (prev == cur) break;
-          cur = prev;
-        }
-        fin[0] = (static_cast<int>(want & 0xffffffffull) == c_last - c_first + 1) ? 1 : 0;
-        fin[1] = c_first;
-        fin[2] = c_last;
-        __threadfence();
-      }
-      named_bar_sync(3, nthr_c);
-      if (fin[0]) {
-        const int c_first = fin[1], c_last = fin[2];
-        const int ooff = partial_o_offset(R);
-        for (int idx = tid; idx < Rs * (D / 4); idx += nthr_c) {
-          const int r = idx / (D / 4), d4 = idx - (idx / (D / 4)) * (D / 4);
-          float M = kNegInf;
-          for (int c = c_first; c <= c_last; ++c)
-            M = fmaxf(M, __ldcg(a.partials + static_cast<size_t>(u + c) * a.slot_floats + r));
-          const float Mu = (M == kNegInf) ? 0.f : M;
-          float lsum = 0.f;
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int c = c_first; c <= c_last; ++c) {
-            const float* P = a.partials + static_cast<size_t>(u + c) * a.slot_floats;
-            const float f = fast_exp2(__ldcg(P + r) - Mu);
-            lsum += f * __ldcg(P + R + r);
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(P + ooff + r * D + d4 * 4));
-            acc.x += f * v.x;
-            acc.y += f * v.y;
-            acc.z += f * v.z;
-            acc.w += f * v.w;
-          }
-          const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-          const int j = r / G, gi = r - j * G;
-          const size_t dst = (static_cast<size_t>(qb + j) * Hq + h * G + gi) * D + d4 * 4;
-          uint2 pk;
-          pk.x = pack_p<KV>(acc.x * inv, acc.y * inv);
-          pk.y = pack_p<KV>(acc.z * inv, acc.w * inv);
-          *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + dst) = pk;
-        }
-      }
+      finish_split_piece<KV, D>(a, u, gpos - lb, nb, total, ncta, Rs, qb, h, tid, nthr_c, 3, fin);
     }
 
     // ---- advance the walk ----

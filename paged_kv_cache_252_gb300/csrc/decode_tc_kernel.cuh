@@ -1,0 +1,689 @@
+// Paged decode attention on the 5th-generation tensor core (tcgen05) for wide
+// units: 17..64 query rows per (sequence, KV head) -- a GQA group times several
+// speculative query tokens -- over an E5M2 KV cache with head size 128.
+//
+// What it computes is the same as the mma.sync kernel (decode_kernel.cuh):
+// PagedAttention over blocks reached through a block table, the E5M2 cache
+// widened to fp16 on read ("AI大模型推理速度翻倍，Colossal-Inference开源发布",
+// 分页注意力算法 and KV缓存量化), softmax reduced chunk by chunk with a running
+// max and sum ("AI 大模型推理优化技术详解", 2.2.1 Flash Attention), one KV head
+// serving its query-head group (2.2.2 GQA), query token j of n seeing the
+// context up to its own position (or the draft tokens its tree mask allows).
+// The CTA's share of the batch and the split-KV combine are shared with that
+// kernel (decode_common.cuh).
+//
+// Work is done in chunks of 8 KV blocks (128 tokens) of one unit.
+//   S^T (128 tokens x RP rows)  = K_chunk (128 x 128, fp16) . Q^T      [TMEM, fp32]
+//   O^T (128 dims   x RP rows) += V_chunk^T (128 x 128 tokens) . P^T   [TMEM, fp32]
+// with RP = 32 or 64 (rows padded; padding rows of Q are zero).
+//
+// Warp roles (192 threads, one CTA per SM):
+//   warp 5      : TMA producer. Copies the chunk's K and V tiles (E5M2,
+//                 [16 tokens][128 bytes], 128-byte swizzle) into a ring of
+//                 chunk buffers.
+//   warp 4      : one thread issues every tcgen05.mma and commits each group
+//                 to an mbarrier; the warp owns the tensor-memory allocation.
+//   warps 0..3  : thread t owns token t of the chunk, which is also TMEM lane
+//                 t of S^T and head dimension t of O^T. Each chunk: widen the
+//                 next chunk's K and V rows to fp16 in the MMA operand layout,
+//                 read its own 32/64 scores from TMEM, mask, exponentiate
+//                 against the rows' running max, keep per-thread partial sums,
+//                 write P^T; at the end of a unit piece, reduce the sums over
+//                 the CTA, read O^T from TMEM and write the output or a split
+//                 partial.
+// The running max of a row moves only when a score exceeds it by more than
+// kRescaleSlack (base 2): then the chunk's exact row maxima are reduced across
+// the 128 threads and O^T and the partial sums are rescaled. Probabilities are
+// therefore at most 2^kRescaleSlack, well inside fp16.
+//
+// Pipeline per chunk c (softmax warps): wait S(c); widen K(c+1) (+ Q of a new
+// piece) -> the MMA thread issues S(c+1) while the softmax of chunk c runs;
+// wait O(c-1); write P(c); widen V(c+1) -> the MMA thread issues O(c).
+// K16, P and the S^T columns are single-buffered, V16 and Q double-buffered.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "decode_common.cuh"
+#include "pkv_internal.h"
+#include "pkv_ptx.cuh"
+#include "pkv_tc.cuh"
+
+namespace pkv {
+
+constexpr int kTcSoftmaxThreads = 128;
+constexpr int kTcMmaWarp = 4;
+constexpr int kTcProducerWarp = 5;
+constexpr uint32_t kTcOCol = 64;             // first TMEM column of O^T
+constexpr uint32_t kTcLCol = 128;            // first TMEM column of the row sums
+constexpr float kRescaleSlack = 8.f;         // base-2 headroom before the running max moves
+
+// Order-preserving map between floats and signed ints, for integer max reductions.
+__device__ __forceinline__ int float_order_key(float f) {
+  const int i = __float_as_int(f);
+  return i >= 0 ? i : (i ^ 0x7FFFFFFF);
+}
+__device__ __forceinline__ float float_from_order_key(int k) {
+  return __int_as_float(k >= 0 ? k : (k ^ 0x7FFFFFFF));
+}
+
+// v[lane] without dynamic register indexing.
+__device__ __forceinline__ float select_lane32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) {
+    const bool up = (lane & s) != 0;
+#pragma unroll
+    for (int k = 0; k < s; ++k) v[k] = up ? v[k + s] : v[k];
+  }
+  return v[0];
+}
+
+// Widen token row t of an E5M2 chunk (128 rows x 128 bytes, 128-byte swizzle,
+// as TMA wrote it) into the fp16 operand layout: two 64-dimension halves of
+// [128 rows][128 bytes], same swizzle. E5M2 byte b is the fp16 pattern b << 8.
+// Rows that are not part of the sequence are written as zeros.
+__device__ __forceinline__ void widen_e5m2_row(const uint8_t* src, uint8_t* dst, int t, bool valid) {
+  const int sw = t & 7;
+  const uint8_t* s = src + t * 128;
+  uint8_t* d = dst + t * 128;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (valid) v = *reinterpret_cast<const uint4*>(s + ((c ^ sw) << 4));
+    uint4 lo, hi;
+    lo.x = __byte_perm(v.x, 0, 0x1404);
+    lo.y = __byte_perm(v.x, 0, 0x3424);
+    lo.z = __byte_perm(v.y, 0, 0x1404);
+    lo.w = __byte_perm(v.y, 0, 0x3424);
+    hi.x = __byte_perm(v.z, 0, 0x1404);
+    hi.y = __byte_perm(v.z, 0, 0x3424);
+    hi.z = __byte_perm(v.w, 0, 0x1404);
+    hi.w = __byte_perm(v.w, 0, 0x3424);
+    uint8_t* dh = d + (c >> 2) * (128 * 128);
+    const int c16 = (2 * c) & 7;
+    *reinterpret_cast<uint4*>(dh + ((c16 ^ sw) << 4)) = lo;
+    *reinterpret_cast<uint4*>(dh + (((c16 + 1) ^ sw) << 4)) = hi;
+  }
+}
+
+// Position in a CTA's share: the current piece (unit (s, h), blocks
+// [lb, lb + take) of it) and the current chunk (blocks cofs .. cofs + 7 of the piece).
+struct TcWalk {
+  long long gpos;   // global index of the piece's first block
+  long long b1;     // end of the CTA's share
+  int s, h, lb, nb, ctx, take, cofs;
+
+  __device__ bool done() const { return gpos >= b1; }
+  __device__ int nblk() const { return take - cofs < kTcChunk ? take - cofs : kTcChunk; }
+  __device__ bool first() const { return cofs == 0; }
+  __device__ bool last() const { return cofs + kTcChunk >= take; }
+  __device__ int first_token() const { return (lb + cofs) * kBlockSize; }
+  __device__ void advance(const DecodeArgs& a) {
+    cofs += kTcChunk;
+    if (cofs < take) return;
+    cofs = 0;
+    gpos += take;
+    lb += take;
+    if (lb == nb) {
+      lb = 0;
+      if (++h == a.num_kv_heads) {
+        h = 0;
+        ++s;
+        if (gpos < b1) {
+          ctx = a.context_lens[s];
+          nb = unit_blocks(ctx, a.max_blocks_per_seq);
+        }
+      }
+    }
+    if (gpos < b1) {
+      const long long left = b1 - gpos;
+      take = left < nb - lb ? static_cast<int>(left) : nb - lb;
+    }
+  }
+};
+
+// Per-piece facts the softmax warps need.
+struct TcPiece {
+  int n_s, qb, Rs, ctx_eff, cb, u;
+  bool split;
+};
+
+__device__ __forceinline__ TcPiece tc_piece(const DecodeArgs& a, const TcWalk& w, int tid) {
+  TcPiece p;
+  const int n = a.q_per_seq;
+  const int cap = a.max_blocks_per_seq * kBlockSize;
+  p.ctx_eff = w.ctx < cap ? w.ctx : cap;
+  // Query tokens of sequence s: n_s of them at rows qb.. of q/out; a count
+  // outside [1, q_per_seq] is flagged and the sequence gets no rows.
+  int n_s = n, qb = w.s * n;
+  if (a.cu_q_lens) {
+    qb = a.cu_q_lens[w.s];
+    n_s = a.cu_q_lens[w.s + 1] - qb;
+  }
+  const bool rows_ok = n_s >= 1 && n_s <= n;
+  p.Rs = rows_ok ? a.group * n_s : 0;
+  if (!rows_ok) n_s = 1;
+  if (w.lb == 0 && tid == 0 && (!rows_ok || w.ctx < n_s || w.ctx > cap) && a.status) {
+    atomicOr(a.status, kDevBadCtx);
+  }
+  p.n_s = n_s;
+  p.qb = qb;
+  p.cb = p.ctx_eff - n_s;
+  p.u = w.s * a.num_kv_heads + w.h;
+  p.split = !(w.lb == 0 && w.lb + w.take == w.nb);
+  return p;
+}
+
+// Start the asynchronous copy of a piece's query rows into the K-major operand
+// layout [2 halves][RP rows][128 B], row r = j*G + gi (query token j, query head
+// h*G + gi); rows >= Rs are zero-filled. Each of the 128 threads copies RC*4
+// chunks of 16 bytes.
+template <int RC>
+__device__ __forceinline__ void tc_copy_q(const DecodeArgs& a, const TcPiece& p, int h, int t,
+                                          uint8_t* qdst) {
+  constexpr int RP = 32 * RC;
+#pragma unroll
+  for (int k = 0; k < RC * 4; ++k) {
+    const int idx = t + kTcSoftmaxThreads * k;
+    const int r = idx >> 4, ch = idx & 15;
+    const bool real = r < p.Rs;
+    const int j = real ? r / a.group : 0, gi = real ? r - j * a.group : 0;
+    const uint16_t* src = static_cast<const uint16_t*>(a.q) +
+                          (static_cast<size_t>(p.qb + j) * a.num_q_heads + h * a.group + gi) * 128 + ch * 8;
+    cp_async_16(smem_addr(qdst + (ch >> 3) * (RP * 128) + r * 128 + (((ch & 7) ^ (r & 7)) << 4)),
+                real ? static_cast<const void*>(src) : a.q, real ? 16u : 0u);
+  }
+}
+
+template <int RC>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                     const DecodeArgs a) {
+  constexpr int RP = 32 * RC;                         // padded rows = the MMA's N
+  constexpr int D = 128;
+  constexpr int TILE = kBlockSize * D;                // bytes of one E5M2 (block, head) tile
+  constexpr int CHUNK_BYTES = 2 * kTcChunk * TILE;    // one ring buffer: 8 K tiles, then 8 V tiles
+  constexpr uint32_t kHalf = 128 * 128;               // one 64-dim half of a widened chunk
+  constexpr uint32_t kWide = 2 * kHalf;               // one widened chunk
+  constexpr uint32_t kRowsHalf = RP * 128;            // one 64-element half of Q or P^T
+  constexpr float kNegInf = -INFINITY;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int nbuf = a.stages;
+  const TcSmem lay = tc_smem_layout(RP, nbuf);
+  uint8_t* k16 = smem + lay.k16;
+  uint8_t* v16 = smem + lay.v16;
+  uint8_t* pst = smem + lay.p;
+  uint8_t* qst = smem + lay.q;
+  uint8_t* ring = smem + lay.ring;
+  const uint32_t bars = smem_addr(smem + lay.bars);   // full[k]: +8k, empty[k]: +8(nbuf+k)
+  const uint32_t bar_kready = bars + 16 * nbuf;        // K16 (+Q) of a chunk written (128 arrivals)
+  const uint32_t bar_pvready = bar_kready + 8;         // P^T of a chunk written (128 arrivals)
+  const uint32_t bar_sfull = bar_kready + 16;          // S^T MMAs of a chunk complete
+  const uint32_t bar_odone = bar_kready + 24;          // O^T and row-sum MMAs of a chunk complete
+  const uint32_t bar_final = bar_kready + 32;          // every MMA complete (teardown)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + lay.misc);
+  float* red_m = reinterpret_cast<float*>(smem + lay.misc + 16);   // [4][RP] per-warp row maxima
+  float* row_m = red_m + 4 * RP;                                    // [2][RP] running max, two buffers
+  long long* red = reinterpret_cast<long long*>(row_m + 2 * RP);    // [8] plan scan scratch
+  long long* plan = red + 8;                                        // total, b0, b1, s0, cum0
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(plan + 5);
+  volatile int* fin = abort_flag + 1;                               // is_last, first CTA, last CTA
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int k = 0; k < nbuf; ++k) {
+      mbar_init(bars + 8 * k, 1);
+      mbar_init(bars + 8 * (nbuf + k), kTcSoftmaxThreads / 32);
+    }
+    mbar_init(bar_kready, kTcSoftmaxThreads);
+    mbar_init(bar_pvready, kTcSoftmaxThreads);
+    mbar_init(bar_sfull, 1);
+    mbar_init(bar_odone, 1);
+    mbar_init(bar_final, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kTcMmaWarp) {
+    tmem_alloc(smem_addr(tmem_slot), kTcTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kTcProducerWarp && lane == 0) {
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
+  }
+  // The all-ones A operand of the row-sum MMA, and the running maxima.
+  if (tid < 64) reinterpret_cast<uint4*>(smem + lay.ones)[tid] = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
+  for (int r = tid; r < 2 * RP; r += blockDim.x) row_m[r] = kNegInf;
+  fence_proxy_async_smem();
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  // Everything below reads inputs a previous kernel in the stream may write.
+  pdl_wait_prior_grid();
+  plan_cta_share(a, red, plan);
+  pdl_launch_dependents();
+
+  const long long total = plan[0], b0 = plan[1], b1 = plan[2];
+  if (b0 < b1 && plan[3] >= 0) {
+    TcWalk w0;
+    {
+      const int mbs = a.max_blocks_per_seq, Hkv = a.num_kv_heads;
+      w0.b1 = b1;
+      w0.gpos = b0;
+      w0.s = static_cast<int>(plan[3]);
+      w0.ctx = a.context_lens[w0.s];
+      w0.nb = unit_blocks(w0.ctx, mbs);
+      const long long off = b0 - static_cast<long long>(Hkv) * plan[4];
+      w0.h = static_cast<int>(off / w0.nb);
+      w0.lb = static_cast<int>(off % w0.nb);
+      const long long left = b1 - b0;
+      w0.take = left < w0.nb - w0.lb ? static_cast<int>(left) : w0.nb - w0.lb;
+      w0.cofs = 0;
+    }
+
+    if (warp == kTcProducerWarp) {
+      // ------------------------------- producer ----------------------------------
+      const uint64_t pol = l2_policy_evict_first();
+      const int total_rows = a.num_blocks * a.num_kv_heads * kBlockSize;   // host guarantees < 2^31
+      TcWalk w = w0;
+      int c = 0;
+      while (!w.done()) {
+        const int nbk = w.nblk();
+        const int32_t* bt = a.block_tables + static_cast<size_t>(w.s) * a.max_blocks_per_seq + w.lb + w.cofs;
+        const int mine = lane < nbk ? bt[lane] : 0;
+        int blk[kTcChunk];
+#pragma unroll
+        for (int k = 0; k < kTcChunk; ++k) blk[k] = __shfl_sync(0xffffffffu, mine, k);
+        int good = 1;
+        if (lane == 0) {
+          const int buf = c % nbuf;
+          if (c >= nbuf && !wait_or_abort(bars + 8 * (nbuf + buf), ((c / nbuf) - 1) & 1, abort_flag)) {
+            good = 0;
+            *abort_flag = 1;
+            if (a.status) atomicOr(a.status, kDevTimeout);
+          } else {
+            const uint32_t full = bars + 8 * buf;
+            const uint32_t kdst = smem_addr(ring + buf * CHUNK_BYTES);
+            mbar_arrive_expect_tx(full, nbk * 2 * TILE);
+#pragma unroll
+            for (int k = 0; k < kTcChunk; ++k) {
+              if (k < nbk) {
+                const bool bad = static_cast<unsigned>(blk[k]) >= static_cast<unsigned>(a.num_blocks);
+                if (bad && a.status) atomicOr(a.status, kDevBadBlock);
+                // A bad block id reads a box wholly past the end: TMA fills it with zeros.
+                const int row = bad ? total_rows : (blk[k] * a.num_kv_heads + w.h) * kBlockSize;
+                tma_load_2d(kdst + k * TILE, &tm_k, 0, row, full, pol);
+                tma_load_2d(kdst + kTcChunk * TILE + k * TILE, &tm_v, 0, row, full, pol);
+              }
+            }
+          }
+        }
+        if (__shfl_sync(0xffffffffu, good, 0) == 0) break;   // chunk c was not issued
+        ++c;
+        w.advance(a);
+      }
+      // Drain: every copy issued into this CTA's shared memory lands before exit.
+      if (lane == 0) {
+        for (int k = (c > nbuf ? c - nbuf : 0); k < c; ++k) mbar_wait(bars + 8 * (k % nbuf), (k / nbuf) & 1);
+      }
+    } else if (warp == kTcMmaWarp) {
+      // ------------------------------ MMA issue -----------------------------------
+      if (lane == 0) {
+        const uint32_t id_kk = idesc_kind_f16(128, RP, 0, 0, 0);   // K-major A x K-major B
+        const uint32_t id_mk = idesc_kind_f16(128, RP, 0, 1, 0);   // MN-major A (V^T) x K-major B
+        const uint32_t t_s = tmem, t_o = tmem + kTcOCol, t_l = tmem + kTcLCol;
+        const uint32_t k16a = smem_addr(k16), v16a = smem_addr(v16), pa = smem_addr(pst), qa = smem_addr(qst);
+        const uint32_t onesa = smem_addr(smem + lay.ones);
+        TcWalk w = w0;
+        int c = 0, piece = 0;
+        bool prev = false, prev_first = false, ok = true;
+        for (;;) {
+          const bool cur = !w.done();
+          if (cur) {
+            // S^T(c) = K(c) Q^T
+            if (!(ok = wait_or_abort(bar_kready, c & 1, abort_flag))) break;
+            tc_fence_after_sync();
+            const uint32_t qsel = qa + (piece & 1) * 2 * kRowsHalf;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint64_t da = smem_desc_sw128(k16a + (kk >> 2) * kHalf + (kk & 3) * 32, 0, 1024);
+              const uint64_t db = smem_desc_sw128(qsel + (kk >> 2) * kRowsHalf + (kk & 3) * 32, 0, 1024);
+              tc_mma_f16_ss(t_s, da, db, id_kk, kk > 0 ? 1u : 0u);
+            }
+            tc_commit(bar_sfull);
+          }
+          if (prev) {
+            // O^T += V(c-1)^T P^T and, with an all-ones A, every lane's row sums += column sums of P^T
+            if (!(ok = wait_or_abort(bar_pvready, (c - 1) & 1, abort_flag))) break;
+            tc_fence_after_sync();
+            const uint32_t vsel = v16a + ((c - 1) & 1) * kWide;
+#pragma unroll
+            for (int kk = 0; kk < kTcChunk; ++kk) {
+              const uint32_t acc = (kk > 0 || !prev_first) ? 1u : 0u;
+              const uint64_t db = smem_desc_sw128(pa + (kk >> 2) * kRowsHalf + (kk & 3) * 32, 0, 1024);
+              tc_mma_f16_ss(t_o, smem_desc_sw128(vsel + kk * 2048, kHalf, 1024), db, id_mk, acc);
+              tc_mma_f16_ss(t_l, smem_desc_sw128(onesa + (kk & 3) * 32, 0, 0), db, id_kk, acc);
+            }
+            tc_commit(bar_odone);
+          }
+          if (!cur) break;
+          prev = true;
+          prev_first = w.first();
+          if (w.last()) ++piece;
+          w.advance(a);
+          ++c;
+        }
+        if (!ok) {
+          *abort_flag = 1;
+          if (a.status) atomicOr(a.status, kDevTimeout);
+        }
+        // Every MMA issued above completes before the tensor memory is released.
+        tc_commit(bar_final);
+        mbar_wait(bar_final, 0);
+      }
+      __syncwarp();
+    } else {
+      // ---------------------- widen / softmax / epilogue (warps 0..3) --------------
+      const int t = tid;   // token of the chunk, TMEM lane of S^T, head dimension of O^T
+      const uint32_t t_lane = static_cast<uint32_t>(warp * 32) << 16;
+      const int G = a.group, Hq = a.num_q_heads, R = a.rows;
+      const long long ncta = gridDim.x, cta = blockIdx.x;
+      uint16_t* out16 = static_cast<uint16_t*>(a.out);
+      bool alive = true;
+      int o_waited = -1;
+      int mp = 0;   // current running-max buffer
+
+      auto wait_bar = [&](uint32_t bar, uint32_t parity) {
+        if (!alive) return;
+        const bool ok = wait_or_abort(bar, parity, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+          alive = false;
+          *abort_flag = 1;
+          if (lane == 0 && a.status) atomicOr(a.status, kDevTimeout);
+        }
+      };
+      auto wait_o = [&](int k) {
+        if (o_waited < k) {
+          wait_bar(bar_odone, static_cast<uint32_t>(k & 1));
+          o_waited = k;
+        }
+      };
+
+      TcWalk cur = w0;
+      TcPiece pc = tc_piece(a, cur, t);
+      int c = 0, piece = 0;
+
+      // Prologue: chunk 0 and the first piece's queries.
+      {
+        tc_copy_q<RC>(a, pc, cur.h, t, qst);
+        wait_bar(bars, 0);
+        const bool valid = (t >> 4) < cur.nblk() && cur.first_token() + t < pc.ctx_eff;
+        if (alive) {
+          widen_e5m2_row(ring, k16, t, valid);
+          widen_e5m2_row(ring + kTcChunk * TILE, v16, t, valid);
+        }
+        cp_async_wait_all();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (alive) {
+          if (lane == 0) mbar_arrive(bars + 8 * nbuf);
+          mbar_arrive(bar_kready);
+        }
+      }
+
+      while (!cur.done()) {
+        TcWalk nxt = cur;
+        nxt.advance(a);
+        const bool has_next = !nxt.done();
+        const bool new_piece = has_next && nxt.first();
+        TcPiece pn = pc;
+        if (new_piece) {
+          // The other query buffer was last read by S^T MMAs of an earlier piece, all complete.
+          pn = tc_piece(a, nxt, t);
+          tc_copy_q<RC>(a, pn, nxt.h, t, qst + ((piece + 1) & 1) * 2 * kRowsHalf);
+        }
+        const int buf_next = (c + 1) % nbuf;
+        const uint8_t* ring_next = ring + buf_next * CHUNK_BYTES;
+        const bool valid_next =
+            has_next && (t >> 4) < nxt.nblk() && nxt.first_token() + t < pn.ctx_eff;
+
+        // (1) scores of chunk c
+        uint32_t sv[RC][32];
+        wait_bar(bar_sfull, c & 1);
+        if (alive) {
+          tc_fence_after_sync();
+#pragma unroll
+          for (int rc = 0; rc < RC; ++rc) tmem_ld32(tmem + t_lane + rc * 32, sv[rc]);
+        } else {
+#pragma unroll
+          for (int rc = 0; rc < RC; ++rc)
+#pragma unroll
+            for (int k = 0; k < 32; ++k) sv[rc][k] = 0u;
+        }
+
+        // (2) K of chunk c+1 (and the queries of a new piece): S(c+1) overlaps (3)
+        if (has_next) {
+          wait_bar(bars + 8 * buf_next, ((c + 1) / nbuf) & 1);
+          if (alive) widen_e5m2_row(ring_next, k16, t, valid_next);
+          cp_async_wait_all();
+          fence_proxy_async_smem();
+          tc_fence_before_sync();
+          if (alive) mbar_arrive(bar_kready);
+        }
+
+        // (3) softmax of chunk c (base 2)
+        const int p = cur.first_token() + t;
+        const bool valid = (t >> 4) < cur.nblk() && p < pc.ctx_eff;
+        // Rows that see token p: all before the draft tokens; draft token i = p - cb
+        // is seen by query token j when its tree mask has bit i (or, causally, j >= i).
+        // Padding rows (>= Rs) are kept finite and never written out.
+        unsigned long long vis = 0ull;
+        if (valid) {
+          if (p < pc.cb) {
+            vis = ~0ull;
+          } else {
+            const int i = p - pc.cb;
+            const unsigned long long pad = pc.Rs >= 64 ? 0ull : (~0ull << pc.Rs);
+            if (a.tree_masks) {
+              const unsigned long long gm = G >= 64 ? ~0ull : ((1ull << G) - 1ull);
+              unsigned long long m = 0ull;
+              for (int j = 0; j < pc.n_s; ++j)
+                if ((__ldg(a.tree_masks + pc.qb + j) >> i) & 1ull) m |= gm << (j * G);
+              vis = m | pad;
+            } else {
+              const int lo = i * G;
+              vis = (lo >= 64 ? 0ull : (~0ull << lo)) | pad;
+            }
+          }
+        }
+        float x[RC][32];
+        bool need = false;
+        {
+          const float* mrow = row_m + mp * RP;
+#pragma unroll
+          for (int rc = 0; rc < RC; ++rc)
+#pragma unroll
+            for (int k4 = 0; k4 < 8; ++k4) {
+              const float4 m4 = *reinterpret_cast<const float4*>(mrow + rc * 32 + 4 * k4);
+              const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int k = 4 * k4 + e, r = rc * 32 + k;
+                const float xv = ((vis >> r) & 1ull) ? __uint_as_float(sv[rc][k]) * a.scale_log2 : kNegInf;
+                x[rc][k] = xv;
+                need |= xv > mm[e] + kRescaleSlack;
+              }
+            }
+        }
+        if (bar_red_or(1, kTcSoftmaxThreads, need)) {
+          // Exact row maxima of this chunk over the 128 tokens; the running max of
+          // every row that grows moves there, and what was accumulated is rescaled.
+#pragma unroll
+          for (int rc = 0; rc < RC; ++rc)
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const int km = __reduce_max_sync(0xffffffffu, float_order_key(x[rc][k]));
+              if (lane == k) red_m[warp * RP + rc * 32 + k] = float_from_order_key(km);
+            }
+          named_bar_sync(2, kTcSoftmaxThreads);
+          const float* mold = row_m + mp * RP;
+          bool grows = false;
+#pragma unroll
+          for (int r = 0; r < RP; ++r) {
+            const float cm = fmaxf(fmaxf(red_m[r], red_m[RP + r]), fmaxf(red_m[2 * RP + r], red_m[3 * RP + r]));
+            grows |= cm > mold[r];
+          }
+          if (grows && !cur.first()) {
+            // O^T and the row sums hold earlier chunks of this piece.
+            wait_o(c - 1);
+            if (alive) {
+              tc_fence_after_sync();
+#pragma unroll
+              for (int rc = 0; rc < RC; ++rc) {
+                float al[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                  const int r = rc * 32 + k;
+                  const float cm =
+                      fmaxf(fmaxf(red_m[r], red_m[RP + r]), fmaxf(red_m[2 * RP + r], red_m[3 * RP + r]));
+                  al[k] = cm > mold[r] ? fast_exp2(mold[r] - cm) : 1.f;
+                }
+                uint32_t ov[32];
+                tmem_ld32(tmem + t_lane + kTcOCol + rc * 32, ov);
+#pragma unroll
+                for (int k = 0; k < 32; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * al[k]);
+                tmem_st32(tmem + t_lane + kTcOCol + rc * 32, ov);
+                tmem_ld32(tmem + t_lane + kTcLCol + rc * 32, ov);
+#pragma unroll
+                for (int k = 0; k < 32; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * al[k]);
+                tmem_st32(tmem + t_lane + kTcLCol + rc * 32, ov);
+              }
+            }
+          }
+          if (t < RP) {
+            const float cm = fmaxf(fmaxf(red_m[t], red_m[RP + t]), fmaxf(red_m[2 * RP + t], red_m[3 * RP + t]));
+            row_m[(mp ^ 1) * RP + t] = fmaxf(mold[t], cm);
+          }
+          named_bar_sync(2, kTcSoftmaxThreads);
+          mp ^= 1;
+        }
+
+        // (4) P^T of chunk c: K-major [token half][row][128 B]; the buffer was read by O(c-1).
+        if (c > 0) wait_o(c - 1);
+        if (alive) {
+          const float* mrow = row_m + mp * RP;
+          uint8_t* prow = pst + (t >> 6) * kRowsHalf + (t & 7) * 2;
+          const int tch = (t & 63) >> 3;
+#pragma unroll
+          for (int rc = 0; rc < RC; ++rc)
+#pragma unroll
+            for (int k4 = 0; k4 < 8; ++k4) {
+              const float4 m4 = *reinterpret_cast<const float4*>(mrow + rc * 32 + 4 * k4);
+              const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int k = 4 * k4 + e, r = rc * 32 + k;
+                const float mu = mm[e] == kNegInf ? 0.f : mm[e];
+                const float pv = fast_exp2(x[rc][k] - mu);
+                *reinterpret_cast<__half*>(prow + r * 128 + ((tch ^ (r & 7)) << 4)) = __float2half_rn(pv);
+              }
+            }
+        }
+
+        // (5) V of chunk c+1 (its buffer was read by O(c-1)); release the ring buffer.
+        if (has_next) {
+          if (alive) widen_e5m2_row(ring_next + kTcChunk * TILE, v16 + ((c + 1) & 1) * kWide, t, valid_next);
+          __syncwarp();
+          if (alive && lane == 0) mbar_arrive(bars + 8 * (nbuf + buf_next));
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        if (alive) mbar_arrive(bar_pvready);
+
+        // (6) end of a piece: normalise and write, or write the split partial.
+        if (cur.last()) {
+          wait_o(c);
+          if (alive) tc_fence_after_sync();
+          float* slot = a.partials + static_cast<size_t>(pc.u + cta) * a.slot_floats;
+          const int ooff = partial_o_offset(R);
+#pragma unroll
+          for (int rc = 0; rc < RC; ++rc) {
+            uint32_t ov[32], lv[32];
+            if (alive) {
+              tmem_ld32(tmem + t_lane + kTcOCol + rc * 32, ov);
+              tmem_ld32(tmem + t_lane + kTcLCol + rc * 32, lv);
+            } else {
+#pragma unroll
+              for (int k = 0; k < 32; ++k) ov[k] = lv[k] = 0u;
+            }
+            int j = (rc * 32) / G, gi = rc * 32 - j * G;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const int r = rc * 32 + k;
+              if (r < pc.Rs) {
+                const float o = __uint_as_float(ov[k]);
+                if (!pc.split) {
+                  const float L = __uint_as_float(lv[k]);
+                  const float inv = L > 0.f ? 1.f / L : 0.f;
+                  const size_t dst = (static_cast<size_t>(pc.qb + j) * Hq + cur.h * G + gi) * D + t;
+                  out16[dst] = __half_as_ushort(__float2half_rn(o * inv));
+                } else {
+                  slot[ooff + r * D + t] = o;
+                }
+              }
+              if (++gi == G) {
+                gi = 0;
+                ++j;
+              }
+            }
+            if (pc.split && warp == 0) {
+              // Row rc*32 + lane: its running max and sum.
+              float v[32];
+#pragma unroll
+              for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(lv[k]);
+              const float lsum = select_lane32(v, lane);
+              const int r = rc * 32 + lane;
+              if (r < R) {
+                slot[r] = row_m[mp * RP + r];
+                slot[R + r] = lsum;
+              }
+            }
+          }
+          if (pc.split) {
+            finish_split_piece<kKvE5m2, D>(a, pc.u, cur.gpos - cur.lb, cur.nb, total, ncta, pc.Rs, pc.qb,
+                                           cur.h, t, kTcSoftmaxThreads, 3, fin);
+          }
+          // The next piece starts from an empty running max.
+          named_bar_sync(2, kTcSoftmaxThreads);
+          if (t < RP) row_m[mp * RP + t] = kNegInf;
+          named_bar_sync(2, kTcSoftmaxThreads);
+        }
+
+        if (new_piece) {
+          pc = pn;
+          ++piece;
+        }
+        cur = nxt;
+        ++c;
+      }
+    }
+  }
+
+  // Teardown: every role is done with the tensor memory.
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kTcMmaWarp) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTcTmemCols);
+  }
+}
+
+}  // namespace pkv

@@ -49,6 +49,8 @@ struct DecodeArgs {
 
 // Shared-memory and launch geometry of one decode instantiation.
 struct DecodeGeometry {
+  int tc;             // 1: tcgen05 kernel (then rc = 32-row column groups, stages = ring buffers)
+  int rc;
   int ntw;            // n-tiles (8 rows each) per consumer warp
   int warps_rows;
   int warps_blocks;
@@ -87,6 +89,37 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int kv, int d, int ntw,
   s.total = s.misc + 256;   // block-reduce scratch, CTA plan, abort flag
   return s;
 }
+
+// Tensor-core (tcgen05) decode kernel for wide units: 128-token chunks (8 KV
+// blocks, the MMA's M), 4 softmax warps, 1 MMA-issue warp, 1 TMA warp.
+constexpr int kTcChunk = 8;          // KV blocks per chunk
+constexpr int kTcThreads = 192;
+constexpr int kTcTmemCols = 256;     // S^T at columns [0, 64), O^T at [64, 128), row sums at [128, 192)
+
+// Shared memory of the tcgen05 kernel for rows_pad (32 or 64) query rows and
+// nbuf ring buffers of one E5M2 chunk each (8 K tiles + 8 V tiles, 32 KB).
+struct TcSmem {
+  size_t k16, v16, p, q, ones, ring, bars, misc, total;
+};
+__host__ __device__ inline TcSmem tc_smem_layout(int rows_pad, int nbuf) {
+  TcSmem s{};
+  const size_t wide = 128 * 128 * 2;          // one chunk of K or V widened to fp16
+  const size_t rows_bytes = (size_t)rows_pad * 256;
+  s.k16 = 0;
+  s.v16 = s.k16 + wide;                        // two buffers
+  s.p = s.v16 + 2 * wide;
+  s.q = s.p + rows_bytes;                      // two buffers
+  s.ones = s.q + 2 * rows_bytes;               // one 1024-byte atom of fp16 1.0
+  s.ring = s.ones + 1024;
+  s.bars = s.ring + (size_t)nbuf * 2 * kTcChunk * kBlockSize * 128;
+  s.misc = s.bars + (size_t)(2 * nbuf + 5) * 8;
+  s.misc = (s.misc + 15) & ~(size_t)15;
+  // TMEM address, per-warp row maxima [4][rows_pad], running max [2][rows_pad],
+  // plan scan scratch, plan, abort flag and finish flags.
+  s.total = s.misc + 16 + (size_t)6 * rows_pad * 4 + 8 * 8 + 5 * 8 + 16 * 4;
+  return s;
+}
+const void* decode_tc_kernel_ptr(int kv, int rc);
 
 // Kernel entry points, one set per KV dtype translation unit (nullptr if the
 // head size / rows-per-warp combination is not instantiated).

@@ -69,9 +69,13 @@ def full_check(orc, w, dev, *, seqs=None, values_device="cpu", check_cache=True,
     """CUDA path vs oracle on workload w. Cache images must match bit for bit; outputs
     within tolerance (all sequences, or the sampled ones in `seqs`)."""
     vals = wl.token_values(w, device=values_device)
+    return check_values(orc, w, vals, dev, seqs=seqs, check_cache=check_cache, threads=threads)
+
+
+def check_values(orc, w, vals, dev, *, seqs=None, check_cache=True, threads=None):
+    """full_check on given token values (q, k_all, v_all, slot_all)."""
     kc, vc, out = cuda_path(w, vals, dev)
-    if values_device != "cpu":
-        vals = {k: v.cpu() for k, v in vals.items()}
+    vals = {k: v.cpu() for k, v in vals.items()}
     okc, ovc = oracle_caches(orc, w, vals)
     if check_cache:
         assert np.array_equal(cache_bytes(kc), okc), "K cache bytes differ from the oracle's"

@@ -94,6 +94,8 @@ SHAPES = [
     (16, 2, 2),    # rows 16
     (12, 4, 5),    # rows 15 (ragged tile)
     (64, 8, 4),    # 70B verify, rows 32
+    (24, 1, 1),    # rows 24 (padded to 32 on the tensor-core path)
+    (8, 1, 5),     # rows 40 (padded to 64)
     (16, 1, 4),    # rows 64
 ]
 
@@ -149,6 +151,52 @@ def test_bad_block_and_context_are_flagged_not_faulted(orc, dev, gpu):
     okc, ovc = gpu.oracle_caches(orc, w, vals)
     ref, _, _ = gpu.oracle_attention(orc, w, vals, okc, ovc, seqs=[1])
     gpu.compare(out, ref, rows=[2, 3])
+
+
+def test_bad_block_and_context_flagged_on_wide_units(orc, dev, gpu):
+    """The same checks on a unit of 32 rows over an E5M2 cache (tensor-core kernel)."""
+    import paged_kv_cache_252_gb300 as pkv
+    w = wl.custom(num_seqs=3, num_q_heads=64, num_kv_heads=8, head_size=128, q_per_seq=4,
+                  kv_dtype="e5m2", context_lens=[200, 400, 9], seed=4)
+    vals = wl.token_values(w)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    kc, vc, _ = gpu.cuda_path(w, vals, dev, status=status)
+    assert int(status.item()) == 0
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    bt[0, 1] = w.num_blocks + 5          # out-of-range physical block
+    cl = torch.from_numpy(w.context_lens).to(dev)
+    cl[2] = 1                            # shorter than q_per_seq
+    q = vals["q"].to(dev)
+    out = torch.empty_like(q)
+    pkv.paged_attention_decode(out, q, kc, vc, bt, cl, 4, w.scale, device_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 0x2 and int(status.item()) & 0x4
+    assert not int(status.item()) & 0x8
+    okc, ovc = gpu.oracle_caches(orc, w, vals)
+    ref, _, _ = gpu.oracle_attention(orc, w, vals, okc, ovc, seqs=[1])
+    gpu.compare(out, ref, rows=[4, 5, 6, 7])
+
+
+def _ramp_keys(w, vals, slope):
+    """Scale each sequence's keys by 1 + slope*position: later tokens score far
+    higher, so the running max of every row keeps moving after the first chunk."""
+    starts = w.seq_starts()
+    k = vals["k_all"].float()
+    for s in range(w.num_seqs):
+        n = int(starts[s + 1] - starts[s])
+        f = 1.0 + slope * torch.arange(n, dtype=torch.float32)
+        k[starts[s]:starts[s + 1]] *= f[:, None, None]
+    vals["k_all"] = k.to(vals["k_all"].dtype)
+    return vals
+
+
+@pytest.mark.parametrize("kv,Hq,Hkv,n", [("e5m2", 64, 8, 4), ("e5m2", 8, 1, 5), ("fp16", 32, 8, 1),
+                                         ("bf16", 64, 8, 4)])
+def test_rising_scores_move_the_running_max(orc, dev, gpu, kv, Hq, Hkv, n):
+    w = wl.custom(num_seqs=4, num_q_heads=Hq, num_kv_heads=Hkv, head_size=128, q_per_seq=n,
+                  kv_dtype=kv, context_lens=[900, 300, 129, 2000], seed=77)
+    vals = _ramp_keys(w, wl.token_values(w), 1.0 / 32)
+    gpu.check_values(orc, w, vals, dev)
 
 
 def test_empty_batch_is_a_no_op(dev):
