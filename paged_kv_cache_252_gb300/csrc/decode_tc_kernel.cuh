@@ -15,31 +15,37 @@
 // Work is done in chunks of 8 KV blocks (128 tokens) of one unit.
 //   S^T (128 tokens x RP rows)  = K_chunk (128 x 128, fp16) . Q^T      [TMEM, fp32]
 //   O^T (128 dims   x RP rows) += V_chunk^T (128 x 128 tokens) . P^T   [TMEM, fp32]
-// with RP = 32 or 64 (rows padded; padding rows of Q are zero).
+// with RP = 32 or 64 (rows padded; padding rows of Q are zero). K_chunk is
+// the A operand straight from tensor memory (token t in lane t); Q^T, V^T and
+// P^T come from shared memory.
 //
-// Warp roles (192 threads, one CTA per SM):
-//   warp 5      : TMA producer. Copies the chunk's K and V tiles (E5M2,
+// Warp roles (320 threads, one CTA per SM):
+//   warp 9      : TMA producer. Copies the chunk's K and V tiles (E5M2,
 //                 [16 tokens][128 bytes], 128-byte swizzle) into a ring of
 //                 chunk buffers.
-//   warp 4      : one thread issues every tcgen05.mma and commits each group
+//   warp 8      : one thread issues every tcgen05.mma and commits each group
 //                 to an mbarrier; the warp owns the tensor-memory allocation.
-//   warps 0..3  : thread t owns token t of the chunk, which is also TMEM lane
-//                 t of S^T and head dimension t of O^T. Each chunk: widen the
-//                 next chunk's K and V rows to fp16 in the MMA operand layout,
-//                 read its own 32/64 scores from TMEM, mask, exponentiate
-//                 against the rows' running max, keep per-thread partial sums,
-//                 write P^T; at the end of a unit piece, reduce the sums over
-//                 the CTA, read O^T from TMEM and write the output or a split
-//                 partial.
+//   warps 0..7  : warp w reads TMEM lane quarter q = w % 4, so its thread owns
+//                 token t = 32q + lane of the chunk (TMEM lane t of S^T and of
+//                 K, head dimension t of O^T) and half h = w / 4 of the unit's
+//                 rows and of the head dimensions. Each chunk: widen half h of
+//                 the next chunk's K row of token t to fp16 into TMEM and of its
+//                 V row into the shared-memory operand layout, read its scores
+//                 from TMEM, mask, exponentiate against the rows' running max,
+//                 add to its partial row sums and write P^T; at the end of a
+//                 unit piece reduce the sums over the CTA, read O^T from TMEM
+//                 and write the output or a split partial.
 // The running max of a row moves only when a score exceeds it by more than
 // kRescaleSlack (base 2): then the chunk's exact row maxima are reduced across
-// the 128 threads and O^T and the partial sums are rescaled. Probabilities are
-// therefore at most 2^kRescaleSlack, well inside fp16.
+// the softmax threads and O^T and the partial sums are rescaled. Probabilities are
+// therefore at most 2^kRescaleSlack, well inside fp16. Everything that runs once
+// per piece or on that rare path lives in out-of-line functions, so the per-chunk
+// loop stays small enough for the instruction cache.
 //
-// Pipeline per chunk c (softmax warps): wait S(c); widen K(c+1) (+ Q of a new
+// Pipeline per chunk c (softmax warps): read S(c); widen K(c+1) (+ Q of a new
 // piece) -> the MMA thread issues S(c+1) while the softmax of chunk c runs;
 // wait O(c-1); write P(c); widen V(c+1) -> the MMA thread issues O(c).
-// K16, P and the S^T columns are single-buffered, V16 and Q double-buffered.
+// P^T is single-buffered; K (TMEM), S^T (TMEM), V16 and Q double-buffered.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -53,12 +59,17 @@
 
 namespace pkv {
 
-constexpr int kTcSoftmaxThreads = 128;
-constexpr int kTcMmaWarp = 4;
-constexpr int kTcProducerWarp = 5;
-constexpr uint32_t kTcOCol = 64;             // first TMEM column of O^T
-constexpr uint32_t kTcLCol = 128;            // first TMEM column of the row sums
+constexpr int kTcSoftmaxThreads = 256;       // warps 0..7
+constexpr int kTcMmaWarp = 8;
+constexpr int kTcProducerWarp = 9;
+constexpr uint32_t kTcSCols = 64;            // TMEM columns per S^T buffer (two buffers from column 0)
+constexpr uint32_t kTcOCol = 128;            // first TMEM column of O^T
+constexpr uint32_t kTcKCol = 256;            // first TMEM column of the K buffers (64 columns each)
 constexpr float kRescaleSlack = 8.f;         // base-2 headroom before the running max moves
+// Running max of a row that has seen no visible score yet. Finite, so that
+// x - max stays -inf for masked scores and needs no special case; any visible
+// score exceeds it by more than the slack, which moves the max first.
+constexpr float kNoMax = -1.0e30f;
 
 // Order-preserving map between floats and signed ints, for integer max reductions.
 __device__ __forceinline__ int float_order_key(float f) {
@@ -80,16 +91,32 @@ __device__ __forceinline__ float select_lane32(float (&v)[32], int lane) {
   return v[0];
 }
 
-// Widen token row t of an E5M2 chunk (128 rows x 128 bytes, 128-byte swizzle,
-// as TMA wrote it) into the fp16 operand layout: two 64-dimension halves of
-// [128 rows][128 bytes], same swizzle. E5M2 byte b is the fp16 pattern b << 8.
-// Rows that are not part of the sequence are written as zeros.
-__device__ __forceinline__ void widen_e5m2_row(const uint8_t* src, uint8_t* dst, int t, bool valid) {
+// Bounded mbarrier wait in which a waiting warp sleeps (takes no issue slots)
+// until the phase completes; it gives up after kWaitLimitNs or once another
+// warp of the CTA has given up (abort flag).
+constexpr uint32_t kTcSleepNs = 1000000;
+__device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait_sleep(bar, parity, kTcSleepNs)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, kTcSleepNs)) return true;
+    if (*abort_flag || global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// Widen half `half` (dimensions 64*half .. 64*half+63) of token row t of an
+// E5M2 chunk (128 rows x 128 bytes, 128-byte swizzle, as TMA wrote it) into the
+// fp16 operand layout: two 64-dimension halves of [128 rows][128 bytes], same
+// swizzle. E5M2 byte b is the fp16 pattern b << 8. Rows that are not part of
+// the sequence are written as zeros.
+__device__ __forceinline__ void widen_e5m2_half_row(const uint8_t* src, uint8_t* dst, int t, int half,
+                                                    bool valid) {
   const int sw = t & 7;
   const uint8_t* s = src + t * 128;
-  uint8_t* d = dst + t * 128;
+  uint8_t* d = dst + half * (128 * 128) + t * 128;
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
+  for (int cc = 0; cc < 4; ++cc) {
+    const int c = 4 * half + cc;
     uint4 v = make_uint4(0, 0, 0, 0);
     if (valid) v = *reinterpret_cast<const uint4*>(s + ((c ^ sw) << 4));
     uint4 lo, hi;
@@ -101,11 +128,54 @@ __device__ __forceinline__ void widen_e5m2_row(const uint8_t* src, uint8_t* dst,
     hi.y = __byte_perm(v.z, 0, 0x3424);
     hi.z = __byte_perm(v.w, 0, 0x1404);
     hi.w = __byte_perm(v.w, 0, 0x3424);
-    uint8_t* dh = d + (c >> 2) * (128 * 128);
-    const int c16 = (2 * c) & 7;
-    *reinterpret_cast<uint4*>(dh + ((c16 ^ sw) << 4)) = lo;
-    *reinterpret_cast<uint4*>(dh + (((c16 + 1) ^ sw) << 4)) = hi;
+    *reinterpret_cast<uint4*>(d + (((2 * cc) ^ sw) << 4)) = lo;
+    *reinterpret_cast<uint4*>(d + (((2 * cc + 1) ^ sw) << 4)) = hi;
   }
+}
+
+// Widen half `half` (dimensions 64*half .. 64*half+63) of token row t of an
+// E5M2 chunk (as TMA wrote it, see above) to fp16 pairs in tensor memory:
+// column j of the K buffer = dimensions 2j, 2j+1 (the A operand layout of
+// tcgen05.mma). taddr addresses this warp's lane quarter and the K buffer.
+__device__ __forceinline__ void widen_e5m2_half_row_tmem(const uint8_t* src, int t, int half, bool valid,
+                                                         uint32_t taddr) {
+  const int sw = t & 7;
+  const uint8_t* s = src + t * 128;
+  uint32_t v[32];
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    const int c = 4 * half + cc;
+    uint4 x = make_uint4(0, 0, 0, 0);
+    if (valid) x = *reinterpret_cast<const uint4*>(s + ((c ^ sw) << 4));
+    v[8 * cc + 0] = __byte_perm(x.x, 0, 0x1404);
+    v[8 * cc + 1] = __byte_perm(x.x, 0, 0x3424);
+    v[8 * cc + 2] = __byte_perm(x.y, 0, 0x1404);
+    v[8 * cc + 3] = __byte_perm(x.y, 0, 0x3424);
+    v[8 * cc + 4] = __byte_perm(x.z, 0, 0x1404);
+    v[8 * cc + 5] = __byte_perm(x.z, 0, 0x3424);
+    v[8 * cc + 6] = __byte_perm(x.w, 0, 0x1404);
+    v[8 * cc + 7] = __byte_perm(x.w, 0, 0x3424);
+  }
+  tmem_st32(taddr + 32 * half, v);
+}
+
+// v[k] holds this lane's value for row k (N = 16 or 32 rows); returns the sum
+// over the warp's 32 lanes of row (lane % N) (halving exchange, then the halves).
+template <int N>
+__device__ __forceinline__ float warp_rows_sum(float (&v)[N], int lane) {
+#pragma unroll
+  for (int s = N / 2; s >= 1; s >>= 1) {
+    const bool up = (lane & s) != 0;
+#pragma unroll
+    for (int k = 0; k < s; ++k) {
+      const float send = up ? v[k] : v[k + s];
+      const float keep = up ? v[k + s] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+    }
+  }
+#pragma unroll
+  for (int s = N; s < 32; s <<= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], s);
+  return v[0];
 }
 
 // Position in a CTA's share: the current piece (unit (s, h), blocks
@@ -178,15 +248,13 @@ __device__ __forceinline__ TcPiece tc_piece(const DecodeArgs& a, const TcWalk& w
 
 // Start the asynchronous copy of a piece's query rows into the K-major operand
 // layout [2 halves][RP rows][128 B], row r = j*G + gi (query token j, query head
-// h*G + gi); rows >= Rs are zero-filled. Each of the 128 threads copies RC*4
-// chunks of 16 bytes.
-template <int RC>
-__device__ __forceinline__ void tc_copy_q(const DecodeArgs& a, const TcPiece& p, int h, int t,
-                                          uint8_t* qdst) {
-  constexpr int RP = 32 * RC;
+// h*G + gi); rows >= Rs are zero-filled. Each of the NT threads copies
+// RP*16/NT chunks of 16 bytes.
+template <int RP, int NT>
+__device__ __forceinline__ void tc_copy_q(const DecodeArgs& a, const TcPiece& p, int h, int t, uint8_t* qdst) {
 #pragma unroll
-  for (int k = 0; k < RC * 4; ++k) {
-    const int idx = t + kTcSoftmaxThreads * k;
+  for (int k = 0; k < RP * 16 / NT; ++k) {
+    const int idx = t + NT * k;
     const int r = idx >> 4, ch = idx & 15;
     const bool real = r < p.Rs;
     const int j = real ? r / a.group : 0, gi = real ? r - j * a.group : 0;
@@ -197,11 +265,142 @@ __device__ __forceinline__ void tc_copy_q(const DecodeArgs& a, const TcPiece& p,
   }
 }
 
+// Rows that see token p of a piece, as a bit mask over rows r0 .. r0+63: every
+// row for positions before the draft tokens; draft token i = p - cb is seen by
+// query token j when its tree mask has bit i (or, causally, j >= i). Padding
+// rows (>= Rs) are kept finite and never written out. Not part of the sequence: none.
+__device__ __forceinline__ unsigned long long tc_row_visibility(const DecodeArgs& a, const TcPiece& pc, int p,
+                                                             bool valid, int r0) {
+  if (!valid) return 0ull;
+  if (p < pc.cb) return ~0ull;
+  const int G = a.group;
+  const int i = p - pc.cb;
+  const unsigned long long pad = pc.Rs >= 64 ? 0ull : (~0ull << pc.Rs);
+  unsigned long long vis;
+  if (a.tree_masks) {
+    const unsigned long long gm = G >= 64 ? ~0ull : ((1ull << G) - 1ull);
+    unsigned long long m = 0ull;
+    for (int j = 0; j < pc.n_s; ++j)
+      if ((__ldg(a.tree_masks + pc.qb + j) >> i) & 1ull) m |= gm << (j * G);
+    vis = m | pad;
+  } else {
+    const int lo = i * G;
+    vis = (lo >= 64 ? 0ull : (~0ull << lo)) | pad;
+  }
+  return vis >> r0;
+}
+
+// Chunk maximum of row r over the four lane quarters.
+__device__ __forceinline__ float tc_chunk_max(const float* red_m, int RP, int r) {
+  return fmaxf(fmaxf(red_m[r], red_m[RP + r]), fmaxf(red_m[2 * RP + r], red_m[3 * RP + r]));
+}
+
+// Rare path, part 1: the chunk's exact maxima of this thread's rows over the
+// 128 tokens into red_m[quarter][row]. Returns whether any of them exceeds the
+// running max (uniform within the warp: its lanes share the rows).
+template <int RH>
+__device__ __forceinline__ bool tc_chunk_maxima(const float* x, float* red_m, const float* mold, int RP, int q,
+                                             int r0, int lane) {
+#pragma unroll
+  for (int k = 0; k < RH; ++k) {
+    const int km = __reduce_max_sync(0xffffffffu, float_order_key(x[k]));
+    if (lane == k) red_m[q * RP + r0 + k] = float_from_order_key(km);
+  }
+  named_bar_sync(2, kTcSoftmaxThreads);
+  bool grows = false;
+#pragma unroll
+  for (int k = 0; k < RH; ++k) grows |= tc_chunk_max(red_m, RP, r0 + k) > mold[r0 + k];
+  return grows;
+}
+
+// Rare path, part 2: rescale this warp's columns of O^T by 2^(old max - new
+// max) (rescale: they hold earlier chunks of the piece), and write the new
+// running maxima into the other buffer.
+template <int RH>
+__device__ __forceinline__ void tc_move_maxima(uint32_t t_cols, bool rescale, const float* red_m,
+                                               const float* mold, float* mnew, int RP, int r0, int tid) {
+  if (rescale) {
+    tc_fence_after_sync();
+    uint32_t v[RH];
+    tmem_ld<RH>(t_cols + kTcOCol, v);
+#pragma unroll
+    for (int k = 0; k < RH; ++k) {
+      const float cm = tc_chunk_max(red_m, RP, r0 + k);
+      const float al = cm > mold[r0 + k] ? fast_exp2(mold[r0 + k] - cm) : 1.f;
+      v[k] = __float_as_uint(__uint_as_float(v[k]) * al);
+    }
+    tmem_st<RH>(t_cols + kTcOCol, v);
+  }
+  if (tid < RP) mnew[tid] = fmaxf(mold[tid], tc_chunk_max(red_m, RP, tid));
+  named_bar_sync(2, kTcSoftmaxThreads);
+}
+
+// End of a piece: O^T of this thread's rows (head dimension t) from TMEM,
+// the row sums from red_l ([quarter][row] partial sums); the normalised
+// output, or the split partial (o, and m / l of each row).
+template <int RH>
+__device__ __forceinline__ void tc_piece_output(const DecodeArgs& a, uint32_t t_cols, bool alive,
+                                                const TcPiece& pc, int h, int r0, int t, int q, int lane,
+                                                const float* mcur, const float* red_l, long long cta) {
+  constexpr int D = 128;
+  const int G = a.group, Hq = a.num_q_heads, R = a.rows;
+  const int RP = 2 * RH;
+  uint32_t ov[RH];
+  if (alive) {
+    tc_fence_after_sync();
+    tmem_ld<RH>(t_cols + kTcOCol, ov);
+  } else {
+#pragma unroll
+    for (int k = 0; k < RH; ++k) ov[k] = 0u;
+  }
+  float* slot = a.partials + static_cast<size_t>(pc.u + cta) * a.slot_floats;
+  const int ooff = partial_o_offset(R);
+  uint16_t* out16 = static_cast<uint16_t*>(a.out);
+  int j = r0 / G, gi = r0 - j * G;
+#pragma unroll
+  for (int k = 0; k < RH; ++k) {
+    const int r = r0 + k;
+    if (r < pc.Rs) {
+      const float o = __uint_as_float(ov[k]);
+      if (!pc.split) {
+        const float L = (red_l[r] + red_l[RP + r]) + (red_l[2 * RP + r] + red_l[3 * RP + r]);
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        const size_t dst = (static_cast<size_t>(pc.qb + j) * Hq + h * G + gi) * D + t;
+        out16[dst] = __half_as_ushort(__float2half_rn(o * inv));
+      } else {
+        slot[ooff + r * D + t] = o;
+      }
+    }
+    if (++gi == G) {
+      gi = 0;
+      ++j;
+    }
+  }
+  if (pc.split && q == 0 && lane < RH) {
+    const int r = r0 + lane;
+    if (r < R) {
+      slot[r] = mcur[r];
+      slot[R + r] = (red_l[r] + red_l[RP + r]) + (red_l[2 * RP + r] + red_l[3 * RP + r]);
+    }
+  }
+}
+
+__device__ __forceinline__ void tc_finish_split(const DecodeArgs& a, const TcPiece& pc, long long ustart, int nb,
+                                             long long total, long long ncta, int h, int tid, volatile int* fin) {
+  finish_split_piece<kKvE5m2, 128>(a, pc.u, ustart, nb, total, ncta, pc.Rs, pc.qb, h, tid, kTcSoftmaxThreads,
+                                   3, fin);
+}
+
+__device__ __forceinline__ void tc_plan(const DecodeArgs& a, long long* red, long long* plan) {
+  plan_cta_share(a, red, plan);
+}
+
 template <int RC>
 __global__ void __launch_bounds__(kTcThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                     const DecodeArgs a) {
+                     const __grid_constant__ DecodeArgs a) {
   constexpr int RP = 32 * RC;                         // padded rows = the MMA's N
+  constexpr int RH = RP / 2;                          // rows per softmax thread
   constexpr int D = 128;
   constexpr int TILE = kBlockSize * D;                // bytes of one E5M2 (block, head) tile
   constexpr int CHUNK_BYTES = 2 * kTcChunk * TILE;    // one ring buffer: 8 K tiles, then 8 V tiles
@@ -215,22 +414,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   const int nbuf = a.stages;
   const TcSmem lay = tc_smem_layout(RP, nbuf);
-  uint8_t* k16 = smem + lay.k16;
   uint8_t* v16 = smem + lay.v16;
   uint8_t* pst = smem + lay.p;
   uint8_t* qst = smem + lay.q;
   uint8_t* ring = smem + lay.ring;
   const uint32_t bars = smem_addr(smem + lay.bars);   // full[k]: +8k, empty[k]: +8(nbuf+k)
-  const uint32_t bar_kready = bars + 16 * nbuf;        // K16 (+Q) of a chunk written (128 arrivals)
-  const uint32_t bar_pvready = bar_kready + 8;         // P^T of a chunk written (128 arrivals)
+  const uint32_t bar_kready = bars + 16 * nbuf;        // K (+Q) of a chunk written (256 arrivals)
+  const uint32_t bar_pvready = bar_kready + 8;         // P^T (+V16 of the next chunk) written (256 arrivals)
   const uint32_t bar_sfull = bar_kready + 16;          // S^T MMAs of a chunk complete
-  const uint32_t bar_odone = bar_kready + 24;          // O^T and row-sum MMAs of a chunk complete
+  const uint32_t bar_odone = bar_kready + 24;          // O^T MMAs of a chunk complete
   const uint32_t bar_final = bar_kready + 32;          // every MMA complete (teardown)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + lay.misc);
-  float* red_m = reinterpret_cast<float*>(smem + lay.misc + 16);   // [4][RP] per-warp row maxima
-  float* row_m = red_m + 4 * RP;                                    // [2][RP] running max, two buffers
-  long long* red = reinterpret_cast<long long*>(row_m + 2 * RP);    // [8] plan scan scratch
-  long long* plan = red + 8;                                        // total, b0, b1, s0, cum0
+  float* red_m = reinterpret_cast<float*>(smem + lay.misc + 16);   // [4][RP] per-quarter row maxima
+  float* red_l = red_m + 4 * RP;                                    // [4][RP] per-quarter row sums
+  float* row_m = red_l + 4 * RP;                                    // [2][RP] running max, two buffers
+  long long* red = reinterpret_cast<long long*>(row_m + 2 * RP);    // [16] plan scan scratch, one per warp
+  long long* plan = red + 16;                                       // total, b0, b1, s0, cum0
   volatile int* abort_flag = reinterpret_cast<volatile int*>(plan + 5);
   volatile int* fin = abort_flag + 1;                               // is_last, first CTA, last CTA
 
@@ -239,7 +438,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (tid == 0) {
     for (int k = 0; k < nbuf; ++k) {
       mbar_init(bars + 8 * k, 1);
-      mbar_init(bars + 8 * (nbuf + k), kTcSoftmaxThreads / 32);
+      mbar_init(bars + 8 * (nbuf + k), kTcSoftmaxThreads / 32);   // one arrival per softmax warp
     }
     mbar_init(bar_kready, kTcSoftmaxThreads);
     mbar_init(bar_pvready, kTcSoftmaxThreads);
@@ -257,10 +456,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
   }
-  // The all-ones A operand of the row-sum MMA, and the running maxima.
-  if (tid < 64) reinterpret_cast<uint4*>(smem + lay.ones)[tid] = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
-  for (int r = tid; r < 2 * RP; r += blockDim.x) row_m[r] = kNegInf;
-  fence_proxy_async_smem();
+  for (int r = tid; r < 2 * RP; r += blockDim.x) row_m[r] = kNoMax;
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -268,7 +464,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   // Everything below reads inputs a previous kernel in the stream may write.
   pdl_wait_prior_grid();
-  plan_cta_share(a, red, plan);
+  tc_plan(a, red, plan);
   pdl_launch_dependents();
 
   const long long total = plan[0], b0 = plan[1], b1 = plan[2];
@@ -305,7 +501,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int good = 1;
         if (lane == 0) {
           const int buf = c % nbuf;
-          if (c >= nbuf && !wait_or_abort(bars + 8 * (nbuf + buf), ((c / nbuf) - 1) & 1, abort_flag)) {
+          if (c >= nbuf && !tc_wait(bars + 8 * (nbuf + buf), ((c / nbuf) - 1) & 1, abort_flag)) {
             good = 0;
             *abort_flag = 1;
             if (a.status) atomicOr(a.status, kDevTimeout);
@@ -337,40 +533,39 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else if (warp == kTcMmaWarp) {
       // ------------------------------ MMA issue -----------------------------------
       if (lane == 0) {
-        const uint32_t id_kk = idesc_kind_f16(128, RP, 0, 0, 0);   // K-major A x K-major B
-        const uint32_t id_mk = idesc_kind_f16(128, RP, 0, 1, 0);   // MN-major A (V^T) x K-major B
-        const uint32_t t_s = tmem, t_o = tmem + kTcOCol, t_l = tmem + kTcLCol;
-        const uint32_t k16a = smem_addr(k16), v16a = smem_addr(v16), pa = smem_addr(pst), qa = smem_addr(qst);
-        const uint32_t onesa = smem_addr(smem + lay.ones);
+        const uint32_t id_s = idesc_kind_f16(128, RP, 0, 0, 0);   // K (TMEM, K-major) x Q^T (K-major)
+        const uint32_t id_o = idesc_kind_f16(128, RP, 0, 1, 0);   // V^T (MN-major) x P^T (K-major)
+        const uint32_t t_o = tmem + kTcOCol;
+        const uint32_t v16a = smem_addr(v16), pa = smem_addr(pst), qa = smem_addr(qst);
         TcWalk w = w0;
         int c = 0, piece = 0;
         bool prev = false, prev_first = false, ok = true;
         for (;;) {
           const bool cur = !w.done();
           if (cur) {
-            // S^T(c) = K(c) Q^T
-            if (!(ok = wait_or_abort(bar_kready, c & 1, abort_flag))) break;
+            // S^T(c) = K(c) Q^T: S and K buffer c % 2
+            if (!(ok = tc_wait(bar_kready, c & 1, abort_flag))) break;
             tc_fence_after_sync();
             const uint32_t qsel = qa + (piece & 1) * 2 * kRowsHalf;
+            const uint32_t t_s = tmem + (c & 1) * kTcSCols;
+            const uint32_t t_k = tmem + kTcKCol + (c & 1) * 64;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-              const uint64_t da = smem_desc_sw128(k16a + (kk >> 2) * kHalf + (kk & 3) * 32, 0, 1024);
               const uint64_t db = smem_desc_sw128(qsel + (kk >> 2) * kRowsHalf + (kk & 3) * 32, 0, 1024);
-              tc_mma_f16_ss(t_s, da, db, id_kk, kk > 0 ? 1u : 0u);
+              tc_mma_f16_ts(t_s, t_k + kk * 8, db, id_s, kk > 0 ? 1u : 0u);
             }
             tc_commit(bar_sfull);
           }
           if (prev) {
-            // O^T += V(c-1)^T P^T and, with an all-ones A, every lane's row sums += column sums of P^T
-            if (!(ok = wait_or_abort(bar_pvready, (c - 1) & 1, abort_flag))) break;
+            // O^T += V(c-1)^T P^T
+            if (!(ok = tc_wait(bar_pvready, (c - 1) & 1, abort_flag))) break;
             tc_fence_after_sync();
             const uint32_t vsel = v16a + ((c - 1) & 1) * kWide;
 #pragma unroll
             for (int kk = 0; kk < kTcChunk; ++kk) {
-              const uint32_t acc = (kk > 0 || !prev_first) ? 1u : 0u;
               const uint64_t db = smem_desc_sw128(pa + (kk >> 2) * kRowsHalf + (kk & 3) * 32, 0, 1024);
-              tc_mma_f16_ss(t_o, smem_desc_sw128(vsel + kk * 2048, kHalf, 1024), db, id_mk, acc);
-              tc_mma_f16_ss(t_l, smem_desc_sw128(onesa + (kk & 3) * 32, 0, 0), db, id_kk, acc);
+              tc_mma_f16_ss(t_o, smem_desc_sw128(vsel + kk * 2048, kHalf, 1024), db, id_o,
+                            (kk > 0 || !prev_first) ? 1u : 0u);
             }
             tc_commit(bar_odone);
           }
@@ -391,19 +586,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       __syncwarp();
     } else {
-      // ---------------------- widen / softmax / epilogue (warps 0..3) --------------
-      const int t = tid;   // token of the chunk, TMEM lane of S^T, head dimension of O^T
-      const uint32_t t_lane = static_cast<uint32_t>(warp * 32) << 16;
-      const int G = a.group, Hq = a.num_q_heads, R = a.rows;
+      // ---------------------- widen / softmax / epilogue (warps 0..7) --------------
+      const int q = warp & 3, hh = warp >> 2;
+      const int t = 32 * q + lane;   // token of the chunk, TMEM lane of S^T and K, head dimension of O^T
+      const int r0 = hh * RH;        // first of this thread's RH rows (TMEM columns)
+      const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * q) << 16);
+      const uint32_t t_cols = t_lane + r0;
       const long long ncta = gridDim.x, cta = blockIdx.x;
-      uint16_t* out16 = static_cast<uint16_t*>(a.out);
+      const float scale_log2 = a.scale_log2;
       bool alive = true;
       int o_waited = -1;
       int mp = 0;   // current running-max buffer
 
       auto wait_bar = [&](uint32_t bar, uint32_t parity) {
         if (!alive) return;
-        const bool ok = wait_or_abort(bar, parity, abort_flag);
+        const bool ok = tc_wait(bar, parity, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) {
           alive = false;
           *abort_flag = 1;
@@ -417,21 +614,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       };
 
+      // Swizzled P^T store addresses: row r = r0 + k lives in 16-byte chunk
+      // (t % 64) / 8 ^ (k % 8) of its 128-byte line (r0 is a multiple of 8).
+      uint8_t* pbase = pst + (t >> 6) * kRowsHalf + r0 * 128 + (t & 7) * 2;
+      const int tch = (t & 63) >> 3;
+
+      float l_run[RH];   // this thread's (token's) share of each row's sum of exponentials
+#pragma unroll
+      for (int k = 0; k < RH; ++k) l_run[k] = 0.f;
+
       TcWalk cur = w0;
-      TcPiece pc = tc_piece(a, cur, t);
+      TcPiece pc = tc_piece(a, cur, tid);
       int c = 0, piece = 0;
 
       // Prologue: chunk 0 and the first piece's queries.
       {
-        tc_copy_q<RC>(a, pc, cur.h, t, qst);
+        tc_copy_q<RP, kTcSoftmaxThreads>(a, pc, cur.h, tid, qst);
         wait_bar(bars, 0);
         const bool valid = (t >> 4) < cur.nblk() && cur.first_token() + t < pc.ctx_eff;
         if (alive) {
-          widen_e5m2_row(ring, k16, t, valid);
-          widen_e5m2_row(ring + kTcChunk * TILE, v16, t, valid);
+          widen_e5m2_half_row_tmem(ring, t, hh, valid, t_lane + kTcKCol);
+          widen_e5m2_half_row(ring + kTcChunk * TILE, v16, t, hh, valid);
         }
         cp_async_wait_all();
         fence_proxy_async_smem();
+        tc_fence_before_sync();
         __syncwarp();
         if (alive) {
           if (lane == 0) mbar_arrive(bars + 8 * nbuf);
@@ -447,160 +654,101 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         TcPiece pn = pc;
         if (new_piece) {
           // The other query buffer was last read by S^T MMAs of an earlier piece, all complete.
-          pn = tc_piece(a, nxt, t);
-          tc_copy_q<RC>(a, pn, nxt.h, t, qst + ((piece + 1) & 1) * 2 * kRowsHalf);
+          pn = tc_piece(a, nxt, tid);
+          tc_copy_q<RP, kTcSoftmaxThreads>(a, pn, nxt.h, tid, qst + ((piece + 1) & 1) * 2 * kRowsHalf);
         }
         const int buf_next = (c + 1) % nbuf;
         const uint8_t* ring_next = ring + buf_next * CHUNK_BYTES;
         const bool valid_next =
             has_next && (t >> 4) < nxt.nblk() && nxt.first_token() + t < pn.ctx_eff;
 
-        // (1) scores of chunk c
-        uint32_t sv[RC][32];
+        // (1) scores of chunk c, rows r0 .. r0+RH-1, from S buffer c % 2
+        uint32_t sv[RH];
         wait_bar(bar_sfull, c & 1);
         if (alive) {
           tc_fence_after_sync();
-#pragma unroll
-          for (int rc = 0; rc < RC; ++rc) tmem_ld32(tmem + t_lane + rc * 32, sv[rc]);
+          tmem_ld<RH>(t_cols + (c & 1) * kTcSCols, sv);
         } else {
 #pragma unroll
-          for (int rc = 0; rc < RC; ++rc)
-#pragma unroll
-            for (int k = 0; k < 32; ++k) sv[rc][k] = 0u;
+          for (int k = 0; k < RH; ++k) sv[k] = 0u;
         }
 
-        // (2) K of chunk c+1 (and the queries of a new piece): S(c+1) overlaps (3)
+        // (2) K of chunk c+1 into K buffer (c+1) % 2, last read by S(c-1) (complete):
+        //     S(c+1) overlaps the softmax below
         if (has_next) {
           wait_bar(bars + 8 * buf_next, ((c + 1) / nbuf) & 1);
-          if (alive) widen_e5m2_row(ring_next, k16, t, valid_next);
+          if (alive) widen_e5m2_half_row_tmem(ring_next, t, hh, valid_next, t_lane + kTcKCol + ((c + 1) & 1) * 64);
           cp_async_wait_all();
           fence_proxy_async_smem();
           tc_fence_before_sync();
           if (alive) mbar_arrive(bar_kready);
         }
 
-        // (3) softmax of chunk c (base 2)
+        // (3) scores in base 2, masked; does any exceed its row's running max by the slack?
         const int p = cur.first_token() + t;
         const bool valid = (t >> 4) < cur.nblk() && p < pc.ctx_eff;
-        // Rows that see token p: all before the draft tokens; draft token i = p - cb
-        // is seen by query token j when its tree mask has bit i (or, causally, j >= i).
-        // Padding rows (>= Rs) are kept finite and never written out.
-        unsigned long long vis = 0ull;
-        if (valid) {
-          if (p < pc.cb) {
-            vis = ~0ull;
-          } else {
-            const int i = p - pc.cb;
-            const unsigned long long pad = pc.Rs >= 64 ? 0ull : (~0ull << pc.Rs);
-            if (a.tree_masks) {
-              const unsigned long long gm = G >= 64 ? ~0ull : ((1ull << G) - 1ull);
-              unsigned long long m = 0ull;
-              for (int j = 0; j < pc.n_s; ++j)
-                if ((__ldg(a.tree_masks + pc.qb + j) >> i) & 1ull) m |= gm << (j * G);
-              vis = m | pad;
-            } else {
-              const int lo = i * G;
-              vis = (lo >= 64 ? 0ull : (~0ull << lo)) | pad;
-            }
-          }
+        float x[RH];
+        if (valid && p < pc.cb) {
+#pragma unroll
+          for (int k = 0; k < RH; ++k) x[k] = __uint_as_float(sv[k]) * scale_log2;
+        } else {
+          const unsigned long long vis = tc_row_visibility(a, pc, p, valid, r0);
+#pragma unroll
+          for (int k = 0; k < RH; ++k) x[k] = ((vis >> k) & 1ull) ? __uint_as_float(sv[k]) * scale_log2 : kNegInf;
         }
-        float x[RC][32];
-        bool need = false;
+        float excess = kNegInf;
         {
-          const float* mrow = row_m + mp * RP;
+          const float* mrow = row_m + mp * RP + r0;
 #pragma unroll
-          for (int rc = 0; rc < RC; ++rc)
-#pragma unroll
-            for (int k4 = 0; k4 < 8; ++k4) {
-              const float4 m4 = *reinterpret_cast<const float4*>(mrow + rc * 32 + 4 * k4);
-              const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int k = 4 * k4 + e, r = rc * 32 + k;
-                const float xv = ((vis >> r) & 1ull) ? __uint_as_float(sv[rc][k]) * a.scale_log2 : kNegInf;
-                x[rc][k] = xv;
-                need |= xv > mm[e] + kRescaleSlack;
-              }
-            }
+          for (int k4 = 0; k4 < RH / 4; ++k4) {
+            const float4 m4 = *reinterpret_cast<const float4*>(mrow + 4 * k4);
+            excess = fmaxf(excess, fmaxf(fmaxf(x[4 * k4] - m4.x, x[4 * k4 + 1] - m4.y),
+                                         fmaxf(x[4 * k4 + 2] - m4.z, x[4 * k4 + 3] - m4.w)));
+          }
         }
-        if (bar_red_or(1, kTcSoftmaxThreads, need)) {
-          // Exact row maxima of this chunk over the 128 tokens; the running max of
-          // every row that grows moves there, and what was accumulated is rescaled.
-#pragma unroll
-          for (int rc = 0; rc < RC; ++rc)
-#pragma unroll
-            for (int k = 0; k < 32; ++k) {
-              const int km = __reduce_max_sync(0xffffffffu, float_order_key(x[rc][k]));
-              if (lane == k) red_m[warp * RP + rc * 32 + k] = float_from_order_key(km);
-            }
-          named_bar_sync(2, kTcSoftmaxThreads);
+        if (bar_red_or(1, kTcSoftmaxThreads, excess > kRescaleSlack)) {
+          // Rare: the running maxima move to this chunk's maxima.
           const float* mold = row_m + mp * RP;
-          bool grows = false;
+          const bool grows = tc_chunk_maxima<RH>(x, red_m, mold, RP, q, r0, lane);
+          if (grows) {
 #pragma unroll
-          for (int r = 0; r < RP; ++r) {
-            const float cm = fmaxf(fmaxf(red_m[r], red_m[RP + r]), fmaxf(red_m[2 * RP + r], red_m[3 * RP + r]));
-            grows |= cm > mold[r];
-          }
-          if (grows && !cur.first()) {
-            // O^T and the row sums hold earlier chunks of this piece.
-            wait_o(c - 1);
-            if (alive) {
-              tc_fence_after_sync();
-#pragma unroll
-              for (int rc = 0; rc < RC; ++rc) {
-                float al[32];
-#pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                  const int r = rc * 32 + k;
-                  const float cm =
-                      fmaxf(fmaxf(red_m[r], red_m[RP + r]), fmaxf(red_m[2 * RP + r], red_m[3 * RP + r]));
-                  al[k] = cm > mold[r] ? fast_exp2(mold[r] - cm) : 1.f;
-                }
-                uint32_t ov[32];
-                tmem_ld32(tmem + t_lane + kTcOCol + rc * 32, ov);
-#pragma unroll
-                for (int k = 0; k < 32; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * al[k]);
-                tmem_st32(tmem + t_lane + kTcOCol + rc * 32, ov);
-                tmem_ld32(tmem + t_lane + kTcLCol + rc * 32, ov);
-#pragma unroll
-                for (int k = 0; k < 32; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * al[k]);
-                tmem_st32(tmem + t_lane + kTcLCol + rc * 32, ov);
-              }
+            for (int k = 0; k < RH; ++k) {
+              const float cm = tc_chunk_max(red_m, RP, r0 + k);
+              if (cm > mold[r0 + k]) l_run[k] *= fast_exp2(mold[r0 + k] - cm);
             }
           }
-          if (t < RP) {
-            const float cm = fmaxf(fmaxf(red_m[t], red_m[RP + t]), fmaxf(red_m[2 * RP + t], red_m[3 * RP + t]));
-            row_m[(mp ^ 1) * RP + t] = fmaxf(mold[t], cm);
-          }
-          named_bar_sync(2, kTcSoftmaxThreads);
+          const bool rescale = grows && !cur.first();
+          if (rescale) wait_o(c - 1);   // O^T holds earlier chunks
+          tc_move_maxima<RH>(t_cols, rescale && alive, red_m, mold, row_m + (mp ^ 1) * RP, RP, r0, tid);
           mp ^= 1;
         }
 
         // (4) P^T of chunk c: K-major [token half][row][128 B]; the buffer was read by O(c-1).
         if (c > 0) wait_o(c - 1);
         if (alive) {
-          const float* mrow = row_m + mp * RP;
-          uint8_t* prow = pst + (t >> 6) * kRowsHalf + (t & 7) * 2;
-          const int tch = (t & 63) >> 3;
+          const float* mrow = row_m + mp * RP + r0;
 #pragma unroll
-          for (int rc = 0; rc < RC; ++rc)
+          for (int k4 = 0; k4 < RH / 4; ++k4) {
+            const float4 m4 = *reinterpret_cast<const float4*>(mrow + 4 * k4);
+            const __half2 p01 = __floats2half2_rn(fast_exp2(x[4 * k4] - m4.x), fast_exp2(x[4 * k4 + 1] - m4.y));
+            const __half2 p23 = __floats2half2_rn(fast_exp2(x[4 * k4 + 2] - m4.z), fast_exp2(x[4 * k4 + 3] - m4.w));
+            // The sums add exactly the fp16 values the P V product uses.
+            l_run[4 * k4] += __low2float(p01);
+            l_run[4 * k4 + 1] += __high2float(p01);
+            l_run[4 * k4 + 2] += __low2float(p23);
+            l_run[4 * k4 + 3] += __high2float(p23);
+            const __half pk[4] = {__low2half(p01), __high2half(p01), __low2half(p23), __high2half(p23)};
 #pragma unroll
-            for (int k4 = 0; k4 < 8; ++k4) {
-              const float4 m4 = *reinterpret_cast<const float4*>(mrow + rc * 32 + 4 * k4);
-              const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int k = 4 * k4 + e, r = rc * 32 + k;
-                const float mu = mm[e] == kNegInf ? 0.f : mm[e];
-                const float pv = fast_exp2(x[rc][k] - mu);
-                *reinterpret_cast<__half*>(prow + r * 128 + ((tch ^ (r & 7)) << 4)) = __float2half_rn(pv);
-              }
+            for (int e = 0; e < 4; ++e) {
+              const int k = 4 * k4 + e;
+              *reinterpret_cast<__half*>(pbase + k * 128 + ((tch ^ (k & 7)) << 4)) = pk[e];
             }
+          }
         }
 
         // (5) V of chunk c+1 (its buffer was read by O(c-1)); release the ring buffer.
         if (has_next) {
-          if (alive) widen_e5m2_row(ring_next + kTcChunk * TILE, v16 + ((c + 1) & 1) * kWide, t, valid_next);
+          if (alive) widen_e5m2_half_row(ring_next + kTcChunk * TILE, v16 + ((c + 1) & 1) * kWide, t, hh, valid_next);
           __syncwarp();
           if (alive && lane == 0) mbar_arrive(bars + 8 * (nbuf + buf_next));
         }
@@ -610,60 +758,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
         // (6) end of a piece: normalise and write, or write the split partial.
         if (cur.last()) {
+          {
+            float v[RH];
+#pragma unroll
+            for (int k = 0; k < RH; ++k) {
+              v[k] = l_run[k];
+              l_run[k] = 0.f;
+            }
+            const float ls = warp_rows_sum<RH>(v, lane);
+            if (lane < RH) red_l[q * RP + r0 + lane] = ls;
+          }
+          named_bar_sync(2, kTcSoftmaxThreads);
           wait_o(c);
-          if (alive) tc_fence_after_sync();
-          float* slot = a.partials + static_cast<size_t>(pc.u + cta) * a.slot_floats;
-          const int ooff = partial_o_offset(R);
-#pragma unroll
-          for (int rc = 0; rc < RC; ++rc) {
-            uint32_t ov[32], lv[32];
-            if (alive) {
-              tmem_ld32(tmem + t_lane + kTcOCol + rc * 32, ov);
-              tmem_ld32(tmem + t_lane + kTcLCol + rc * 32, lv);
-            } else {
-#pragma unroll
-              for (int k = 0; k < 32; ++k) ov[k] = lv[k] = 0u;
-            }
-            int j = (rc * 32) / G, gi = rc * 32 - j * G;
-#pragma unroll
-            for (int k = 0; k < 32; ++k) {
-              const int r = rc * 32 + k;
-              if (r < pc.Rs) {
-                const float o = __uint_as_float(ov[k]);
-                if (!pc.split) {
-                  const float L = __uint_as_float(lv[k]);
-                  const float inv = L > 0.f ? 1.f / L : 0.f;
-                  const size_t dst = (static_cast<size_t>(pc.qb + j) * Hq + cur.h * G + gi) * D + t;
-                  out16[dst] = __half_as_ushort(__float2half_rn(o * inv));
-                } else {
-                  slot[ooff + r * D + t] = o;
-                }
-              }
-              if (++gi == G) {
-                gi = 0;
-                ++j;
-              }
-            }
-            if (pc.split && warp == 0) {
-              // Row rc*32 + lane: its running max and sum.
-              float v[32];
-#pragma unroll
-              for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(lv[k]);
-              const float lsum = select_lane32(v, lane);
-              const int r = rc * 32 + lane;
-              if (r < R) {
-                slot[r] = row_m[mp * RP + r];
-                slot[R + r] = lsum;
-              }
-            }
-          }
-          if (pc.split) {
-            finish_split_piece<kKvE5m2, D>(a, pc.u, cur.gpos - cur.lb, cur.nb, total, ncta, pc.Rs, pc.qb,
-                                           cur.h, t, kTcSoftmaxThreads, 3, fin);
-          }
+          tc_piece_output<RH>(a, t_cols, alive, pc, cur.h, r0, t, q, lane, row_m + mp * RP, red_l, cta);
+          if (pc.split) tc_finish_split(a, pc, cur.gpos - cur.lb, cur.nb, total, ncta, cur.h, tid, fin);
           // The next piece starts from an empty running max.
           named_bar_sync(2, kTcSoftmaxThreads);
-          if (t < RP) row_m[mp * RP + t] = kNegInf;
+          if (tid < RP) row_m[mp * RP + tid] = kNoMax;
           named_bar_sync(2, kTcSoftmaxThreads);
         }
 

@@ -91,32 +91,32 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int kv, int d, int ntw,
 }
 
 // Tensor-core (tcgen05) decode kernel for wide units: 128-token chunks (8 KV
-// blocks, the MMA's M), 4 softmax warps, 1 MMA-issue warp, 1 TMA warp.
+// blocks, the MMA's M), 8 softmax warps, 1 MMA-issue warp, 1 TMA warp.
 constexpr int kTcChunk = 8;          // KV blocks per chunk
-constexpr int kTcThreads = 192;
-constexpr int kTcTmemCols = 256;     // S^T at columns [0, 64), O^T at [64, 128), row sums at [128, 192)
+constexpr int kTcThreads = 320;
+// Tensor memory: S^T buffers at columns [0, 64) and [64, 128), O^T at
+// [128, 192), fp16 K buffers (two per column) at [256, 320) and [320, 384).
+constexpr int kTcTmemCols = 512;
 
 // Shared memory of the tcgen05 kernel for rows_pad (32 or 64) query rows and
 // nbuf ring buffers of one E5M2 chunk each (8 K tiles + 8 V tiles, 32 KB).
 struct TcSmem {
-  size_t k16, v16, p, q, ones, ring, bars, misc, total;
+  size_t v16, p, q, ring, bars, misc, total;
 };
 __host__ __device__ inline TcSmem tc_smem_layout(int rows_pad, int nbuf) {
   TcSmem s{};
-  const size_t wide = 128 * 128 * 2;          // one chunk of K or V widened to fp16
+  const size_t wide = 128 * 128 * 2;          // one chunk of V widened to fp16
   const size_t rows_bytes = (size_t)rows_pad * 256;
-  s.k16 = 0;
-  s.v16 = s.k16 + wide;                        // two buffers
+  s.v16 = 0;                                   // two buffers
   s.p = s.v16 + 2 * wide;
   s.q = s.p + rows_bytes;                      // two buffers
-  s.ones = s.q + 2 * rows_bytes;               // one 1024-byte atom of fp16 1.0
-  s.ring = s.ones + 1024;
+  s.ring = s.q + 2 * rows_bytes;
   s.bars = s.ring + (size_t)nbuf * 2 * kTcChunk * kBlockSize * 128;
   s.misc = s.bars + (size_t)(2 * nbuf + 5) * 8;
   s.misc = (s.misc + 15) & ~(size_t)15;
-  // TMEM address, per-warp row maxima [4][rows_pad], running max [2][rows_pad],
-  // plan scan scratch, plan, abort flag and finish flags.
-  s.total = s.misc + 16 + (size_t)6 * rows_pad * 4 + 8 * 8 + 5 * 8 + 16 * 4;
+  // TMEM address, per-quarter row maxima and row sums [4][rows_pad] each,
+  // running max [2][rows_pad], plan scan scratch, plan, abort and finish flags.
+  s.total = s.misc + 16 + (size_t)10 * rows_pad * 4 + 16 * 8 + 5 * 8 + 16 * 4;
   return s;
 }
 const void* decode_tc_kernel_ptr(int kv, int rc);
