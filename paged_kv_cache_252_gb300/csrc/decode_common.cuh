@@ -149,14 +149,17 @@ __device__ inline void finish_split_piece(const DecodeArgs& a, int u, long long 
   if (!fin[0]) return;
   const int c_first = fin[1], c_last = fin[2];
   const int ooff = partial_o_offset(R);
+#pragma unroll 1
   for (int idx = tid; idx < Rs * (D / 4); idx += nthr) {
     const int r = idx / (D / 4), d4 = idx - (idx / (D / 4)) * (D / 4);
     float M = kNegInf;
+#pragma unroll 1
     for (int c = c_first; c <= c_last; ++c)
       M = fmaxf(M, __ldcg(a.partials + static_cast<size_t>(u + c) * a.slot_floats + r));
     const float Mu = (M == kNegInf) ? 0.f : M;
     float lsum = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
     for (int c = c_first; c <= c_last; ++c) {
       const float* P = a.partials + static_cast<size_t>(u + c) * a.slot_floats;
       const float f = fast_exp2(__ldcg(P + r) - Mu);

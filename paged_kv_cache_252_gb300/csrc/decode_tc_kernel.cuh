@@ -315,73 +315,68 @@ __device__ __forceinline__ bool tc_chunk_maxima(const float* x, float* red_m, co
 
 // Rare path, part 2: rescale this warp's columns of O^T by 2^(old max - new
 // max) (rescale: they hold earlier chunks of the piece), and write the new
-// running maxima into the other buffer.
+// running maxima into the other buffer. Runs once per piece or less, so its
+// loops stay rolled: cold code is fetched from L2 each time it runs.
 template <int RH>
 __device__ __forceinline__ void tc_move_maxima(uint32_t t_cols, bool rescale, const float* red_m,
                                                const float* mold, float* mnew, int RP, int r0, int tid) {
   if (rescale) {
     tc_fence_after_sync();
-    uint32_t v[RH];
-    tmem_ld<RH>(t_cols + kTcOCol, v);
-#pragma unroll
+#pragma unroll 1
     for (int k = 0; k < RH; ++k) {
       const float cm = tc_chunk_max(red_m, RP, r0 + k);
-      const float al = cm > mold[r0 + k] ? fast_exp2(mold[r0 + k] - cm) : 1.f;
-      v[k] = __float_as_uint(__uint_as_float(v[k]) * al);
+      if (cm > mold[r0 + k]) {
+        const uint32_t col = t_cols + kTcOCol + k;
+        tmem_st1(col, __float_as_uint(__uint_as_float(tmem_ld1(col)) * fast_exp2(mold[r0 + k] - cm)));
+      }
     }
-    tmem_st<RH>(t_cols + kTcOCol, v);
   }
   if (tid < RP) mnew[tid] = fmaxf(mold[tid], tc_chunk_max(red_m, RP, tid));
   named_bar_sync(2, kTcSoftmaxThreads);
 }
 
-// End of a piece: O^T of this thread's rows (head dimension t) from TMEM,
-// the row sums from red_l ([quarter][row] partial sums); the normalised
-// output, or the split partial (o, and m / l of each row).
-template <int RH>
-__device__ __forceinline__ void tc_piece_output(const DecodeArgs& a, uint32_t t_cols, bool alive,
-                                                const TcPiece& pc, int h, int r0, int t, int q, int lane,
-                                                const float* mcur, const float* red_l, long long cta) {
+// End of a piece, once the per-quarter row sums are in red_l: threads r < RP
+// turn row r's sum into 1 / L (row_inv) or, for a split piece, write its m and
+// l to the partial slot.
+__device__ __forceinline__ void tc_piece_rows(const DecodeArgs& a, const TcPiece& pc, int RP, int tid,
+                                              const float* mcur, const float* red_l, float* row_inv,
+                                              long long cta) {
+  if (tid < RP) {
+    const float L = (red_l[tid] + red_l[RP + tid]) + (red_l[2 * RP + tid] + red_l[3 * RP + tid]);
+    row_inv[tid] = L > 0.f ? 1.f / L : 0.f;
+    if (pc.split && tid < a.rows) {
+      float* slot = a.partials + static_cast<size_t>(pc.u + cta) * a.slot_floats;
+      slot[tid] = mcur[tid];
+      slot[a.rows + tid] = L;
+    }
+  }
+}
+
+// O^T of this thread's rows (head dimension t), one TMEM column per row (a
+// rolled loop: this runs once per piece): the normalised output, or the
+// split partial's o.
+__device__ __forceinline__ void tc_piece_output(const DecodeArgs& a, uint32_t t_cols, const TcPiece& pc,
+                                                int h, int r0, int RH, int t, const float* row_inv,
+                                                long long cta) {
   constexpr int D = 128;
-  const int G = a.group, Hq = a.num_q_heads, R = a.rows;
-  const int RP = 2 * RH;
-  uint32_t ov[RH];
-  if (alive) {
-    tc_fence_after_sync();
-    tmem_ld<RH>(t_cols + kTcOCol, ov);
+  const int G = a.group, Hq = a.num_q_heads;
+  tc_fence_after_sync();
+  const int r_end = r0 + RH < pc.Rs ? r0 + RH : pc.Rs;
+  if (!pc.split) {
+    int j = r0 / G, gi = r0 - j * G;
+    uint16_t* dst = static_cast<uint16_t*>(a.out) + (static_cast<size_t>(pc.qb + j) * Hq + h * G + gi) * D + t;
+#pragma unroll 1
+    for (int r = r0; r < r_end; ++r) {
+      const float o = __uint_as_float(tmem_ld1(t_cols + kTcOCol + (r - r0)));
+      *dst = __half_as_ushort(__float2half_rn(o * row_inv[r]));
+      // next row: next head of the group, or the first head for the next query token
+      dst += (++gi == G) ? static_cast<ptrdiff_t>(Hq - G + 1) * D : D;
+      if (gi == G) gi = 0;
+    }
   } else {
-#pragma unroll
-    for (int k = 0; k < RH; ++k) ov[k] = 0u;
-  }
-  float* slot = a.partials + static_cast<size_t>(pc.u + cta) * a.slot_floats;
-  const int ooff = partial_o_offset(R);
-  uint16_t* out16 = static_cast<uint16_t*>(a.out);
-  int j = r0 / G, gi = r0 - j * G;
-#pragma unroll
-  for (int k = 0; k < RH; ++k) {
-    const int r = r0 + k;
-    if (r < pc.Rs) {
-      const float o = __uint_as_float(ov[k]);
-      if (!pc.split) {
-        const float L = (red_l[r] + red_l[RP + r]) + (red_l[2 * RP + r] + red_l[3 * RP + r]);
-        const float inv = L > 0.f ? 1.f / L : 0.f;
-        const size_t dst = (static_cast<size_t>(pc.qb + j) * Hq + h * G + gi) * D + t;
-        out16[dst] = __half_as_ushort(__float2half_rn(o * inv));
-      } else {
-        slot[ooff + r * D + t] = o;
-      }
-    }
-    if (++gi == G) {
-      gi = 0;
-      ++j;
-    }
-  }
-  if (pc.split && q == 0 && lane < RH) {
-    const int r = r0 + lane;
-    if (r < R) {
-      slot[r] = mcur[r];
-      slot[R + r] = (red_l[r] + red_l[RP + r]) + (red_l[2 * RP + r] + red_l[3 * RP + r]);
-    }
+    float* slot = a.partials + static_cast<size_t>(pc.u + cta) * a.slot_floats + partial_o_offset(a.rows) + t;
+#pragma unroll 1
+    for (int r = r0; r < r_end; ++r) slot[r * D] = __uint_as_float(tmem_ld1(t_cols + kTcOCol + (r - r0)));
   }
 }
 
@@ -428,7 +423,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   float* red_m = reinterpret_cast<float*>(smem + lay.misc + 16);   // [4][RP] per-quarter row maxima
   float* red_l = red_m + 4 * RP;                                    // [4][RP] per-quarter row sums
   float* row_m = red_l + 4 * RP;                                    // [2][RP] running max, two buffers
-  long long* red = reinterpret_cast<long long*>(row_m + 2 * RP);    // [16] plan scan scratch, one per warp
+  float* row_inv = row_m + 2 * RP;                                  // [RP] 1 / row sum at a piece's end
+  long long* red = reinterpret_cast<long long*>(row_inv + RP);      // [16] plan scan scratch, one per warp
   long long* plan = red + 16;                                       // total, b0, b1, s0, cum0
   volatile int* abort_flag = reinterpret_cast<volatile int*>(plan + 5);
   volatile int* fin = abort_flag + 1;                               // is_last, first CTA, last CTA
@@ -769,8 +765,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (lane < RH) red_l[q * RP + r0 + lane] = ls;
           }
           named_bar_sync(2, kTcSoftmaxThreads);
+          tc_piece_rows(a, pc, RP, tid, row_m + mp * RP, red_l, row_inv, cta);
+          named_bar_sync(2, kTcSoftmaxThreads);
           wait_o(c);
-          tc_piece_output<RH>(a, t_cols, alive, pc, cur.h, r0, t, q, lane, row_m + mp * RP, red_l, cta);
+          if (alive) tc_piece_output(a, t_cols, pc, cur.h, r0, RH, t, row_inv, cta);
           if (pc.split) tc_finish_split(a, pc, cur.gpos - cur.lb, cur.nb, total, ncta, cur.h, tid, fin);
           // The next piece starts from an empty running max.
           named_bar_sync(2, kTcSoftmaxThreads);
