@@ -296,43 +296,48 @@ __device__ __forceinline__ float tc_chunk_max(const float* red_m, int RP, int r)
 }
 
 // Rare path, part 1: the chunk's exact maxima of this thread's rows over the
-// 128 tokens into red_m[quarter][row]. Returns whether any of them exceeds the
-// running max (uniform within the warp: its lanes share the rows).
-template <int RH>
-__device__ __forceinline__ bool tc_chunk_maxima(const float* x, float* red_m, const float* mold, int RP, int q,
-                                             int r0, int lane) {
-#pragma unroll
+// 128 tokens into red_m[quarter][row], re-reading the scores from the S^T
+// columns (still intact: S(c+2) is not issued before the next chunk's K).
+// Runs about once per piece, so the loop stays rolled.
+__device__ __forceinline__ void tc_chunk_maxima(uint32_t s_cols, unsigned long long vis, float scale_log2,
+                                                float* red_m, int RP, int q, int r0, int RH, int lane) {
+#pragma unroll 1
   for (int k = 0; k < RH; ++k) {
-    const int km = __reduce_max_sync(0xffffffffu, float_order_key(x[k]));
+    // Every lane loads (the load is warp-collective); the mask is applied after.
+    const float sk = __uint_as_float(tmem_ld1(s_cols + k));
+    const float xv = ((vis >> k) & 1ull) ? sk * scale_log2 : -INFINITY;
+    const int km = __reduce_max_sync(0xffffffffu, float_order_key(xv));
     if (lane == k) red_m[q * RP + r0 + k] = float_from_order_key(km);
   }
   named_bar_sync(2, kTcSoftmaxThreads);
-  bool grows = false;
-#pragma unroll
-  for (int k = 0; k < RH; ++k) grows |= tc_chunk_max(red_m, RP, r0 + k) > mold[r0 + k];
-  return grows;
 }
 
-// Rare path, part 2: rescale this warp's columns of O^T by 2^(old max - new
-// max) (rescale: they hold earlier chunks of the piece), and write the new
-// running maxima into the other buffer. Runs once per piece or less, so its
-// loops stay rolled: cold code is fetched from L2 each time it runs.
-template <int RH>
-__device__ __forceinline__ void tc_move_maxima(uint32_t t_cols, bool rescale, const float* red_m,
-                                               const float* mold, float* mnew, int RP, int r0, int tid) {
-  if (rescale) {
-    tc_fence_after_sync();
+// Rare path, part 2: threads r < RP move row r's running max to the larger of
+// it and the chunk maximum (into the other max buffer) and record the factor
+// 2^(old - new) that rescales what the row accumulated so far.
+__device__ __forceinline__ void tc_new_maxima(const float* red_m, const float* mold, float* mnew, float* alpha,
+                                              int RP, int tid) {
+  if (tid < RP) {
+    const float mo = mold[tid];
+    const float mn = fmaxf(mo, tc_chunk_max(red_m, RP, tid));
+    mnew[tid] = mn;
+    alpha[tid] = mn > mo ? fast_exp2(mo - mn) : 1.f;
+  }
+  named_bar_sync(2, kTcSoftmaxThreads);
+}
+
+// Rare path, part 3: rescale this warp's columns of O^T (they hold earlier
+// chunks of the piece), one TMEM column per row.
+__device__ __forceinline__ void tc_rescale_o(uint32_t t_cols, const float* alpha, int r0, int RH) {
+  tc_fence_after_sync();
 #pragma unroll 1
-    for (int k = 0; k < RH; ++k) {
-      const float cm = tc_chunk_max(red_m, RP, r0 + k);
-      if (cm > mold[r0 + k]) {
-        const uint32_t col = t_cols + kTcOCol + k;
-        tmem_st1(col, __float_as_uint(__uint_as_float(tmem_ld1(col)) * fast_exp2(mold[r0 + k] - cm)));
-      }
+  for (int k = 0; k < RH; ++k) {
+    const float al = alpha[r0 + k];
+    if (al != 1.f) {
+      const uint32_t col = t_cols + kTcOCol + k;
+      tmem_st1(col, __float_as_uint(__uint_as_float(tmem_ld1(col)) * al));
     }
   }
-  if (tid < RP) mnew[tid] = fmaxf(mold[tid], tc_chunk_max(red_m, RP, tid));
-  named_bar_sync(2, kTcSoftmaxThreads);
 }
 
 // End of a piece, once the per-quarter row sums are in red_l: threads r < RP
@@ -424,7 +429,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   float* red_l = red_m + 4 * RP;                                    // [4][RP] per-quarter row sums
   float* row_m = red_l + 4 * RP;                                    // [2][RP] running max, two buffers
   float* row_inv = row_m + 2 * RP;                                  // [RP] 1 / row sum at a piece's end
-  long long* red = reinterpret_cast<long long*>(row_inv + RP);      // [16] plan scan scratch, one per warp
+  float* row_alpha = row_inv + RP;                                  // [RP] rescale factor when the max moves
+  long long* red = reinterpret_cast<long long*>(row_alpha + RP);    // [16] plan scan scratch, one per warp
   long long* plan = red + 16;                                       // total, b0, b1, s0, cum0
   volatile int* abort_flag = reinterpret_cast<volatile int*>(plan + 5);
   volatile int* fin = abort_flag + 1;                               // is_last, first CTA, last CTA
@@ -683,12 +689,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // (3) scores in base 2, masked; does any exceed its row's running max by the slack?
         const int p = cur.first_token() + t;
         const bool valid = (t >> 4) < cur.nblk() && p < pc.ctx_eff;
+        const bool allvis = valid && p < pc.cb;
+        const unsigned long long vis = allvis ? ~0ull : tc_row_visibility(a, pc, p, valid, r0);
         float x[RH];
-        if (valid && p < pc.cb) {
+        if (allvis) {
 #pragma unroll
           for (int k = 0; k < RH; ++k) x[k] = __uint_as_float(sv[k]) * scale_log2;
         } else {
-          const unsigned long long vis = tc_row_visibility(a, pc, p, valid, r0);
 #pragma unroll
           for (int k = 0; k < RH; ++k) x[k] = ((vis >> k) & 1ull) ? __uint_as_float(sv[k]) * scale_log2 : kNegInf;
         }
@@ -703,20 +710,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         if (bar_red_or(1, kTcSoftmaxThreads, excess > kRescaleSlack)) {
-          // Rare: the running maxima move to this chunk's maxima.
-          const float* mold = row_m + mp * RP;
-          const bool grows = tc_chunk_maxima<RH>(x, red_m, mold, RP, q, r0, lane);
-          if (grows) {
-#pragma unroll
-            for (int k = 0; k < RH; ++k) {
-              const float cm = tc_chunk_max(red_m, RP, r0 + k);
-              if (cm > mold[r0 + k]) l_run[k] *= fast_exp2(mold[r0 + k] - cm);
-            }
-          }
-          const bool rescale = grows && !cur.first();
-          if (rescale) wait_o(c - 1);   // O^T holds earlier chunks
-          tc_move_maxima<RH>(t_cols, rescale && alive, red_m, mold, row_m + (mp ^ 1) * RP, RP, r0, tid);
+          // Rare: the running maxima move to this chunk's maxima, and what the
+          // rows accumulated so far is rescaled.
+          if (alive) tc_chunk_maxima(t_cols + (c & 1) * kTcSCols, vis, scale_log2, red_m, RP, q, r0, RH, lane);
+          else named_bar_sync(2, kTcSoftmaxThreads);
+          tc_new_maxima(red_m, row_m + mp * RP, row_m + (mp ^ 1) * RP, row_alpha, RP, tid);
           mp ^= 1;
+          if (!cur.first()) {
+            wait_o(c - 1);   // O^T holds earlier chunks
+            if (alive) tc_rescale_o(t_cols, row_alpha, r0, RH);
+          }
+#pragma unroll
+          for (int k = 0; k < RH; ++k) l_run[k] *= row_alpha[r0 + k];
         }
 
         // (4) P^T of chunk c: K-major [token half][row][128 B]; the buffer was read by O(c-1).

@@ -115,9 +115,9 @@ __host__ __device__ inline TcSmem tc_smem_layout(int rows_pad, int nbuf) {
   s.misc = s.bars + (size_t)(2 * nbuf + 5) * 8;
   s.misc = (s.misc + 15) & ~(size_t)15;
   // TMEM address, per-quarter row maxima and row sums [4][rows_pad] each,
-  // running max [2][rows_pad], 1 / row sum [rows_pad], plan scan scratch, plan,
-  // abort and finish flags.
-  s.total = s.misc + 16 + (size_t)11 * rows_pad * 4 + 16 * 8 + 5 * 8 + 16 * 4;
+  // running max [2][rows_pad], 1 / row sum and rescale factor [rows_pad] each,
+  // plan scan scratch, plan, abort and finish flags.
+  s.total = s.misc + 16 + (size_t)12 * rows_pad * 4 + 16 * 8 + 5 * 8 + 16 * 4;
   return s;
 }
 const void* decode_tc_kernel_ptr(int kv, int rc);
