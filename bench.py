@@ -3,7 +3,8 @@
 
 A step is one pass of the whole hot path over one batch: the cache write of
 the step's new tokens (fp16 -> E5M2 cast for an E5M2 cache) followed by paged
-decode attention over every sequence's blocks (decode kernel + split-KV reduce).
+decode attention over every sequence's blocks (one decode launch; split units are
+combined inside it).
 
     python bench.py [--config 8b] [--steps K] [--warmup W] [--gpus N]
     python bench.py --impl reference ...   # the CPU oracle on the same workload
@@ -253,7 +254,7 @@ def run_ours(args, rank, world, local):
     elapsed = e0.elapsed_time(e1) / 1e3
     job_elapsed, job_bytes = aggregate(elapsed, step_bytes * args.steps, world, dev)
 
-    # Decode op alone (decode kernel + split-KV reduce), per-launch CUDA events on its stream.
+    # Decode op alone (one decode launch, split-KV combine fused), per-launch CUDA events on its stream.
     n_r = max(args.steps, 50)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_r)]
     for i in range(n_r):
@@ -337,7 +338,7 @@ def run_ours(args, rank, world, local):
         "seq_steps_per_s": round(w.num_seqs * world * args.steps / job_elapsed, 1),
         "tokens_per_s": round(w.num_new_tokens * world * args.steps / job_elapsed, 1),
         "pct_of_hbm_peak": round(100 * value / peak, 2),
-        "roofline": {"bound": "hbm", "kernel": "paged_attention_decode (decode + split-KV reduce)",
+        "roofline": {"bound": "hbm", "kernel": "paged_attention_decode (one launch, split-KV combine fused)",
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,
                      "traffic": profiled_traffic(args.config),
