@@ -60,7 +60,8 @@ typedef enum {
   PKV_ERR_UNSUPPORTED = -2,        /* shape or dtype combination this build does not handle */
   PKV_ERR_WORKSPACE_TOO_SMALL = -3,
   PKV_ERR_CUDA = -4,               /* a CUDA runtime call failed (launch, attribute, ...) */
-  PKV_ERR_NO_DEVICE = -5
+  PKV_ERR_NO_DEVICE = -5,
+  PKV_ERR_OUT_OF_BLOCKS = -6      /* block allocator: the pool cannot supply the blocks asked for */
 } pkv_status;
 
 /* Device-side status bits OR-ed into *device_status. */
@@ -229,6 +230,86 @@ int pkv_paged_attention_decode_noalloc(void* out, const void* q, int32_t num_seq
                                        const int32_t* block_tables, int32_t max_blocks_per_seq,
                                        const int32_t* context_lens, float scale,
                                        int32_t* device_status, void* stream);
+
+/* ==== Block pool (host side) =================================================
+ *
+ * "AI 大模型推理优化技术详解", 2.1.2 Paged Attention: each sequence's KV cache is
+ * a list of fixed-size blocks; a table maps its logical blocks to physical
+ * blocks of a pool allocated up front; several logical blocks may map to one
+ * physical block, whose reference count says how many do, and a block whose
+ * count drops to 0 returns to the pool. "TACO-LLM 如何实现降本增效?",
+ * 2、使用 Prefix Cache 技术降低 TTFT: the KV of earlier prompts is kept in a prefix
+ * tree so a new prompt's matching prefix is looked up instead of recomputed.
+ *
+ * pkv_allocator manages the block ids of one pool of num_blocks blocks of 16
+ * tokens (the caches themselves stay with the caller). It is plain host code,
+ * not thread-safe (one owner thread), with deterministic choices:
+ *   - a new block is the lowest-numbered free block;
+ *   - sequences are identified by caller-chosen 64-bit ids;
+ *   - fork gives the child the parent's block list (every block's count + 1);
+ *   - appending to a sequence whose last block is shared (count > 1) first
+ *     replaces that block by a fresh one and reports the pair (copy-on-write);
+ *     the caller copies the block (pkv_copy_blocks) before writing new tokens;
+ *   - the prefix cache is a tree of full blocks keyed by (parent block, the 16
+ *     token ids); it holds one reference to each cached block; when the pool
+ *     has no free block, the least recently used cached leaf that nothing else
+ *     references is evicted and reused.
+ * Every call either succeeds or leaves the allocator unchanged. */
+typedef struct pkv_allocator pkv_allocator;
+
+/* A new allocator over blocks 0 .. num_blocks-1, all free. NULL if num_blocks
+ * is not in [1, 2^26] or memory runs out. */
+pkv_allocator* pkv_allocator_create(int32_t num_blocks);
+void pkv_allocator_destroy(pkv_allocator* a);
+
+/* Blocks not referenced by anything. Cached blocks that only the prefix cache
+ * references are not counted (pkv_allocator_evictable counts them). */
+int32_t pkv_allocator_free_blocks(const pkv_allocator* a);
+int32_t pkv_allocator_evictable(const pkv_allocator* a);
+/* References to a block (sequences + the prefix cache); -1 if out of range. */
+int32_t pkv_allocator_refcount(const pkv_allocator* a, int32_t block);
+
+/* A new empty sequence. PKV_ERR_INVALID_ARGUMENT if the id exists. */
+int pkv_seq_add(pkv_allocator* a, int64_t seq);
+/* A new sequence sharing all of parent's blocks and its length. */
+int pkv_seq_fork(pkv_allocator* a, int64_t parent, int64_t child);
+/* Drops the sequence; its blocks lose one reference each. */
+int pkv_seq_release(pkv_allocator* a, int64_t seq);
+/* Tokens in the sequence, or -1 if unknown. */
+int32_t pkv_seq_length(const pkv_allocator* a, int64_t seq);
+/* Writes min(capacity, blocks) block ids of the sequence (its block-table row)
+ * to out and returns the sequence's block count, or a negative status. */
+int32_t pkv_seq_block_table(const pkv_allocator* a, int64_t seq, int32_t* out, int32_t capacity);
+
+/* Reserves n new tokens at the end of the sequence and writes their slots
+ * (block * 16 + offset, n of them) to slots. If the sequence's last block was
+ * shared and receives tokens, it is replaced by a new block first: the pair is
+ * written to copy_src[0] / copy_dst[0] and *num_copies = 1 (else 0); copy_src
+ * and copy_dst must hold one entry. PKV_ERR_OUT_OF_BLOCKS if the pool (free and
+ * evictable blocks) is too small, with nothing changed. */
+int pkv_seq_append(pkv_allocator* a, int64_t seq, int32_t n, int32_t* slots, int32_t* copy_src,
+                   int32_t* copy_dst, int32_t* num_copies);
+
+/* Prefix cache. pkv_prefix_insert caches the sequence's full blocks holding its
+ * first n tokens (token ids in tokens[0..n)), under the chain of their
+ * contents; returns the number of blocks newly cached, or a negative status.
+ * pkv_seq_add_cached creates a sequence whose first blocks are the cached
+ * blocks matching the longest prefix of tokens[0..n) in whole blocks (each
+ * gains a reference) and writes the number of tokens they hold to
+ * *cached_tokens; the caller appends the rest. */
+int32_t pkv_prefix_insert(pkv_allocator* a, int64_t seq, const int32_t* tokens, int32_t n);
+int pkv_seq_add_cached(pkv_allocator* a, int64_t seq, const int32_t* tokens, int32_t n,
+                       int32_t* cached_tokens);
+
+/* ==== Block copy (device) ===================================================
+ * For i < n: physical block dst[i] of both caches becomes a copy of block
+ * src[i] (every head's 16 rows). src and dst are DEVICE int32 arrays; ids out of
+ * range are skipped and set PKV_DEV_BAD_BLOCK. The pairs must not overlap in a
+ * way that reads a block after it was written in the same call. Asynchronous on
+ * stream. */
+int pkv_copy_blocks(void* k_cache, void* v_cache, pkv_dtype kv_dtype, const pkv_cache_desc* cache,
+                    const int32_t* src, const int32_t* dst, int32_t n, int32_t* device_status,
+                    void* stream);
 
 /* Static description of a status code. Never NULL. */
 const char* pkv_error_string(int code);

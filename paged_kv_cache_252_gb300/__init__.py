@@ -8,6 +8,9 @@ Two calls, both hand-written CUDA for sm_103a behind a C ABI (``libpagedkv.so``)
   sequence over its blocks, one CTA stream per KV head serving the whole GQA
   group, causal among a sequence's query tokens (speculative verify).
 
+:class:`BlockAllocator` (host, C++) hands out the blocks: sequences, fork with
+copy-on-write (:func:`copy_blocks` performs the copies), and a prefix cache.
+
 The Python layer only marshals torch tensors into pointers and sizes; every
 step of the computation runs in the CUDA library. Importing this package does
 not load the library; the first call does, and fails loudly if it is missing.
@@ -19,4 +22,5 @@ from .api import (  # noqa: F401
     paged_attention_decode_tree,
     paged_attention_decode_noalloc, decode_workspace_bytes,
     library_path, load_library, alloc_kv_cache, PagedKVError,
+    BlockAllocator, copy_blocks,
 )

@@ -71,6 +71,34 @@ def load_library():
             vp, vp, i32, i32, i32, vp, vp, ctypes.c_int, P(_CacheDesc), vp, i32, vp,
             ctypes.c_float, vp, vp]
         lib.pkv_paged_attention_decode_noalloc.restype = ctypes.c_int
+        i64 = ctypes.c_int64
+        lib.pkv_allocator_create.argtypes = [i32]
+        lib.pkv_allocator_create.restype = vp
+        lib.pkv_allocator_destroy.argtypes = [vp]
+        lib.pkv_allocator_destroy.restype = None
+        for fn in ("pkv_allocator_free_blocks", "pkv_allocator_evictable"):
+            getattr(lib, fn).argtypes = [vp]
+            getattr(lib, fn).restype = i32
+        lib.pkv_allocator_refcount.argtypes = [vp, i32]
+        lib.pkv_allocator_refcount.restype = i32
+        lib.pkv_seq_add.argtypes = [vp, i64]
+        lib.pkv_seq_add.restype = ctypes.c_int
+        lib.pkv_seq_fork.argtypes = [vp, i64, i64]
+        lib.pkv_seq_fork.restype = ctypes.c_int
+        lib.pkv_seq_release.argtypes = [vp, i64]
+        lib.pkv_seq_release.restype = ctypes.c_int
+        lib.pkv_seq_length.argtypes = [vp, i64]
+        lib.pkv_seq_length.restype = i32
+        lib.pkv_seq_block_table.argtypes = [vp, i64, vp, i32]
+        lib.pkv_seq_block_table.restype = i32
+        lib.pkv_seq_append.argtypes = [vp, i64, i32, vp, vp, vp, vp]
+        lib.pkv_seq_append.restype = ctypes.c_int
+        lib.pkv_prefix_insert.argtypes = [vp, i64, vp, i32]
+        lib.pkv_prefix_insert.restype = i32
+        lib.pkv_seq_add_cached.argtypes = [vp, i64, vp, i32, vp]
+        lib.pkv_seq_add_cached.restype = ctypes.c_int
+        lib.pkv_copy_blocks.argtypes = [vp, vp, ctypes.c_int, P(_CacheDesc), vp, vp, i32, vp, vp]
+        lib.pkv_copy_blocks.restype = ctypes.c_int
         lib.pkv_error_string.argtypes = [ctypes.c_int]
         lib.pkv_error_string.restype = ctypes.c_char_p
         lib.pkv_version.restype = ctypes.c_int
@@ -289,3 +317,105 @@ def paged_attention_decode_tree(out, q, tree_masks, k_cache, v_cache, block_tabl
             _ptr(device_status), _stream_handle(stream, q.device))
     _check(rc, "paged_attention_decode_tree")
     return out
+
+
+# ------------------------------------------------------------------------------------
+# Block pool (host) and block copy (device)
+# ------------------------------------------------------------------------------------
+
+OUT_OF_BLOCKS = -6
+
+
+class BlockAllocator:
+    """Host-side block pool of ``num_blocks`` 16-token blocks (the C allocator in
+    libpagedkv.so): sequences, fork with copy-on-write, release, and a prefix
+    cache of full blocks. Block ids index the caches' first dimension; the
+    caches themselves stay with the caller."""
+
+    def __init__(self, num_blocks: int):
+        self._lib = load_library()
+        self._h = self._lib.pkv_allocator_create(int(num_blocks))
+        if not self._h:
+            raise PagedKVError(f"pkv_allocator_create({num_blocks}) failed")
+        self.num_blocks = int(num_blocks)
+
+    def close(self):
+        if self._h:
+            self._lib.pkv_allocator_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def free_blocks(self) -> int:
+        return int(self._lib.pkv_allocator_free_blocks(self._h))
+
+    def evictable(self) -> int:
+        return int(self._lib.pkv_allocator_evictable(self._h))
+
+    def refcount(self, block: int) -> int:
+        return int(self._lib.pkv_allocator_refcount(self._h, int(block)))
+
+    def add(self, seq: int):
+        _check(self._lib.pkv_seq_add(self._h, int(seq)), "seq_add")
+
+    def fork(self, parent: int, child: int):
+        _check(self._lib.pkv_seq_fork(self._h, int(parent), int(child)), "seq_fork")
+
+    def release(self, seq: int):
+        _check(self._lib.pkv_seq_release(self._h, int(seq)), "seq_release")
+
+    def length(self, seq: int) -> int:
+        return int(self._lib.pkv_seq_length(self._h, int(seq)))
+
+    def block_table(self, seq: int) -> list:
+        n = int(self._lib.pkv_seq_block_table(self._h, int(seq), None, 0))
+        if n < 0:
+            _check(n, "seq_block_table")
+        buf = (ctypes.c_int32 * max(n, 1))()
+        self._lib.pkv_seq_block_table(self._h, int(seq), buf, n)
+        return [int(buf[i]) for i in range(n)]
+
+    def append(self, seq: int, n: int):
+        """Reserve n tokens; returns (slots, copies) with copies a list of
+        (src, dst) block pairs to copy before the new tokens are written."""
+        slots = (ctypes.c_int32 * max(int(n), 1))()
+        src, dst, nc = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        rc = self._lib.pkv_seq_append(self._h, int(seq), int(n), slots, ctypes.byref(src),
+                                      ctypes.byref(dst), ctypes.byref(nc))
+        _check(rc, "seq_append")
+        copies = [(int(src.value), int(dst.value))] if nc.value else []
+        return [int(slots[i]) for i in range(int(n))], copies
+
+    def prefix_insert(self, seq: int, tokens) -> int:
+        arr = (ctypes.c_int32 * max(len(tokens), 1))(*[int(t) for t in tokens])
+        rc = int(self._lib.pkv_prefix_insert(self._h, int(seq), arr, len(tokens)))
+        if rc < 0:
+            _check(rc, "prefix_insert")
+        return rc
+
+    def add_cached(self, seq: int, tokens) -> int:
+        """New sequence starting from the longest cached prefix of ``tokens``
+        (whole blocks); returns the number of tokens it already holds."""
+        arr = (ctypes.c_int32 * max(len(tokens), 1))(*[int(t) for t in tokens])
+        got = ctypes.c_int32()
+        _check(self._lib.pkv_seq_add_cached(self._h, int(seq), arr, len(tokens), ctypes.byref(got)),
+               "seq_add_cached")
+        return int(got.value)
+
+
+def copy_blocks(k_cache, v_cache, src, dst, kv_dtype=None, *, device_status=None, stream=None):
+    """Physical block dst[i] of both caches becomes a copy of block src[i]
+    (int32 device tensors of equal length)."""
+    for n_, t in (("k_cache", k_cache), ("v_cache", v_cache), ("src", src), ("dst", dst)):
+        _need_cuda_contig(n_, t)
+    if src.dtype != torch.int32 or dst.dtype != torch.int32 or src.numel() != dst.numel():
+        raise PagedKVError("src and dst must be int32 tensors of equal length")
+    d = _desc(k_cache)
+    rc = load_library().pkv_copy_blocks(_ptr(k_cache), _ptr(v_cache), _kv_code(kv_dtype, k_cache),
+                                        ctypes.byref(d), _ptr(src), _ptr(dst), int(src.numel()),
+                                        _ptr(device_status), _stream_handle(stream, k_cache.device))
+    _check(rc, "copy_blocks")

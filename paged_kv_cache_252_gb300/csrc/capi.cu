@@ -239,6 +239,7 @@ const char* pkv_error_string(int code) {
     case PKV_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case PKV_ERR_CUDA: return "CUDA runtime error";
     case PKV_ERR_NO_DEVICE: return "no usable CUDA device";
+    case PKV_ERR_OUT_OF_BLOCKS: return "block pool exhausted";
     default: return "unknown status";
   }
 }
