@@ -11,7 +11,7 @@ combined inside it).
 
 Workloads (seeded, synthetic; see paged_kv_cache_252_gb300/workloads.py):
   tiny, 8b (default: Llama-3-8B-shaped decode layer, batch 64, fp16 KV),
-  8b_fp8, long, 70b_spec, mixed (decode + 4-token verify rows packed together).
+  8b_fp8, 8b_int8, long, 70b_spec, mixed (decode + 4-token verify rows packed together).
 
 value  = algorithmic bytes of the step / device time per step (GB/s), inputs
          resident in HBM. Algorithmic bytes: every visible token's K and V once,
@@ -202,11 +202,20 @@ def run_ours(args, rank, world, local):
     kv_bytes = w.kv_bytes_read()
     pools = args.pools or max(2, math.ceil(4 * l2 / kv_bytes))
 
-    caches = []
+    int8 = w.kv_dtype == "int8"
+
+    def write(kn, vn, sn, c):
+        if int8:
+            pkv.kv_cache_write_int8(kn, vn, sn, *c)
+        else:
+            pkv.kv_cache_write(kn, vn, sn, c[0], c[1])
+
+    caches = []   # (k_cache, v_cache[, k_scale, v_scale])
     for _ in range(pools):
         kc, vc = pkv.alloc_kv_cache(w.num_blocks, w.num_kv_heads, w.head_size, w.kv_dtype, dev)
-        pkv.kv_cache_write(vals["k_all"], vals["v_all"], vals["slot_all"], kc, vc)   # prefill
-        caches.append((kc, vc))
+        c = (kc, vc) + (pkv.alloc_kv_scales(w.num_blocks, w.num_kv_heads, dev) if int8 else ())
+        write(vals["k_all"], vals["v_all"], vals["slot_all"], c)   # prefill
+        caches.append(c)
     new_idx = vals["new_idx"]
     k_new = vals["k_all"][new_idx].contiguous()
     v_new = vals["v_all"][new_idx].contiguous()
@@ -219,17 +228,18 @@ def run_ours(args, rank, world, local):
     del vals
     torch.cuda.synchronize(dev)
 
-    def decode(o, q, kc, vc, bt_, cl_, cu_):
-        if cu_ is not None:
-            pkv.paged_attention_decode_varlen(o, q, cu_, kc, vc, bt_, cl_, w.q_per_seq, w.scale)
+    def decode(o, q, c, bt_, cl_, cu_):
+        if int8:
+            pkv.paged_attention_decode_int8(o, q, *c, bt_, cl_, w.q_per_seq, w.scale)
+        elif cu_ is not None:
+            pkv.paged_attention_decode_varlen(o, q, cu_, c[0], c[1], bt_, cl_, w.q_per_seq, w.scale)
         else:
-            pkv.paged_attention_decode(o, q, kc, vc, bt_, cl_, w.q_per_seq, w.scale)
+            pkv.paged_attention_decode(o, q, c[0], c[1], bt_, cl_, w.q_per_seq, w.scale)
 
     def step(i):
         p = i % pools
-        kc, vc = caches[p]
-        pkv.kv_cache_write(k_new, v_new, s_new, kc, vc)
-        decode(outs[p], qs[p], kc, vc, bt, cl, cu)
+        write(k_new, v_new, s_new, caches[p])
+        decode(outs[p], qs[p], caches[p], bt, cl, cu)
 
     step_bytes = kv_bytes + w.q_out_bytes() + w.write_bytes()
     attn_bytes = kv_bytes + w.q_out_bytes()
@@ -259,9 +269,8 @@ def run_ours(args, rank, world, local):
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_r)]
     for i in range(n_r):
         p = i % pools
-        kc, vc = caches[p]
         evs[i][0].record()
-        decode(outs[p], qs[p], kc, vc, bt, cl, cu)
+        decode(outs[p], qs[p], caches[p], bt, cl, cu)
         evs[i][1].record()
     torch.cuda.synchronize(dev)
     dec_s = float(np.mean([a.elapsed_time(b) for a, b in evs])) / 1e3
@@ -282,7 +291,6 @@ def run_ours(args, rank, world, local):
 
         def e2e_step(i):
             p = i % pools
-            kc, vc = caches[p]
             dq.copy_(host["q"], non_blocking=True)
             dk.copy_(host["k_new"], non_blocking=True)
             dv.copy_(host["v_new"], non_blocking=True)
@@ -291,8 +299,8 @@ def run_ours(args, rank, world, local):
             dcl.copy_(host["cl"], non_blocking=True)
             if dcu is not None:
                 dcu.copy_(host["cu"], non_blocking=True)
-            pkv.kv_cache_write(dk, dv, ds, kc, vc)
-            decode(outs[p], dq, kc, vc, dbt, dcl, dcu)
+            write(dk, dv, ds, caches[p])
+            decode(outs[p], dq, caches[p], dbt, dcl, dcu)
             out_h.copy_(outs[p], non_blocking=True)
 
         for i in range(args.warmup):
@@ -371,34 +379,47 @@ def _oracle_inputs(w, seqs):
     new = np.zeros(w.num_tokens_total, dtype=bool)
     new[w.new_token_index()] = True
     pre, stp = mask & ~new, mask & new
-    dt = np.uint8 if w.kv_dtype == "e5m2" else np.uint16
+    dt = {"e5m2": np.uint8, "int8": np.int8}.get(w.kv_dtype, np.uint16)
     shape = (w.num_blocks, w.num_kv_heads, 16, w.head_size)
     kc, vc = np.zeros(shape, dt), np.zeros(shape, dt)
-    code = {"fp16": 0, "bf16": 1, "e5m2": 2}[w.kv_dtype]
+    code = {"fp16": 0, "bf16": 1, "e5m2": 2, "int8": 3}[w.kv_dtype]
     src = 1 if w.kv_dtype == "bf16" else 0
-    oracle.kv_cache_write(k_all[pre], v_all[pre], src, slots[pre], kc, vc, code)
-    return {"kc": kc, "vc": vc, "q": bits(vals["q"]), "k_new": k_all[stp], "v_new": v_all[stp],
-            "s_new": slots[stp], "src": src, "code": code}
+    ks = vs = None
+    if code == 3:
+        ks, vs = np.zeros(shape[:3], np.float32), np.zeros(shape[:3], np.float32)
+    inp = {"kc": kc, "vc": vc, "ks": ks, "vs": vs, "q": bits(vals["q"]), "k_new": k_all[stp],
+           "v_new": v_all[stp], "s_new": slots[stp], "src": src, "code": code}
+    _oracle_write(inp, k_all[pre], v_all[pre], slots[pre])
+    return inp
+
+
+def _oracle_write(inp, k, v, slots):
+    import oracle
+    if inp["code"] == 3:
+        oracle.kv_cache_write_int8(k, v, slots, inp["kc"], inp["vc"], inp["ks"], inp["vs"])
+    else:
+        oracle.kv_cache_write(k, v, inp["src"], slots, inp["kc"], inp["vc"], inp["code"])
 
 
 def _oracle_step(w, inp, seqs, threads):
     import oracle
-    oracle.kv_cache_write(inp["k_new"], inp["v_new"], inp["src"], inp["s_new"], inp["kc"], inp["vc"],
-                          inp["code"])
+    _oracle_write(inp, inp["k_new"], inp["v_new"], inp["s_new"])
     qcode = 1 if w.q_dtype == "bf16" else 0
     _, _, rc = oracle.paged_attention(inp["q"], qcode, w.q_per_seq, inp["kc"], inp["vc"], inp["code"],
                                       w.block_tables, w.context_lens, w.scale, seqs=seqs,
                                       num_threads=threads,
-                                      cu_q_lens=w.cu_q_lens() if w.q_lens is not None else None)
+                                      cu_q_lens=w.cu_q_lens() if w.q_lens is not None else None,
+                                      k_scale=inp["ks"], v_scale=inp["vs"])
     assert rc == 0
 
 
 def _sample_bytes(w, seqs):
     lens = w.context_lens[seqs].astype(np.int64)
-    kv = int(lens.sum()) * w.num_kv_heads * w.head_size * 2 * w.kv_elem_bytes
+    row = w.head_size * w.kv_elem_bytes + w.kv_row_extra_bytes
+    kv = int(lens.sum()) * w.num_kv_heads * row * 2
     t = int(w.query_lens()[seqs].sum())
     qo = 2 * t * w.num_q_heads * w.head_size * 2
-    wr = t * w.num_kv_heads * w.head_size * (4 + w.kv_elem_bytes) + 4 * t
+    wr = t * w.num_kv_heads * (w.head_size * 4 + 2 * row) + 4 * t
     return kv + qo + wr
 
 
@@ -471,7 +492,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--config", default="8b", choices=["tiny", "8b", "8b_fp8", "long", "70b_spec", "mixed"])
+    ap.add_argument("--config", default="8b", choices=["tiny", "8b", "8b_fp8", "8b_int8", "long", "70b_spec", "mixed"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--pools", type=int, default=0, help="KV pools to rotate (default: >4x L2)")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)

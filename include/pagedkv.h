@@ -51,7 +51,8 @@ extern "C" {
 typedef enum {
   PKV_FP16 = 0,
   PKV_BF16 = 1,
-  PKV_FP8_E5M2 = 2
+  PKV_FP8_E5M2 = 2,
+  PKV_INT8 = 3      /* int8 codes with float32 row scales: see pkv_kv_cache_write_int8 */
 } pkv_dtype;
 
 typedef enum {
@@ -230,6 +231,34 @@ int pkv_paged_attention_decode_noalloc(void* out, const void* q, int32_t num_seq
                                        const int32_t* block_tables, int32_t max_blocks_per_seq,
                                        const int32_t* context_lens, float scale,
                                        int32_t* device_status, void* stream);
+
+/* ==== INT8 KV cache ===========================================================
+ *
+ * The inference-framework survey lists "KV Cache INT8 量化" for LMDeploy
+ * without a codec; this one is symmetric per (token, KV head) row:
+ *   scale = max|x| / 127,  code = round-half-even(x / scale) clamped to [-127, 127],
+ * both divisions in IEEE fp32; an all-zero row has scale 0 and codes 0; an
+ * element's value is code * scale.
+ *
+ * Caches: int8 [num_blocks][num_kv_heads][16][head_size]; scales: float32
+ * [num_blocks][num_kv_heads][16] (one per cached row), all 16-byte aligned.
+ * key/value: fp16 [num_tokens][num_kv_heads][head_size]. Slots as in
+ * pkv_kv_cache_write (-1 skipped, other out-of-range slots skipped and flagged). */
+int pkv_kv_cache_write_int8(const void* key, const void* value, int32_t num_tokens,
+                            const int32_t* slot_mapping, void* k_cache, void* v_cache,
+                            float* k_scale, float* v_scale, const pkv_cache_desc* cache,
+                            int32_t* device_status, void* stream);
+
+/* pkv_paged_attention_decode over an INT8 cache (q and out fp16): each token's
+ * score is scaled by its K row scale and its probability by its V row scale.
+ * Workspace as for pkv_paged_attention_decode (pkv_decode_workspace_bytes). */
+int pkv_paged_attention_decode_int8(void* out, const void* q, int32_t num_seqs, int32_t num_q_heads,
+                                    int32_t q_per_seq, const void* k_cache, const void* v_cache,
+                                    const float* k_scale, const float* v_scale,
+                                    const pkv_cache_desc* cache, const int32_t* block_tables,
+                                    int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                    float scale, void* workspace, size_t workspace_bytes,
+                                    int32_t* device_status, void* stream);
 
 /* ==== Block pool (host side) =================================================
  *

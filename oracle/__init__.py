@@ -5,9 +5,9 @@ reference leg may import this package. The product path (the CUDA library and
 its Python binding) never imports it.
 """
 from .oracle import (  # noqa: F401
-    FP16, BF16, E5M2,
+    FP16, BF16, E5M2, INT8,
     build, load,
     e5m2_from_fp16, fp16_from_e5m2, e5m2_to_f64, fp16_to_f64, bf16_to_f64,
     round_from_f64, decode_to_f64,
-    kv_cache_write, paged_attention, hardware_threads,
+    kv_cache_write, kv_cache_write_int8, paged_attention, hardware_threads,
 )

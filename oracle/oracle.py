@@ -15,7 +15,7 @@ import threading
 
 import numpy as np
 
-FP16, BF16, E5M2 = 0, 1, 2
+FP16, BF16, E5M2, INT8 = 0, 1, 2, 3
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "pagedkv_oracle.cpp")
@@ -77,8 +77,13 @@ def load():
             P(dbl), P(dbl), i64, P(ctypes.c_uint16), ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_int, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_int, P(i32), ctypes.c_int, P(i32), dbl, P(i32), ctypes.c_int, ctypes.c_int,
-            P(i32), P(ctypes.c_uint64)]
+            P(i32), P(ctypes.c_uint64), P(ctypes.c_float), P(ctypes.c_float)]
         lib.orc_paged_attention.restype = ctypes.c_int
+        lib.orc_kv_cache_write_int8.argtypes = [
+            P(ctypes.c_uint16), P(ctypes.c_uint16), ctypes.c_int, P(i32), P(ctypes.c_int8),
+            P(ctypes.c_int8), P(ctypes.c_float), P(ctypes.c_float), ctypes.c_int, ctypes.c_int,
+            ctypes.c_int, ctypes.c_int]
+        lib.orc_kv_cache_write_int8.restype = ctypes.c_int
         lib.orc_hardware_threads.restype = ctypes.c_int
         assert lib.orc_version() == 1
         _lib = lib
@@ -153,10 +158,26 @@ def kv_cache_write(key, value, src_dtype: int, slot_mapping, k_cache, v_cache,
         v_cache.ctypes.data_as(ctypes.c_void_p), kv_dtype, NB, block_size, Hkv, D)
 
 
+def kv_cache_write_int8(key, value, slot_mapping, k_cache, v_cache, k_scale, v_scale,
+                        block_size: int = 16) -> int:
+    """INT8 cache write: fp16 key/value [T, Hkv, D] -> int8 caches [NB, Hkv, block_size, D]
+    and float32 scales [NB, Hkv, block_size], in place."""
+    key, value = _u16(key), _u16(value)
+    T, Hkv, D = key.shape
+    slot_mapping = np.ascontiguousarray(slot_mapping, dtype=np.int32)
+    for a in (k_cache, v_cache, k_scale, v_scale):
+        assert a.flags.c_contiguous
+    assert k_cache.dtype == np.int8 and k_scale.dtype == np.float32
+    return load().orc_kv_cache_write_int8(
+        _p(key, ctypes.c_uint16), _p(value, ctypes.c_uint16), T, _p(slot_mapping, ctypes.c_int32),
+        _p(k_cache, ctypes.c_int8), _p(v_cache, ctypes.c_int8), _p(k_scale, ctypes.c_float),
+        _p(v_scale, ctypes.c_float), k_cache.shape[0], block_size, Hkv, D)
+
+
 def paged_attention(q, q_dtype: int, q_per_seq: int, k_cache, v_cache, kv_dtype: int,
                     block_tables, context_lens, scale: float, *, block_size: int = 16,
                     seqs=None, num_threads: int = 1, want_weights: bool = False,
-                    out=None, cu_q_lens=None, tree_masks=None):
+                    out=None, cu_q_lens=None, tree_masks=None, k_scale=None, v_scale=None):
     """fp64 paged decode attention.
 
     q: [rows, Hq, D] uint16 patterns: S*q_per_seq rows, or cu_q_lens[S] rows when
@@ -164,6 +185,7 @@ def paged_attention(q, q_dtype: int, q_per_seq: int, k_cache, v_cache, kv_dtype:
     Caches: [NB, Hkv, block_size, D]. Returns (out_f64 [rows, Hq, D], weights or
     None, rc). Only the rows of ``seqs`` are computed when given. tree_masks (uint64,
     one per query row) replaces the causal rule: bit i lets a token see draft token i.
+    An INT8 cache (kv_dtype 3) needs its float32 scales k_scale / v_scale [NB, Hkv, block_size].
     """
     q = _u16(q)
     SN, Hq, D = q.shape
@@ -181,6 +203,8 @@ def paged_attention(q, q_dtype: int, q_per_seq: int, k_cache, v_cache, kv_dtype:
     if want_weights:
         wstride = mbs * block_size
         weights = np.zeros((SN, Hq, wstride), dtype=np.float64)
+    ks = None if k_scale is None else np.ascontiguousarray(k_scale, dtype=np.float32)
+    vs = None if v_scale is None else np.ascontiguousarray(v_scale, dtype=np.float32)
     subset = None
     nsub = 0
     if seqs is not None:
@@ -192,7 +216,8 @@ def paged_attention(q, q_dtype: int, q_per_seq: int, k_cache, v_cache, kv_dtype:
         k_cache.ctypes.data_as(ctypes.c_void_p), v_cache.ctypes.data_as(ctypes.c_void_p),
         kv_dtype, NB, block_size, Hkv, D, _p(block_tables, ctypes.c_int32), mbs,
         _p(context_lens, ctypes.c_int32), float(scale), _p(subset, ctypes.c_int32), nsub,
-        int(num_threads), _p(cu, ctypes.c_int32), _p(tm, ctypes.c_uint64))
+        int(num_threads), _p(cu, ctypes.c_int32), _p(tm, ctypes.c_uint64),
+        _p(ks, ctypes.c_float), _p(vs, ctypes.c_float))
     return out, weights, rc
 
 

@@ -29,6 +29,12 @@
 //    positions p <= ctx - n + j (causal among the query tokens).
 //  * query head hq uses KV head hq / G (contiguous groups).
 //  * slot -1 in a slot mapping means "do not write".
+//  * INT8 KV cache (the LMDeploy section of the inference-framework survey says
+//    only "KV Cache INT8 量化"): symmetric codes per (token, KV head) row:
+//    scale = max|x| / 127 and code = round-half-even(x / scale) clamped to
+//    [-127, 127], both divisions in fp32 (the precision the kernel decides
+//    the code in); an all-zero row has scale 0 and codes 0. A cached element's
+//    value is code * scale.
 //
 // Arithmetic is fp64 throughout (products, sums, exp), with a single final
 // rounding to the query dtype done by orc_round_from_f64.
@@ -42,7 +48,7 @@
 
 namespace {
 
-enum { ORC_FP16 = 0, ORC_BF16 = 1, ORC_E5M2 = 2 };
+enum { ORC_FP16 = 0, ORC_BF16 = 1, ORC_E5M2 = 2, ORC_INT8 = 3 };
 
 // ---- scalar decodes: bit pattern -> exact double --------------------------------
 
@@ -176,7 +182,20 @@ uint8_t e5m2_from_fp16_bits(uint16_t h) {
   return encode_e5m2(r);
 }
 
-double kv_value(const void* cache, int kv_dtype, int64_t idx) {
+// One INT8 code: fp32 division by the row's scale, round half to even, clamp.
+int8_t int8_code(float x, float scale) {
+  if (scale == 0.0f) return 0;
+  float q = std::nearbyint(x / scale);
+  q = std::fmax(q, -127.0f);
+  q = std::fmin(q, 127.0f);
+  return (int8_t)q;
+}
+
+// Element idx of a cache; INT8 elements are code * scale of their row
+// (scales: one float per (slot, head) row of head_size elements).
+double kv_value(const void* cache, int kv_dtype, int64_t idx, const float* scales = nullptr,
+                int head_size = 1) {
+  if (kv_dtype == ORC_INT8) return (double)((const int8_t*)cache)[idx] * (double)scales[idx / head_size];
   if (kv_dtype == ORC_E5M2) return e5m2_value(((const uint8_t*)cache)[idx]);
   const uint16_t bits = ((const uint16_t*)cache)[idx];
   return kv_dtype == ORC_BF16 ? bf16_value(bits) : fp16_value(bits);
@@ -263,6 +282,36 @@ int orc_kv_cache_write(const uint16_t* key, const uint16_t* value, int src_dtype
   return rc;
 }
 
+// INT8 cache write: key/value fp16 [num_tokens][num_kv_heads][head_size];
+// caches int8 [num_blocks][num_kv_heads][block_size][head_size]; scales float
+// [num_blocks][num_kv_heads][block_size]. Codes as in the file header.
+int orc_kv_cache_write_int8(const uint16_t* key, const uint16_t* value, int num_tokens,
+                            const int32_t* slot_mapping, int8_t* k_cache, int8_t* v_cache,
+                            float* k_scale, float* v_scale, int num_blocks, int block_size,
+                            int num_kv_heads, int head_size) {
+  int rc = 0;
+  const int64_t num_slots = (int64_t)num_blocks * block_size;
+  for (int t = 0; t < num_tokens; ++t) {
+    const int64_t slot = slot_mapping[t];
+    if (slot == -1) continue;
+    if (slot < 0 || slot >= num_slots) { rc = -1; continue; }
+    const int64_t block = slot / block_size, offset = slot % block_size;
+    for (int h = 0; h < num_kv_heads; ++h) {
+      const int64_t row = (block * num_kv_heads + h) * block_size + offset;
+      for (int which = 0; which < 2; ++which) {
+        const uint16_t* src = (which ? value : key) + ((int64_t)t * num_kv_heads + h) * head_size;
+        float amax = 0.0f;
+        for (int d = 0; d < head_size; ++d) amax = std::fmax(amax, std::fabs((float)fp16_value(src[d])));
+        const float scale = amax / 127.0f;
+        int8_t* dst = (which ? v_cache : k_cache) + row * head_size;
+        for (int d = 0; d < head_size; ++d) dst[d] = int8_code((float)fp16_value(src[d]), scale);
+        (which ? v_scale : k_scale)[row] = scale;
+      }
+    }
+  }
+  return rc;
+}
+
 // Paged decode attention, fp64.
 //
 // q: [rows][num_q_heads][head_size] in q_dtype (fp16/bf16). With cu_q_lens NULL,
@@ -284,7 +333,9 @@ int orc_paged_attention(double* out, double* weights, int64_t weights_stride,
                         int head_size, const int32_t* block_tables,
                         int max_blocks_per_seq, const int32_t* context_lens, double scale,
                         const int32_t* seq_subset, int n_subset, int num_threads,
-                        const int32_t* cu_q_lens, const uint64_t* tree_masks) {
+                        const int32_t* cu_q_lens, const uint64_t* tree_masks,
+                        const float* k_scale, const float* v_scale) {
+  if (kv_dtype == ORC_INT8 && (!k_scale || !v_scale)) return -1;
   if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return -1;
   const int group = num_q_heads / num_kv_heads;
   // Query tokens and first query row of sequence s.
@@ -348,7 +399,8 @@ int orc_paged_attention(double* out, double* weights, int64_t weights_stride,
         if (!kv_index(p, &kbase)) { ok = false; break; }
         double dot = 0.0;
         for (int d = 0; d < head_size; ++d) {
-          dot += src_value(q, q_dtype, qrow * head_size + d) * kv_value(k_cache, kv_dtype, kbase + d);
+          dot += src_value(q, q_dtype, qrow * head_size + d) *
+                 kv_value(k_cache, kv_dtype, kbase + d, k_scale, head_size);
         }
         logits[p] = scale * dot;
       }
@@ -372,7 +424,7 @@ int orc_paged_attention(double* out, double* weights, int64_t weights_stride,
         if (weights) weights[qrow * weights_stride + p] = w;
         int64_t vbase;
         kv_index(p, &vbase);
-        for (int d = 0; d < head_size; ++d) o[d] += w * kv_value(v_cache, kv_dtype, vbase + d);
+        for (int d = 0; d < head_size; ++d) o[d] += w * kv_value(v_cache, kv_dtype, vbase + d, v_scale, head_size);
       }
     }
   };

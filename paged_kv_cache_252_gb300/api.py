@@ -13,10 +13,10 @@ import threading
 
 import torch
 
-KV_FP16, KV_BF16, KV_E5M2 = 0, 1, 2
-_NAMES = {"fp16": KV_FP16, "bf16": KV_BF16, "e5m2": KV_E5M2, "fp8_e5m2": KV_E5M2}
+KV_FP16, KV_BF16, KV_E5M2, KV_INT8 = 0, 1, 2, 3
+_NAMES = {"fp16": KV_FP16, "bf16": KV_BF16, "e5m2": KV_E5M2, "fp8_e5m2": KV_E5M2, "int8": KV_INT8}
 _TORCH = {torch.float16: KV_FP16, torch.bfloat16: KV_BF16, torch.uint8: KV_E5M2,
-          torch.float8_e5m2: KV_E5M2}
+          torch.float8_e5m2: KV_E5M2, torch.int8: KV_INT8}
 BLOCK_SIZE = 16
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -99,6 +99,12 @@ def load_library():
         lib.pkv_seq_add_cached.restype = ctypes.c_int
         lib.pkv_copy_blocks.argtypes = [vp, vp, ctypes.c_int, P(_CacheDesc), vp, vp, i32, vp, vp]
         lib.pkv_copy_blocks.restype = ctypes.c_int
+        lib.pkv_kv_cache_write_int8.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, P(_CacheDesc), vp, vp]
+        lib.pkv_kv_cache_write_int8.restype = ctypes.c_int
+        lib.pkv_paged_attention_decode_int8.argtypes = [
+            vp, vp, i32, i32, i32, vp, vp, vp, vp, P(_CacheDesc), vp, i32, vp, ctypes.c_float, vp,
+            ctypes.c_size_t, vp, vp]
+        lib.pkv_paged_attention_decode_int8.restype = ctypes.c_int
         lib.pkv_error_string.argtypes = [ctypes.c_int]
         lib.pkv_error_string.restype = ctypes.c_char_p
         lib.pkv_version.restype = ctypes.c_int
@@ -157,10 +163,60 @@ def alloc_kv_cache(num_blocks: int, num_kv_heads: int, head_size: int, kv_dtype,
                    device="cuda", zero: bool = True):
     """Allocate a K/V cache pair [num_blocks, num_kv_heads, 16, head_size]."""
     code = _NAMES[kv_dtype] if isinstance(kv_dtype, str) else int(kv_dtype)
-    dt = {KV_FP16: torch.float16, KV_BF16: torch.bfloat16, KV_E5M2: torch.uint8}[code]
+    dt = {KV_FP16: torch.float16, KV_BF16: torch.bfloat16, KV_E5M2: torch.uint8, KV_INT8: torch.int8}[code]
     mk = torch.zeros if zero else torch.empty
     shape = (num_blocks, num_kv_heads, BLOCK_SIZE, head_size)
     return mk(shape, dtype=dt, device=device), mk(shape, dtype=dt, device=device)
+
+
+def alloc_kv_scales(num_blocks: int, num_kv_heads: int, device="cuda"):
+    """Row scales of an INT8 cache pair: float32 [num_blocks, num_kv_heads, 16] each."""
+    shape = (num_blocks, num_kv_heads, BLOCK_SIZE)
+    return (torch.zeros(shape, dtype=torch.float32, device=device),
+            torch.zeros(shape, dtype=torch.float32, device=device))
+
+
+def kv_cache_write_int8(key, value, slot_mapping, k_cache, v_cache, k_scale, v_scale, *,
+                        device_status=None, stream=None):
+    """Quantise fp16 key/value [T, Hkv, D] into INT8 caches and their row scales."""
+    for n, t in (("key", key), ("value", value), ("slot_mapping", slot_mapping), ("k_cache", k_cache),
+                 ("v_cache", v_cache), ("k_scale", k_scale), ("v_scale", v_scale)):
+        _need_cuda_contig(n, t)
+    if key.dtype != torch.float16 or k_cache.dtype != torch.int8 or k_scale.dtype != torch.float32:
+        raise PagedKVError("INT8 cache write takes fp16 key/value, int8 caches, float32 scales")
+    if slot_mapping.dtype != torch.int32:
+        raise PagedKVError("slot_mapping must be int32")
+    d = _desc(k_cache)
+    rc = load_library().pkv_kv_cache_write_int8(
+        _ptr(key), _ptr(value), int(key.shape[0]), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
+        _ptr(k_scale), _ptr(v_scale), ctypes.byref(d), _ptr(device_status), _stream_handle(stream, key.device))
+    _check(rc, "kv_cache_write_int8")
+
+
+def paged_attention_decode_int8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                                q_per_seq: int, scale: float, *, workspace=None, device_status=None,
+                                stream=None):
+    """paged_attention_decode over an INT8 cache with its row scales (q/out fp16)."""
+    for n, t in (("out", out), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("k_scale", k_scale),
+                 ("v_scale", v_scale), ("block_tables", block_tables), ("context_lens", context_lens)):
+        _need_cuda_contig(n, t)
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise PagedKVError("block_tables and context_lens must be int32")
+    S = int(context_lens.shape[0])
+    Hq = int(q.shape[1])
+    d = _desc(k_cache)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        need = int(lib.pkv_decode_workspace_bytes(S, Hq, q_per_seq, ctypes.byref(d)))
+        if workspace is None:
+            workspace = _workspace(need, q.device)
+        rc = lib.pkv_paged_attention_decode_int8(
+            _ptr(out), _ptr(q), S, Hq, int(q_per_seq), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+            _ptr(v_scale), ctypes.byref(d), _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens),
+            float(scale), _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+            _ptr(device_status), _stream_handle(stream, q.device))
+    _check(rc, "paged_attention_decode_int8")
+    return out
 
 
 def kv_cache_write(key, value, slot_mapping, k_cache, v_cache, kv_dtype=None, *,

@@ -24,7 +24,7 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpagedkv.so")
 
 SOURCES = ["capi.cu", "kv_cache_write.cu", "decode_f16.cu", "decode_bf16.cu", "decode_e5m2.cu",
-           "decode_tc.cu", "noalloc.cu", "copy_blocks.cu", "block_allocator.cpp"]
+           "decode_tc.cu", "decode_int8.cu", "noalloc.cu", "copy_blocks.cu", "block_allocator.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -30,7 +30,7 @@ struct DeviceState {
   int sm_count = 0;
   bool write_attr_done = false;
   // [kv][d==128][ntw==2]
-  GeomEntry geom[3][2][2];
+  GeomEntry geom[4][2][2];
   // tcgen05 kernel, [rc - 1]
   GeomEntry tc_geom[2];
 };
@@ -70,6 +70,7 @@ const void* decode_fn(int kv, int d, int ntw) {
     case kKvF16: return decode_kernel_ptr_f16(d, ntw);
     case kKvBf16: return decode_kernel_ptr_bf16(d, ntw);
     case kKvE5m2: return decode_kernel_ptr_e5m2(d, ntw);
+    case kKvInt8: return decode_kernel_ptr_int8(d, ntw);
     default: return nullptr;
   }
 }
@@ -303,7 +304,7 @@ size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t
   // The grid follows the kv dtype's occupancy; size for the largest over the
   // supported dtypes so that one workspace serves any of them.
   int ctas = 1;
-  for (int kv = kKvF16; kv <= kKvE5m2; ++kv) {
+  for (int kv = kKvF16; kv <= kKvInt8; ++kv) {
     GeomEntry* ge = nullptr;
     if (get_geometry(st, kv, cache->head_size, rows, &ge)) return 0;
     if (ge->ctas_per_sm > ctas) ctas = ge->ctas_per_sm;
@@ -318,7 +319,8 @@ namespace {
 // Shared body of the decode entry points; cu_q_lens null means q_per_seq query
 // tokens for every sequence.
 int decode_impl(void* out, const void* q, const int32_t* cu_q_lens,
-                const unsigned long long* tree_masks, int32_t num_seqs,
+                const unsigned long long* tree_masks, const float* k_scale, const float* v_scale,
+                int32_t num_seqs,
                 int32_t num_q_heads, int32_t q_per_seq, const void* k_cache, const void* v_cache,
                 pkv_dtype kv_dtype, const pkv_cache_desc* cache, const int32_t* block_tables,
                 int32_t max_blocks_per_seq, const int32_t* context_lens, float scale,
@@ -326,9 +328,13 @@ int decode_impl(void* out, const void* q, const int32_t* cu_q_lens,
   if (num_seqs < 0 || num_q_heads <= 0 || q_per_seq <= 0 || max_blocks_per_seq <= 0 ||
       !valid_cache(cache))
     return PKV_ERR_INVALID_ARGUMENT;
-  if (kv_dtype != PKV_FP16 && kv_dtype != PKV_BF16 && kv_dtype != PKV_FP8_E5M2)
+  if (kv_dtype != PKV_FP16 && kv_dtype != PKV_BF16 && kv_dtype != PKV_FP8_E5M2 && kv_dtype != PKV_INT8)
     return PKV_ERR_UNSUPPORTED;
   if (num_q_heads % cache->num_kv_heads != 0) return PKV_ERR_INVALID_ARGUMENT;
+  // An INT8 cache is read with its row scales, 16-byte aligned (each block's
+  // 16 scales move as one 64-byte copy).
+  if (kv_dtype == PKV_INT8 && (!k_scale || !v_scale || !aligned16(k_scale) || !aligned16(v_scale)))
+    return PKV_ERR_INVALID_ARGUMENT;
   const int group = num_q_heads / cache->num_kv_heads;
   const long long rows_ll = static_cast<long long>(group) * q_per_seq;
   if (rows_ll > kMaxRows) return PKV_ERR_UNSUPPORTED;
@@ -386,6 +392,8 @@ int decode_impl(void* out, const void* q, const int32_t* cu_q_lens,
   a.context_lens = context_lens;
   a.cu_q_lens = cu_q_lens;
   a.tree_masks = tree_masks;
+  a.k_scale = kv_dtype == PKV_INT8 ? k_scale : nullptr;
+  a.v_scale = kv_dtype == PKV_INT8 ? v_scale : nullptr;
   a.piece_counts = reinterpret_cast<unsigned long long*>(ws);
   a.partials = reinterpret_cast<float*>(ws + desc_bytes(units));
   a.status = device_status;
@@ -431,7 +439,8 @@ int pkv_paged_attention_decode(void* out, const void* q, int32_t num_seqs, int32
                                const int32_t* block_tables, int32_t max_blocks_per_seq,
                                const int32_t* context_lens, float scale, void* workspace,
                                size_t workspace_bytes, int32_t* device_status, void* stream) {
-  return decode_impl(out, q, nullptr, nullptr, num_seqs, num_q_heads, q_per_seq, k_cache, v_cache, kv_dtype,
+  return decode_impl(out, q, nullptr, nullptr, nullptr, nullptr, num_seqs, num_q_heads, q_per_seq, k_cache,
+                     v_cache, kv_dtype,
                      cache, block_tables, max_blocks_per_seq, context_lens, scale, workspace,
                      workspace_bytes, device_status, stream);
 }
@@ -444,7 +453,8 @@ int pkv_paged_attention_decode_varlen(void* out, const void* q, const int32_t* c
                                       float scale, void* workspace, size_t workspace_bytes,
                                       int32_t* device_status, void* stream) {
   if (num_seqs > 0 && !cu_q_lens) return PKV_ERR_INVALID_ARGUMENT;
-  return decode_impl(out, q, cu_q_lens, nullptr, num_seqs, num_q_heads, max_q_per_seq, k_cache, v_cache,
+  return decode_impl(out, q, cu_q_lens, nullptr, nullptr, nullptr, num_seqs, num_q_heads, max_q_per_seq,
+                     k_cache, v_cache,
                      kv_dtype, cache, block_tables, max_blocks_per_seq, context_lens, scale,
                      workspace, workspace_bytes, device_status, stream);
 }
@@ -459,10 +469,64 @@ int pkv_paged_attention_decode_tree(void* out, const void* q, const int32_t* cu_
                                     int32_t* device_status, void* stream) {
   if (num_seqs > 0 && !tree_masks) return PKV_ERR_INVALID_ARGUMENT;
   if (max_q_per_seq > 64) return PKV_ERR_UNSUPPORTED;
-  return decode_impl(out, q, cu_q_lens, reinterpret_cast<const unsigned long long*>(tree_masks),
-                     num_seqs, num_q_heads, max_q_per_seq, k_cache, v_cache, kv_dtype, cache,
+  return decode_impl(out, q, cu_q_lens, reinterpret_cast<const unsigned long long*>(tree_masks), nullptr,
+                     nullptr, num_seqs, num_q_heads, max_q_per_seq, k_cache, v_cache, kv_dtype, cache,
                      block_tables, max_blocks_per_seq, context_lens, scale, workspace,
                      workspace_bytes, device_status, stream);
+}
+
+int pkv_paged_attention_decode_int8(void* out, const void* q, int32_t num_seqs, int32_t num_q_heads,
+                                    int32_t q_per_seq, const void* k_cache, const void* v_cache,
+                                    const float* k_scale, const float* v_scale, const pkv_cache_desc* cache,
+                                    const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                    const int32_t* context_lens, float scale, void* workspace,
+                                    size_t workspace_bytes, int32_t* device_status, void* stream) {
+  return decode_impl(out, q, nullptr, nullptr, k_scale, v_scale, num_seqs, num_q_heads, q_per_seq, k_cache,
+                     v_cache, PKV_INT8, cache, block_tables, max_blocks_per_seq, context_lens, scale, workspace,
+                     workspace_bytes, device_status, stream);
+}
+
+int pkv_kv_cache_write_int8(const void* key, const void* value, int32_t num_tokens, const int32_t* slot_mapping,
+                            void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                            const pkv_cache_desc* cache, int32_t* device_status, void* stream) {
+  if (num_tokens < 0 || !valid_cache(cache)) return PKV_ERR_INVALID_ARGUMENT;
+  if (num_tokens == 0) return PKV_OK;
+  if (!key || !value || !slot_mapping || !k_cache || !v_cache || !k_scale || !v_scale)
+    return PKV_ERR_INVALID_ARGUMENT;
+  if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(k_scale) || !aligned16(v_scale) || !aligned4(slot_mapping) ||
+      (device_status && !aligned4(device_status)))
+    return PKV_ERR_INVALID_ARGUMENT;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* st = nullptr;
+  if (int rc = current_device_state(&st)) return rc;
+  CacheWriteArgs a{};
+  a.key = static_cast<const uint4*>(key);
+  a.value = static_cast<const uint4*>(value);
+  a.slot_mapping = slot_mapping;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.status = device_status;
+  a.num_slots = static_cast<long long>(cache->num_blocks) * kBlockSize;
+  a.num_tokens = num_tokens;
+  a.num_kv_heads = cache->num_kv_heads;
+  a.head_size = cache->head_size;
+  a.kv = kKvInt8;
+  // One warp per (token, head) row of K or V.
+  const long long rows = 2ll * num_tokens * cache->num_kv_heads;
+  long long blocks = (rows * 32 + 255) / 256;
+  const long long max_blocks = static_cast<long long>(st->sm_count) * 16;
+  if (blocks > max_blocks) blocks = max_blocks;
+  void* args[1] = {&a};
+  const cudaError_t e = launch(kv_cache_write_int8_kernel_ptr(), dim3(static_cast<unsigned>(blocks)), dim3(256),
+                               0, static_cast<cudaStream_t>(stream), args);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return PKV_ERR_CUDA;
+  }
+  return PKV_OK;
 }
 
 }  // extern "C"

@@ -19,7 +19,10 @@
 //                        WB-th block. Per block: S^T = K Q^T and O^T += V^T P^T on
 //                        tensor cores (mma.sync m16n8k16, fp32 accumulate), online
 //                        softmax in base 2 with quad shuffles. E5M2 tiles are
-//                        widened to fp16 in registers (byte << 8 is exact).
+//                        widened to fp16 in registers (byte << 8 is exact);
+//                        INT8 tiles too (0x64 | (b ^ 0x80) is 1024 + 128 + b,
+//                        minus 1152 is b, exactly), with each token's K scale
+//                        applied to its scores and its V scale folded into P.
 //   Block i of the CTA goes to ring stage i mod STAGES and to block-stream
 //   i mod WB; STAGES is a multiple of WB, so each stage has a single consumer
 //   stream and every wait on its mbarrier is for the next phase in order.
@@ -67,6 +70,28 @@ __device__ __forceinline__ uint32_t swz(uint32_t off) {
   }
 }
 
+// Two bytes of a tile register as an fp16 pair: E5M2 (the byte is the fp16
+// pattern's top byte) or INT8 (r holds the bytes XOR 0x80: 0x64 | u is the
+// fp16 value 1024 + u, and 1024 + u - 1152 is the signed code). sel_e5m2
+// places the two chosen bytes as fp16 high bytes; sel_i8 picks the same two.
+template <int KV>
+__device__ __forceinline__ uint32_t widen_pair(uint32_t r, uint32_t sel_e5m2, uint32_t sel_i8) {
+  if constexpr (KV == kKvInt8) {
+    return sub_f16x2(__byte_perm(r, 0x64646464u, sel_i8), 0x64806480u);
+  } else {
+    return __byte_perm(r, 0, sel_e5m2);
+  }
+}
+
+template <int KV>
+__device__ __forceinline__ uint32_t byte_bias(uint32_t r) {
+  if constexpr (KV == kKvInt8) {
+    return r ^ 0x80808080u;
+  } else {
+    return r;
+  }
+}
+
 template <int KV>
 __device__ __forceinline__ void mma_kv(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                        uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -86,7 +111,8 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
   constexpr int TILE = tile_bytes(KV, D);     // bytes of one (block, head) tile
   constexpr int KS = D / 16;                  // k-steps of S^T = K Q^T
   constexpr int MT = D / 16;                  // m-tiles of O^T = V^T P^T
-  constexpr bool kFp8 = (KV == kKvE5m2);
+  constexpr bool kFp8 = (KV == kKvE5m2 || KV == kKvInt8);   // one byte per element
+  constexpr bool kInt8 = (KV == kKvInt8);
   constexpr int QS = D * 2 + 16;              // query row stride in shared memory (bytes)
   constexpr float kNegInf = -INFINITY;
 
@@ -187,7 +213,16 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
               const int row = bad ? total_rows : (blk * Hkv + h) * kBlockSize;
               const uint32_t full = bars + 8 * stage;
               const uint32_t kdst = ring + stage * 2 * TILE;
-              mbar_arrive_expect_tx(full, 2 * TILE);
+              mbar_arrive_expect_tx(full, 2 * TILE + ((kInt8 && !bad) ? 128 : 0));
+              if constexpr (kInt8) {
+                // The block's 16 K and 16 V row scales (a bad block id reads none).
+                if (!bad) {
+                  const size_t srow = (static_cast<size_t>(blk) * Hkv + h) * kBlockSize;
+                  const uint32_t sdst = smem_addr(smem + lay.scales + stage * 128);
+                  bulk_load(sdst, a.k_scale + srow, 64, full);
+                  bulk_load(sdst + 64, a.v_scale + srow, 64, full);
+                }
+              }
               if constexpr (RB == 256) {
                 // Two 2-D maps per cache, one per 128-byte half of a token row.
                 tma_load_2d(kdst, &tm_k, 0, row, full, pol);
@@ -374,11 +409,12 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
               const int ch = 2 * kp + (mi >> 1);
               uint32_t r0, r1, r2, r3;
               ldsm_x4(kt + swz<RB>(tile_off<RB>(tok, ch)), r0, r1, r2, r3);
-              // E5M2 byte b is the fp16 pattern b << 8: widen with byte permutes.
-              const uint32_t k0 = __byte_perm(r0, 0, 0x1404), k2 = __byte_perm(r0, 0, 0x3424);
-              const uint32_t k1 = __byte_perm(r1, 0, 0x1404), k3 = __byte_perm(r1, 0, 0x3424);
-              const uint32_t k4 = __byte_perm(r2, 0, 0x1404), k6 = __byte_perm(r2, 0, 0x3424);
-              const uint32_t k5 = __byte_perm(r3, 0, 0x1404), k7 = __byte_perm(r3, 0, 0x3424);
+              // Widen bytes (0,1) and (2,3) of each register to fp16 pairs.
+              r0 = byte_bias<KV>(r0); r1 = byte_bias<KV>(r1); r2 = byte_bias<KV>(r2); r3 = byte_bias<KV>(r3);
+              const uint32_t k0 = widen_pair<KV>(r0, 0x1404, 0x4140), k2 = widen_pair<KV>(r0, 0x3424, 0x4342);
+              const uint32_t k1 = widen_pair<KV>(r1, 0x1404, 0x4140), k3 = widen_pair<KV>(r1, 0x3424, 0x4342);
+              const uint32_t k4 = widen_pair<KV>(r2, 0x1404, 0x4140), k6 = widen_pair<KV>(r2, 0x3424, 0x4342);
+              const uint32_t k5 = widen_pair<KV>(r3, 0x1404, 0x4140), k7 = widen_pair<KV>(r3, 0x3424, 0x4342);
 #pragma unroll
               for (int nt = 0; nt < NTW; ++nt) {
                 mma_f16(sa[0][nt], k0, k1, k2, k3, qf[nt][2 * kp][0], qf[nt][2 * kp][1]);
@@ -391,6 +427,17 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
         // ---- online softmax (base 2) over this block ----
         const bool masked = tok0 + (kBlockSize - 1) >= cb;
         const int p_lo = tok0 + g8, p_hi = p_lo + 8;
+        // INT8: this lane's tokens g8 and g8+8 of the block. Their K scales
+        // scale the scores; their V scales are folded into P (0 past the context,
+        // where the stage may hold stale scales); the sums use the unscaled P.
+        float sk_lo = a.scale_log2, sk_hi = a.scale_log2, sv_lo = 1.f, sv_hi = 1.f;
+        if constexpr (kInt8) {
+          const float* sc = reinterpret_cast<const float*>(smem + lay.scales + stage * 128);
+          sk_lo *= sc[g8];
+          sk_hi *= sc[g8 + 8];
+          sv_lo = p_lo < ctx_eff ? sc[16 + g8] : 0.f;
+          sv_hi = p_hi < ctx_eff ? sc[16 + g8 + 8] : 0.f;
+        }
         uint32_t pb[NTW][2];
         uint32_t pb_lo[NTW][2];   // bf16 only: P - bf16(P), a second bf16 term
         float alpha[NTW][2];
@@ -399,8 +446,8 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
           float pv[4];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            float x_lo = (sa[0][nt][e] + sa[1][nt][e]) * a.scale_log2;
-            float x_hi = (sa[0][nt][2 + e] + sa[1][nt][2 + e]) * a.scale_log2;
+            float x_lo = (sa[0][nt][e] + sa[1][nt][e]) * sk_lo;
+            float x_hi = (sa[0][nt][2 + e] + sa[1][nt][2 + e]) * sk_hi;
             if (masked) {
               const bool v_lo = p_lo < cb || (p_lo < ctx_eff && p_lo - cb < 64 &&
                                                ((vis[nt][e] >> (p_lo - cb)) & 1ull));
@@ -424,8 +471,8 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
           // P^T fragments: the S^T accumulator layout (token g, rows 2c..2c+1) is an
           // 8x8 b16 tile per 8 tokens; transposing it gives (row g, tokens 2c..2c+1),
           // which is exactly the B operand of O^T += V^T P^T.
-          const uint32_t h01 = pack_p<KV>(pv[0], pv[1]);
-          const uint32_t h23 = pack_p<KV>(pv[2], pv[3]);
+          const uint32_t h01 = pack_p<KV>(pv[0] * sv_lo, pv[1] * sv_lo);
+          const uint32_t h23 = pack_p<KV>(pv[2] * sv_hi, pv[3] * sv_hi);
           pb[nt][0] = movmatrix_t(h01);
           pb[nt][1] = movmatrix_t(h23);
           if constexpr (KV == kKvBf16) {
@@ -482,10 +529,11 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
               ldsm_x4_t(vt + swz<RB>(tile_off<RB>(tok, ch)), r0, r1, r2, r3);
               // Transposed load of byte pairs: register = {V[2c][2g], V[2c][2g+1],
               // V[2c+1][2g], V[2c+1][2g+1]}; m-row g <-> d 2g, m-row g+8 <-> d 2g+1.
-              const uint32_t v0 = __byte_perm(r0, 0, 0x2404), v1 = __byte_perm(r0, 0, 0x3414);
-              const uint32_t v2 = __byte_perm(r1, 0, 0x2404), v3 = __byte_perm(r1, 0, 0x3414);
-              const uint32_t v4 = __byte_perm(r2, 0, 0x2404), v5 = __byte_perm(r2, 0, 0x3414);
-              const uint32_t v6 = __byte_perm(r3, 0, 0x2404), v7 = __byte_perm(r3, 0, 0x3414);
+              r0 = byte_bias<KV>(r0); r1 = byte_bias<KV>(r1); r2 = byte_bias<KV>(r2); r3 = byte_bias<KV>(r3);
+              const uint32_t v0 = widen_pair<KV>(r0, 0x2404, 0x4240), v1 = widen_pair<KV>(r0, 0x3414, 0x4341);
+              const uint32_t v2 = widen_pair<KV>(r1, 0x2404, 0x4240), v3 = widen_pair<KV>(r1, 0x3414, 0x4341);
+              const uint32_t v4 = widen_pair<KV>(r2, 0x2404, 0x4240), v5 = widen_pair<KV>(r2, 0x3414, 0x4341);
+              const uint32_t v6 = widen_pair<KV>(r3, 0x2404, 0x4240), v7 = widen_pair<KV>(r3, 0x3414, 0x4341);
 #pragma unroll
               for (int nt = 0; nt < NTW; ++nt) {
                 mma_f16(o_acc[2 * mp][nt], v0, v1, v2, v3, pb[nt][0], pb[nt][1]);

@@ -5,6 +5,7 @@
 // One thread moves one 16-byte chunk (8 elements) of one token's key or value
 // row; consecutive threads cover consecutive chunks of a row, so both the read
 // of key/value and the write of the cache row are coalesced.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "pkv_internal.h"
@@ -66,5 +67,69 @@ __global__ void __launch_bounds__(256) kv_cache_write_kernel(const CacheWriteArg
 }
 
 const void* kv_cache_write_kernel_ptr() { return reinterpret_cast<const void*>(&kv_cache_write_kernel); }
+
+// INT8 cache write (the "KV Cache INT8 量化" the inference-framework survey lists
+// for LMDeploy; the codec is ours): one warp quantises one (token, head) row of
+// K or V. scale = max|x| / 127 and code = round-half-even(x / scale) clamped to
+// [-127, 127]; both divisions are IEEE fp32 (__fdiv_rn), so the codes do not
+// depend on compiler flags. An all-zero row gets scale 0 and codes 0.
+__global__ void __launch_bounds__(256) kv_cache_write_int8_kernel(const CacheWriteArgs a) {
+  pdl_wait_prior_grid();
+  const int lane = threadIdx.x & 31;
+  const int per_lane = a.head_size / 32;   // 4 (head 128) or 2 (head 64) elements
+  const long long rows = 2ll * a.num_tokens * a.num_kv_heads;
+  const long long warp0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  for (long long w = warp0; w < rows; w += nwarps) {
+    const bool is_v = w >= static_cast<long long>(a.num_tokens) * a.num_kv_heads;
+    const long long th = is_v ? w - static_cast<long long>(a.num_tokens) * a.num_kv_heads : w;
+    const int t = static_cast<int>(th / a.num_kv_heads), h = static_cast<int>(th - static_cast<long long>(t) * a.num_kv_heads);
+    const long long slot = a.slot_mapping[t];
+    if (slot == -1) continue;
+    if (slot < 0 || slot >= a.num_slots) {
+      if (lane == 0 && !is_v && a.status) atomicOr(a.status, kDevBadSlot);
+      continue;
+    }
+    const __half* src = reinterpret_cast<const __half*>(is_v ? a.value : a.key) + th * a.head_size + lane * per_lane;
+    float x[4] = {0.f, 0.f, 0.f, 0.f};
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (i < per_lane) {
+        x[i] = __half2float(src[i]);
+        amax = fmaxf(amax, fabsf(x[i]));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float scale = __fdiv_rn(amax, 127.0f);
+    uint32_t packed = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (i >= per_lane) break;
+      float qv = 0.f;
+      if (scale != 0.f) {
+        qv = rintf(__fdiv_rn(x[i], scale));
+        qv = fmaxf(qv, -127.0f);
+        qv = fminf(qv, 127.0f);
+      }
+      packed |= (static_cast<uint32_t>(static_cast<int>(qv)) & 0xFFu) << (8 * i);
+    }
+    const long long blk = slot / kBlockSize, off = slot - blk * kBlockSize;
+    const long long row = (blk * a.num_kv_heads + h) * kBlockSize + off;
+    int8_t* dst = static_cast<int8_t*>(is_v ? a.v_cache : a.k_cache) + row * a.head_size + lane * per_lane;
+    if (per_lane == 4) {
+      *reinterpret_cast<uint32_t*>(dst) = packed;
+    } else {
+      *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(packed);
+    }
+    if (lane == 0) (is_v ? a.v_scale : a.k_scale)[row] = scale;
+  }
+  pdl_launch_dependents();
+}
+
+const void* kv_cache_write_int8_kernel_ptr() {
+  return reinterpret_cast<const void*>(&kv_cache_write_int8_kernel);
+}
 
 }  // namespace pkv

@@ -11,7 +11,7 @@ namespace pkv {
 constexpr int kBlockSize = 16;       // tokens per KV block
 constexpr int kMaxRows = 64;         // GQA group size x query tokens handled per CTA
 constexpr int kMaxCtasPerSm = 8;     // upper bound on resident decode CTAs per SM
-constexpr int kKvF16 = 0, kKvBf16 = 1, kKvE5m2 = 2;
+constexpr int kKvF16 = 0, kKvBf16 = 1, kKvE5m2 = 2, kKvInt8 = 3;
 
 // Device-status bits (mirror the public PKV_DEV_* values).
 constexpr int32_t kDevBadSlot = 0x1;
@@ -27,6 +27,8 @@ struct DecodeArgs {
   const int32_t* context_lens; // [S]
   const int32_t* cu_q_lens;    // [S+1] query-token offsets, or null: q_per_seq tokens each
   const unsigned long long* tree_masks;  // [rows] draft tokens visible to each query token, or null: causal
+  const float* k_scale;        // INT8 cache: [num_blocks][Hkv][16] per-row scales, else null
+  const float* v_scale;
   float* partials;             // split-KV partial slots
   unsigned long long* piece_counts;  // [S*Hkv]: (call epoch << 32) | pieces finished
   int32_t* status;             // optional device status word
@@ -60,7 +62,7 @@ struct DecodeGeometry {
 };
 
 // Sizes derived from (kv dtype, head size).
-__host__ __device__ constexpr int kv_elem_bytes(int kv) { return kv == kKvE5m2 ? 1 : 2; }
+__host__ __device__ constexpr int kv_elem_bytes(int kv) { return (kv == kKvE5m2 || kv == kKvInt8) ? 1 : 2; }
 __host__ __device__ constexpr int tile_row_bytes(int kv, int d) { return d * kv_elem_bytes(kv); }
 __host__ __device__ constexpr int tile_bytes(int kv, int d) { return kBlockSize * tile_row_bytes(kv, d); }
 
@@ -71,8 +73,9 @@ __host__ __device__ constexpr int partial_slot_floats(int rows, int d) {
 }
 
 // Shared-memory layout of the decode kernel, relative to a 1024-aligned base.
+// An INT8 cache adds, per ring stage, the 16 K and 16 V row scales (128 bytes).
 struct DecodeSmem {
-  size_t ring, bars, qs, mrg_o, mrg_ml, misc, total;
+  size_t ring, scales, bars, qs, mrg_o, mrg_ml, misc, total;
 };
 // The merge buffers hold only the unit's real rows (rows <= 8*ntw*wr).
 __host__ __device__ inline DecodeSmem decode_smem_layout(int kv, int d, int ntw, int wr, int wb,
@@ -80,7 +83,8 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int kv, int d, int ntw,
   DecodeSmem s{};
   const int rows_pad = 8 * ntw * wr;
   s.ring = 0;
-  s.bars = s.ring + (size_t)stages * 2 * tile_bytes(kv, d);
+  s.scales = s.ring + (size_t)stages * 2 * tile_bytes(kv, d);
+  s.bars = s.scales + (kv == kKvInt8 ? (size_t)stages * 128 : 0);
   s.qs = s.bars + (size_t)stages * 2 * 8;
   s.qs = (s.qs + 15) & ~(size_t)15;
   s.mrg_o = s.qs + (size_t)rows_pad * (d * 2 + 16);
@@ -127,7 +131,9 @@ const void* decode_tc_kernel_ptr(int kv, int rc);
 const void* decode_kernel_ptr_f16(int d, int ntw);
 const void* decode_kernel_ptr_bf16(int d, int ntw);
 const void* decode_kernel_ptr_e5m2(int d, int ntw);
+const void* decode_kernel_ptr_int8(int d, int ntw);
 const void* kv_cache_write_kernel_ptr();
+const void* kv_cache_write_int8_kernel_ptr();
 
 struct CacheWriteArgs {
   const uint4* key;            // [T][Hkv][D] 16-bit elements, 8 per uint4
@@ -140,7 +146,9 @@ struct CacheWriteArgs {
   int32_t num_tokens;
   int32_t num_kv_heads;
   int32_t head_size;
-  int32_t kv;                  // kKvF16 / kKvBf16 / kKvE5m2
+  int32_t kv;                  // kKvF16 / kKvBf16 / kKvE5m2 / kKvInt8
+  float* k_scale;              // INT8 cache: [num_blocks][num_kv_heads][16] row scales
+  float* v_scale;
 };
 
 }  // namespace pkv

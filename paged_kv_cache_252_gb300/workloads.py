@@ -25,7 +25,7 @@ import torch
 
 BLOCK_SIZE = 16
 
-KV_DTYPES = ("fp16", "bf16", "e5m2")
+KV_DTYPES = ("fp16", "bf16", "e5m2", "int8")
 
 
 @dataclass
@@ -61,7 +61,13 @@ class Workload:
 
     @property
     def kv_elem_bytes(self) -> int:
-        return 1 if self.kv_dtype == "e5m2" else 2
+        return 1 if self.kv_dtype in ("e5m2", "int8") else 2
+
+    @property
+    def kv_row_extra_bytes(self) -> int:
+        """Bytes stored per (token, KV head) row besides the elements: the INT8
+        cache's float32 row scale."""
+        return 4 if self.kv_dtype == "int8" else 0
 
     @property
     def max_blocks_per_seq(self) -> int:
@@ -117,8 +123,10 @@ class Workload:
         return np.concatenate(idx).astype(np.int64)
 
     def kv_bytes_read(self) -> int:
-        """Algorithmic KV bytes one decode call must read (K and V of every visible token)."""
-        return int(self.num_tokens_total * self.num_kv_heads * self.head_size * 2 * self.kv_elem_bytes)
+        """Algorithmic KV bytes one decode call must read (K and V of every visible token,
+        and an INT8 cache's row scales)."""
+        row = self.head_size * self.kv_elem_bytes + self.kv_row_extra_bytes
+        return int(self.num_tokens_total * self.num_kv_heads * row * 2)
 
     def q_out_bytes(self) -> int:
         return int(2 * self.num_new_tokens * self.num_q_heads * self.head_size * 2)
@@ -127,7 +135,7 @@ class Workload:
         """Algorithmic bytes of the per-step cache write (read new K/V, write cache slots)."""
         t = self.num_new_tokens
         src = t * self.num_kv_heads * self.head_size * 2 * 2
-        dst = t * self.num_kv_heads * self.head_size * 2 * self.kv_elem_bytes
+        dst = t * self.num_kv_heads * (self.head_size * self.kv_elem_bytes + self.kv_row_extra_bytes) * 2
         return int(src + dst + 4 * t)
 
     def describe(self) -> dict:
@@ -224,6 +232,16 @@ def llama3_8b_bs256_e5m2(num_seqs: int = 256) -> Workload:
                          context_lens=_uniform_lens(seed, num_seqs, 1024, 4096))
 
 
+def llama3_8b_bs256_int8(num_seqs: int = 256) -> Workload:
+    """The 8B fp8 workload with an INT8 KV cache (per-row float32 scales): 256
+    sequences, lengths uniform in [1024, 4096], fp16 queries and output."""
+    seed = 259
+    return make_workload("llama3_8b_decode_bs256_int8", num_seqs=num_seqs, num_q_heads=32,
+                         num_kv_heads=8, head_size=128, q_per_seq=1, kv_dtype="int8",
+                         scale=1.0 / math.sqrt(128), seed=seed,
+                         context_lens=_uniform_lens(seed, num_seqs, 1024, 4096))
+
+
 def long_bs8_bf16(num_seqs: int = 8, lo: int = 32768, hi: int = 131072) -> Workload:
     """Long-context split-KV decode: 8 sequences, 32 q / 8 KV heads, head 128,
     bf16 KV, lengths uniform in [32768, 131072], fully shuffled blocks."""
@@ -262,6 +280,7 @@ NAMED = {
     "tiny": tiny,
     "8b": llama3_8b_bs64_fp16,
     "8b_fp8": llama3_8b_bs256_e5m2,
+    "8b_int8": llama3_8b_bs256_int8,
     "long": long_bs8_bf16,
     "70b_spec": llama3_70b_spec4_e5m2,
     "mixed": mixed_8b_decode_verify,

@@ -460,3 +460,81 @@ def test_random_tree_masks_are_ancestor_closed():
                 if (m[i] >> a) & 1:
                     assert m[a] & m[i] == m[a]     # every ancestor's ancestors are visible too
         off += n
+
+
+# ---------------------------------------------------------------------------------
+# INT8 KV cache (symmetric codes per (token, KV head) row, float32 row scales)
+# ---------------------------------------------------------------------------------
+
+def _int8_rows(orc, x16):
+    """Quantise fp16 rows x16 [T, Hkv, D] with the oracle's INT8 cache write into
+    slots 0..T-1; returns codes [T, Hkv, D] and scales [T, Hkv]."""
+    T, Hkv, D = x16.shape
+    nb = (T + 15) // 16
+    kc = np.zeros((nb, Hkv, 16, D), np.int8)
+    vc = np.zeros_like(kc)
+    ks = np.zeros((nb, Hkv, 16), np.float32)
+    vs = np.zeros_like(ks)
+    assert orc.kv_cache_write_int8(x16.view(np.uint16), x16.view(np.uint16), np.arange(T, dtype=np.int32),
+                                   kc, vc, ks, vs) == 0
+    codes = kc.transpose(0, 2, 1, 3).reshape(nb * 16, Hkv, D)[:T]
+    scales = ks.transpose(0, 2, 1).reshape(nb * 16, Hkv)[:T]
+    assert np.array_equal(codes, vc.transpose(0, 2, 1, 3).reshape(nb * 16, Hkv, D)[:T])
+    return codes, scales
+
+
+def test_int8_codes_are_nearest_and_span_the_row(orc):
+    rng = np.random.default_rng(41)
+    x = (rng.standard_normal((40, 3, 64)) * rng.choice([1e-3, 1.0, 300.0], size=(40, 3, 1))).astype(np.float16)
+    x[5, 1] = 0.0                                          # an all-zero row
+    x[7, 2, 3] = np.float16(-60000.0)                      # one element dominates its row
+    codes, scales = _int8_rows(orc, x)
+    xf = x.astype(np.float64)
+    amax = np.abs(xf).max(axis=2)
+    # the scale is max|x| / 127 rounded to float32
+    np.testing.assert_array_equal(scales, (amax.astype(np.float32) / np.float32(127.0)).astype(np.float32))
+    nz = scales > 0
+    ratio = xf / np.where(nz, scales, 1.0)[..., None]
+    # each code is the integer nearest x / scale (within the float32 rounding of the ratio)
+    assert np.all(np.abs(ratio - codes)[nz] <= 0.5 + 1e-5)
+    assert np.all(np.abs(codes) <= 127)
+    # the row's largest magnitude maps to +-127, with the element's sign
+    i = np.abs(xf).argmax(axis=2)
+    top = np.take_along_axis(codes, i[..., None], axis=2)[..., 0]
+    sgn = np.sign(np.take_along_axis(xf, i[..., None], axis=2)[..., 0])
+    assert np.array_equal(top[nz], (127 * sgn[nz]).astype(np.int8))
+    # zero rows: scale 0 and codes 0
+    assert scales[5, 1] == 0 and not codes[5, 1].any()
+    # reconstruction error is at most half a step
+    assert np.all(np.abs(xf - codes * scales[..., None].astype(np.float64)) <= 0.5 * scales[..., None] * (1 + 1e-5))
+
+
+def test_int8_attention_matches_sdpa_on_the_dequantised_cache(orc):
+    w = wl.custom(num_seqs=4, num_q_heads=8, num_kv_heads=2, head_size=64, q_per_seq=2, kv_dtype="int8",
+                  context_lens=[2, 17, 40, 77], seed=42)
+    vals = wl.token_values(w)
+    k_all, v_all = bits16(vals["k_all"]), bits16(vals["v_all"])
+    slots = vals["slot_all"].numpy().astype(np.int32)
+    kc = np.zeros(cache_shape(w), np.int8)
+    vc = np.zeros_like(kc)
+    ks = np.zeros(cache_shape(w)[:3], np.float32)
+    vs = np.zeros_like(ks)
+    assert orc.kv_cache_write_int8(k_all, v_all, slots, kc, vc, ks, vs) == 0
+    out, _, rc = orc.paged_attention(bits16(vals["q"]), 0, w.q_per_seq, kc, vc, 3, w.block_tables,
+                                     w.context_lens, w.scale, k_scale=ks, v_scale=vs)
+    assert rc == 0
+    n, G = w.q_per_seq, w.group
+    for s in range(w.num_seqs):
+        ctx = int(w.context_lens[s])
+        p = np.arange(ctx)
+        blk = w.block_tables[s][p // 16]
+        off = p % 16
+        k = torch.from_numpy(kc[blk, :, off, :].astype(np.float64) * ks[blk, :, off][..., None])  # [ctx, Hkv, D]
+        v = torch.from_numpy(vc[blk, :, off, :].astype(np.float64) * vs[blk, :, off][..., None])
+        q = vals["q"][s * n:(s + 1) * n].to(torch.float64)
+        kk = k.repeat_interleave(G, dim=1).permute(1, 0, 2)[None]
+        vv = v.repeat_interleave(G, dim=1).permute(1, 0, 2)[None]
+        mask = torch.arange(ctx)[None, :] <= (ctx - n + torch.arange(n))[:, None]
+        ref = torch.nn.functional.scaled_dot_product_attention(q.permute(1, 0, 2)[None], kk, vv,
+                                                               attn_mask=mask, scale=w.scale)
+        np.testing.assert_allclose(out[s * n:(s + 1) * n], ref[0].permute(1, 0, 2).numpy(), rtol=1e-10, atol=1e-12)
