@@ -152,6 +152,51 @@ def _desc(cache: torch.Tensor) -> _CacheDesc:
     return _CacheDesc(cache.shape[0], cache.shape[2], cache.shape[1], cache.shape[3])
 
 
+def _pair(k_cache, v_cache) -> _CacheDesc:
+    d = _desc(k_cache)
+    if tuple(v_cache.shape) != tuple(k_cache.shape) or v_cache.dtype != k_cache.dtype:
+        raise PagedKVError("k_cache and v_cache must have the same shape and dtype")
+    return d
+
+
+def _decode_shapes(out, q, k_cache, v_cache, block_tables, context_lens, rows=None, max_rows=None):
+    """The library sees only pointers: check here that every tensor is as large as
+    the call will read or write. Returns (cache descriptor, num_seqs)."""
+    d = _pair(k_cache, v_cache)
+    if q.dim() != 3 or tuple(out.shape) != tuple(q.shape):
+        raise PagedKVError(f"q and out must both be [rows, num_q_heads, head_size], got "
+                           f"{tuple(q.shape)} and {tuple(out.shape)}")
+    if int(q.shape[2]) != int(k_cache.shape[3]):
+        raise PagedKVError(f"query head size {int(q.shape[2])} != cache head size {int(k_cache.shape[3])}")
+    if context_lens.dim() != 1:
+        raise PagedKVError("context_lens must be 1-D [num_seqs]")
+    S = int(context_lens.shape[0])
+    if block_tables.dim() != 2 or int(block_tables.shape[0]) < S:
+        raise PagedKVError(f"block_tables must be [num_seqs, max_blocks_per_seq], got {tuple(block_tables.shape)}")
+    if rows is not None and int(q.shape[0]) != rows:
+        raise PagedKVError(f"q must have num_seqs * q_per_seq = {rows} rows, got {int(q.shape[0])}")
+    if max_rows is not None and not (S <= int(q.shape[0]) <= max_rows):
+        raise PagedKVError(f"q must have between num_seqs and num_seqs * max_q_per_seq rows, got {int(q.shape[0])}")
+    return d, S
+
+
+def _scales_shape(k_cache, k_scale, v_scale):
+    want = tuple(k_cache.shape[:3])
+    if tuple(k_scale.shape) != want or tuple(v_scale.shape) != want:
+        raise PagedKVError(f"k_scale and v_scale must be float32 {want}")
+
+
+def _write_shapes(key, value, slot_mapping, k_cache, v_cache) -> _CacheDesc:
+    d = _pair(k_cache, v_cache)
+    want = (int(k_cache.shape[1]), int(k_cache.shape[3]))
+    if key.dim() != 3 or tuple(value.shape) != tuple(key.shape) or tuple(key.shape[1:]) != want:
+        raise PagedKVError(f"key and value must both be [T, {want[0]}, {want[1]}], got "
+                           f"{tuple(key.shape)} and {tuple(value.shape)}")
+    if slot_mapping.dim() != 1 or int(slot_mapping.shape[0]) != int(key.shape[0]):
+        raise PagedKVError("slot_mapping must be 1-D with one slot per token")
+    return d
+
+
 def _need_cuda_contig(name, t):
     if not t.is_cuda:
         raise PagedKVError(f"{name} must be a CUDA tensor")
@@ -186,7 +231,8 @@ def kv_cache_write_int8(key, value, slot_mapping, k_cache, v_cache, k_scale, v_s
         raise PagedKVError("INT8 cache write takes fp16 key/value, int8 caches, float32 scales")
     if slot_mapping.dtype != torch.int32:
         raise PagedKVError("slot_mapping must be int32")
-    d = _desc(k_cache)
+    d = _write_shapes(key, value, slot_mapping, k_cache, v_cache)
+    _scales_shape(k_cache, k_scale, v_scale)
     rc = load_library().pkv_kv_cache_write_int8(
         _ptr(key), _ptr(value), int(key.shape[0]), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
         _ptr(k_scale), _ptr(v_scale), ctypes.byref(d), _ptr(device_status), _stream_handle(stream, key.device))
@@ -202,9 +248,10 @@ def paged_attention_decode_int8(out, q, k_cache, v_cache, k_scale, v_scale, bloc
         _need_cuda_contig(n, t)
     if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
         raise PagedKVError("block_tables and context_lens must be int32")
-    S = int(context_lens.shape[0])
+    d, S = _decode_shapes(out, q, k_cache, v_cache, block_tables, context_lens,
+                          rows=int(context_lens.shape[0]) * int(q_per_seq))
+    _scales_shape(k_cache, k_scale, v_scale)
     Hq = int(q.shape[1])
-    d = _desc(k_cache)
     lib = load_library()
     with torch.cuda.device(q.device):
         need = int(lib.pkv_decode_workspace_bytes(S, Hq, q_per_seq, ctypes.byref(d)))
@@ -227,7 +274,7 @@ def kv_cache_write(key, value, slot_mapping, k_cache, v_cache, kv_dtype=None, *,
         _need_cuda_contig(n, t)
     if slot_mapping.dtype != torch.int32:
         raise PagedKVError("slot_mapping must be int32")
-    d = _desc(k_cache)
+    d = _write_shapes(key, value, slot_mapping, k_cache, v_cache)
     rc = load_library().pkv_kv_cache_write(
         _ptr(key), _ptr(value), _src_code(key), int(key.shape[0]), _ptr(slot_mapping),
         _ptr(k_cache), _ptr(v_cache), _kv_code(kv_dtype, k_cache), ctypes.byref(d),
@@ -263,9 +310,9 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
         raise PagedKVError("block_tables and context_lens must be int32")
     if out.dtype != q.dtype:
         raise PagedKVError("out and q must share a dtype")
-    S = int(context_lens.shape[0])
+    d, S = _decode_shapes(out, q, k_cache, v_cache, block_tables, context_lens,
+                          rows=int(context_lens.shape[0]) * int(q_per_seq))
     Hq = int(q.shape[1])
-    d = _desc(k_cache)
     code = _kv_code(kv_dtype, k_cache)
     lib = load_library()
     with torch.cuda.device(q.device):
@@ -296,7 +343,8 @@ def paged_attention_decode_noalloc(out, q, k_cache, v_cache, block_tables, conte
         raise PagedKVError("block_tables and context_lens must be int32")
     if out.dtype != q.dtype:
         raise PagedKVError("out and q must share a dtype")
-    d = _desc(k_cache)
+    d, _ = _decode_shapes(out, q, k_cache, v_cache, block_tables, context_lens,
+                          rows=int(context_lens.shape[0]) * int(q_per_seq))
     with torch.cuda.device(q.device):
         rc = load_library().pkv_paged_attention_decode_noalloc(
             _ptr(out), _ptr(q), int(context_lens.shape[0]), int(q.shape[1]), int(q_per_seq),
@@ -321,11 +369,11 @@ def paged_attention_decode_varlen(out, q, cu_q_lens, k_cache, v_cache, block_tab
         raise PagedKVError("block_tables, context_lens and cu_q_lens must be int32")
     if out.dtype != q.dtype:
         raise PagedKVError("out and q must share a dtype")
-    S = int(context_lens.shape[0])
-    if int(cu_q_lens.shape[0]) != S + 1:
+    d, S = _decode_shapes(out, q, k_cache, v_cache, block_tables, context_lens,
+                          max_rows=int(context_lens.shape[0]) * int(max_q_per_seq))
+    if cu_q_lens.dim() != 1 or int(cu_q_lens.shape[0]) != S + 1:
         raise PagedKVError("cu_q_lens must have num_seqs + 1 entries")
     Hq = int(q.shape[1])
-    d = _desc(k_cache)
     lib = load_library()
     with torch.cuda.device(q.device):
         need = int(lib.pkv_decode_workspace_bytes(S, Hq, int(max_q_per_seq), ctypes.byref(d)))
@@ -357,9 +405,16 @@ def paged_attention_decode_tree(out, q, tree_masks, k_cache, v_cache, block_tabl
         _need_cuda_contig("cu_q_lens", cu_q_lens)
     if out.dtype != q.dtype:
         raise PagedKVError("out and q must share a dtype")
-    S = int(context_lens.shape[0])
+    S0, n_max = int(context_lens.shape[0]), int(max_q_per_seq)
+    if cu_q_lens is None:
+        d, S = _decode_shapes(out, q, k_cache, v_cache, block_tables, context_lens, rows=S0 * n_max)
+    else:
+        d, S = _decode_shapes(out, q, k_cache, v_cache, block_tables, context_lens, max_rows=S0 * n_max)
+        if cu_q_lens.dim() != 1 or int(cu_q_lens.shape[0]) != S + 1 or cu_q_lens.dtype != torch.int32:
+            raise PagedKVError("cu_q_lens must be int32 with num_seqs + 1 entries")
+    if tree_masks.dim() != 1 or int(tree_masks.shape[0]) != int(q.shape[0]):
+        raise PagedKVError("tree_masks must hold one mask per query row")
     Hq = int(q.shape[1])
-    d = _desc(k_cache)
     lib = load_library()
     with torch.cuda.device(q.device):
         need = int(lib.pkv_decode_workspace_bytes(S, Hq, int(max_q_per_seq), ctypes.byref(d)))
@@ -470,7 +525,7 @@ def copy_blocks(k_cache, v_cache, src, dst, kv_dtype=None, *, device_status=None
         _need_cuda_contig(n_, t)
     if src.dtype != torch.int32 or dst.dtype != torch.int32 or src.numel() != dst.numel():
         raise PagedKVError("src and dst must be int32 tensors of equal length")
-    d = _desc(k_cache)
+    d = _pair(k_cache, v_cache)
     rc = load_library().pkv_copy_blocks(_ptr(k_cache), _ptr(v_cache), _kv_code(kv_dtype, k_cache),
                                         ctypes.byref(d), _ptr(src), _ptr(dst), int(src.numel()),
                                         _ptr(device_status), _stream_handle(stream, k_cache.device))

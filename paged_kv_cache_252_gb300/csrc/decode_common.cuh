@@ -122,10 +122,12 @@ __device__ inline void finish_split_piece(const DecodeArgs& a, int u, long long 
   constexpr float kNegInf = -INFINITY;
   const int R = a.rows, G = a.group, Hq = a.num_q_heads;
   // The barrier orders every thread's slot writes before thread 0's device-scope
-  // fence, which makes them visible before the counter update.
+  // release fence, which makes them visible before the counter update; the CTA
+  // that sees the final count acquires the other CTAs' slots through the same
+  // fence after its atomic.
   named_bar_sync(bar_id, nthr);
   if (tid == 0) {
-    __threadfence();
+    fence_acq_rel_gpu();
     const long long nact = ncta < total ? ncta : total;
     const int c_first = static_cast<int>(((ustart + 1) * nact - 1) / total);
     const int c_last = static_cast<int>(((ustart + nb) * nact - 1) / total);
@@ -140,37 +142,53 @@ __device__ inline void finish_split_piece(const DecodeArgs& a, int u, long long 
       if (prev == cur) break;
       cur = prev;
     }
-    fin[0] = (static_cast<int>(want & 0xffffffffull) == c_last - c_first + 1) ? 1 : 0;
+    const bool last = static_cast<int>(want & 0xffffffffull) == c_last - c_first + 1;
+    fin[0] = last ? 1 : 0;
     fin[1] = c_first;
     fin[2] = c_last;
-    __threadfence();
+    if (last) fence_acq_rel_gpu();   // acquire: the other CTAs' slots are read next
   }
   named_bar_sync(bar_id, nthr);
   if (!fin[0]) return;
+  // Merge: out = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c with M = max_c m_c,
+  // accumulated online (the running max moves as slots are read). A thread reads
+  // four slots per step, so their loads are in flight together instead of one
+  // round trip per slot.
   const int c_first = fin[1], c_last = fin[2];
   const int ooff = partial_o_offset(R);
+  const float* base = a.partials + static_cast<size_t>(u) * a.slot_floats;   // slot of CTA c: + c * slot_floats
 #pragma unroll 1
   for (int idx = tid; idx < Rs * (D / 4); idx += nthr) {
     const int r = idx / (D / 4), d4 = idx - (idx / (D / 4)) * (D / 4);
-    float M = kNegInf;
-#pragma unroll 1
-    for (int c = c_first; c <= c_last; ++c)
-      M = fmaxf(M, __ldcg(a.partials + static_cast<size_t>(u + c) * a.slot_floats + r));
-    const float Mu = (M == kNegInf) ? 0.f : M;
-    float lsum = 0.f;
+    float M = kNegInf, L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
-    for (int c = c_first; c <= c_last; ++c) {
-      const float* P = a.partials + static_cast<size_t>(u + c) * a.slot_floats;
-      const float f = fast_exp2(__ldcg(P + r) - Mu);
-      lsum += f * __ldcg(P + R + r);
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(P + ooff + r * D + d4 * 4));
-      acc.x += f * v.x;
-      acc.y += f * v.y;
-      acc.z += f * v.z;
-      acc.w += f * v.w;
+    for (int c0 = c_first; c0 <= c_last; c0 += 4) {
+      float mc[4], lc[4];
+      float4 oc[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const bool live = c0 + k <= c_last;
+        const float* P = base + static_cast<size_t>(live ? c0 + k : c_first) * a.slot_floats;
+        mc[k] = live ? __ldcg(P + r) : kNegInf;
+        lc[k] = live ? __ldcg(P + R + r) : 0.f;
+        oc[k] = live ? __ldcg(reinterpret_cast<const float4*>(P + ooff + r * D + d4 * 4))
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float Mn = fmaxf(M, mc[k]);
+        const float Mu = (Mn == kNegInf) ? 0.f : Mn;
+        const float fo = fast_exp2(M - Mu), fc = fast_exp2(mc[k] - Mu);
+        L = L * fo + fc * lc[k];
+        acc.x = acc.x * fo + fc * oc[k].x;
+        acc.y = acc.y * fo + fc * oc[k].y;
+        acc.z = acc.z * fo + fc * oc[k].z;
+        acc.w = acc.w * fo + fc * oc[k].w;
+        M = Mn;
+      }
     }
-    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    const float inv = L > 0.f ? 1.f / L : 0.f;
     const int j = r / G, gi = r - j * G;
     const size_t dst = (static_cast<size_t>(qb + j) * Hq + h * G + gi) * D + d4 * 4;
     uint2 pk;

@@ -61,6 +61,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Device-scope acquire-release fence: with a relaxed atomic after it, it publishes
+// this thread's earlier writes (and, after a CTA barrier, the CTA's) to any thread
+// that reads the atomic's result and then runs the same fence.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 // As mbar_try_wait, but a thread whose phase is not complete yet is suspended
 // until it completes or about suspend_ns nanoseconds pass, instead of
 // returning at once: a waiting warp then takes no issue slots.
