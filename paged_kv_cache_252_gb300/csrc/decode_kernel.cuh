@@ -39,6 +39,7 @@
 // hit 8 different bank groups.
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -72,12 +73,15 @@ __device__ __forceinline__ uint32_t swz(uint32_t off) {
 
 // Two bytes of a tile register as an fp16 pair: E5M2 (the byte is the fp16
 // pattern's top byte) or INT8 (r holds the bytes XOR 0x80: 0x64 | u is the
-// fp16 value 1024 + u, and 1024 + u - 1152 is the signed code). sel_e5m2
-// places the two chosen bytes as fp16 high bytes; sel_i8 picks the same two.
+// fp16 value 1024 + u = code + kI8Bias). sel_e5m2 places the two chosen bytes
+// as fp16 high bytes; sel_i8 picks the same two. The INT8 bias is not taken
+// off element by element: q . (c + bias) and sum_t P_t (c_t + bias) are
+// corrected once per row by bias * sum(q) and bias * sum_t P_t.
+constexpr float kI8Bias = 1152.f;
 template <int KV>
 __device__ __forceinline__ uint32_t widen_pair(uint32_t r, uint32_t sel_e5m2, uint32_t sel_i8) {
   if constexpr (KV == kKvInt8) {
-    return sub_f16x2(__byte_perm(r, 0x64646464u, sel_i8), 0x64806480u);
+    return __byte_perm(r, 0x64646464u, sel_i8);
   } else {
     return __byte_perm(r, 0, sel_e5m2);
   }
@@ -328,6 +332,36 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
       }
     }
 
+    // INT8: kI8Bias * sum_d q[r][d] for this lane's rows (the 8 lanes of a row
+    // group each add D/8 dimensions), and the running sum of the P values the
+    // P V product uses, scaled by the V scales (lsv), for the output's bias.
+    float kq[NTW][2], lsv[NTW][2];
+#pragma unroll
+    for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        kq[nt][e] = 0.f;
+        lsv[nt][e] = 0.f;
+        if constexpr (kInt8) {
+          const uint8_t* qr = qs + (row_base + nt * 8 + 2 * c4 + e) * QS + g8 * (D / 4);
+          float acc = 0.f;
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c) {
+            const uint4 v = *reinterpret_cast<const uint4*>(qr + 16 * c);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+              acc += f.x + f.y;
+            }
+          }
+          acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+          acc += __shfl_xor_sync(0xffffffffu, acc, 8);
+          acc += __shfl_xor_sync(0xffffffffu, acc, 16);
+          kq[nt][e] = kI8Bias * acc;
+        }
+      }
+
     float m_run[NTW][2], l_run[NTW][2];
     float o_acc[MT][NTW][4];
     // Visibility of the n_s query (draft) tokens: the context before them,
@@ -446,8 +480,8 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
           float pv[4];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            float x_lo = (sa[0][nt][e] + sa[1][nt][e]) * sk_lo;
-            float x_hi = (sa[0][nt][2 + e] + sa[1][nt][2 + e]) * sk_hi;
+            float x_lo = ((sa[0][nt][e] + sa[1][nt][e]) - kq[nt][e]) * sk_lo;
+            float x_hi = ((sa[0][nt][2 + e] + sa[1][nt][2 + e]) - kq[nt][e]) * sk_hi;
             if (masked) {
               const bool v_lo = p_lo < cb || (p_lo < ctx_eff && p_lo - cb < 64 &&
                                                ((vis[nt][e] >> (p_lo - cb)) & 1ull));
@@ -473,6 +507,12 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
           // which is exactly the B operand of O^T += V^T P^T.
           const uint32_t h01 = pack_p<KV>(pv[0] * sv_lo, pv[1] * sv_lo);
           const uint32_t h23 = pack_p<KV>(pv[2] * sv_hi, pv[3] * sv_hi);
+          if constexpr (kInt8) {
+            const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+            const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+            lsv[nt][0] = lsv[nt][0] * alpha[nt][0] + (f01.x + f23.x);
+            lsv[nt][1] = lsv[nt][1] * alpha[nt][1] + (f01.y + f23.y);
+          }
           pb[nt][0] = movmatrix_t(h01);
           pb[nt][1] = movmatrix_t(h23);
           if constexpr (KV == kKvBf16) {
@@ -549,6 +589,24 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
     i += take;
 
     // ---- merge the WB block streams of this piece ----
+    if constexpr (kInt8) {
+      // Take the INT8 bias off O^T: kI8Bias * (sum over the warp's tokens of the P it used).
+#pragma unroll
+      for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float t = lsv[nt][e];
+          t += __shfl_xor_sync(0xffffffffu, t, 4);
+          t += __shfl_xor_sync(0xffffffffu, t, 8);
+          t += __shfl_xor_sync(0xffffffffu, t, 16);
+          const float b = kI8Bias * t;
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            o_acc[mt][nt][e] -= b;
+            o_acc[mt][nt][2 + e] -= b;
+          }
+        }
+    }
 #pragma unroll
     for (int nt = 0; nt < NTW; ++nt)
 #pragma unroll
