@@ -160,10 +160,25 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def csrc_digest() -> str:
+# Sources that decide the decode launch of a workload: the host side and the
+# shared device code, plus the kernel family that runs it (the tcgen05 kernel
+# for E5M2 head-128 units of more than 16 rows, the mma.sync kernel otherwise).
+_DECODE_COMMON = ["capi.cu", "pkv_internal.h", "pkv_ptx.cuh", "decode_common.cuh"]
+_DECODE_FAMILY = {
+    "tc": ["decode_tc.cu", "decode_tc_kernel.cuh", "pkv_tc.cuh"],
+    "mma": ["decode_kernel.cuh", "decode_f16.cu", "decode_bf16.cu", "decode_e5m2.cu", "decode_int8.cu"],
+}
+
+
+def decode_family(w) -> str:
+    rows = w.q_per_seq * (w.num_q_heads // w.num_kv_heads)
+    return "tc" if (w.kv_dtype == "e5m2" and w.head_size == 128 and rows > 16) else "mma"
+
+
+def csrc_digest(family: str) -> str:
     src = hashlib.sha256()
     d = os.path.join(ROOT, "paged_kv_cache_252_gb300", "csrc")
-    for fn in sorted(os.listdir(d)):
+    for fn in sorted(_DECODE_COMMON + _DECODE_FAMILY[family]):
         with open(os.path.join(d, fn), "rb") as f:
             src.update(fn.encode())
             src.update(f.read())
@@ -172,14 +187,15 @@ def csrc_digest() -> str:
 
 def profiled_traffic(config: str):
     """DRAM bytes per decode launch from a committed ncu summary, if it was taken on
-    the current kernel source (else None)."""
+    the current source of the kernel that runs this workload (else None)."""
+    from paged_kv_cache_252_gb300 import workloads as wl
     path = os.path.join(ROOT, "profiles", "decode_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
     entry = d.get(config)
-    if not entry or entry.get("csrc_sha256") != csrc_digest():
+    if not entry or entry.get("csrc_sha256") != csrc_digest(decode_family(wl.by_name(config))):
         return None
     return float(entry["dram_bytes_per_launch"])
 
