@@ -41,6 +41,17 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 std::atomic<uint32_t> g_call_epoch{0};
 
+// Fixed cost of one unit piece on the work line, in KV blocks: the piece's
+// query load, epilogue and (when split) merge take about as long as streaming
+// this many blocks, so CTAs whose share starts more units get fewer blocks.
+constexpr int kPieceCost2B = 5;   // mma.sync kernel, fp16 / bf16 cache
+constexpr int kPieceCost1B = 4;   // mma.sync kernel, E5M2 / INT8 cache
+constexpr int kPieceCostTc = 24;  // tcgen05 kernel (its epilogue reads O from tensor memory)
+int piece_cost(bool tc, int kv) {
+  if (tc) return kPieceCostTc;
+  return (kv == PKV_FP8_E5M2 || kv == PKV_INT8) ? kPieceCost1B : kPieceCost2B;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
@@ -415,6 +426,7 @@ int decode_impl(void* out, const void* q, const int32_t* cu_q_lens,
   uint32_t ep = ++g_call_epoch;
   if (ep == 0) ep = ++g_call_epoch;
   a.epoch = ep;
+  a.piece_cost = piece_cost(g.tc != 0, kv_dtype);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   void* dargs[5] = {&tmk, &tmv, &tmk1, &tmv1, &a};

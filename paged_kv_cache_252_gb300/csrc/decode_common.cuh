@@ -55,12 +55,31 @@ __device__ __forceinline__ uint32_t pack_p(float lo, float hi) {
   }
 }
 
-// This CTA's share [b0, b1) of all (sequence, head, block) triples. Every thread
-// of the CTA calls it. One pass over context_lens: thread t owns a contiguous run
-// of sequences, a block-wide scan of the runs' block counts gives the total and
-// every run's offset, and the thread whose run holds block b0 finds its sequence.
-// Results in plan[0..4] = total, b0, b1, first sequence s0, and the number of
-// blocks per head of the sequences before s0 (plan[3] = -1 if the share is empty).
+// The work is a line of positions: unit (s, h) in order, each a fixed
+// a.piece_cost positions (its per-piece work: queries, epilogue, split merge,
+// counted in blocks) followed by one position per KV block. CTAs take equal
+// shares of the line, so a CTA whose share starts more units takes fewer blocks.
+// A unit whose blocks start at position ub is served by the CTAs that own
+// positions ub .. ub + nb - 1.
+
+// CTAs that take work: each active CTA's share spans at least piece_cost + 1
+// positions, so it holds at least one block.
+__device__ __forceinline__ long long active_ctas(long long ncta, long long total, int piece_cost) {
+  const long long cap = total / (piece_cost + 1);
+  return ncta < cap ? ncta : (cap > 0 ? cap : 1);
+}
+
+// The CTA that owns position p of the line.
+__device__ __forceinline__ int position_owner(long long p, long long nact, long long total) {
+  return static_cast<int>(((p + 1) * nact - 1) / total);
+}
+
+// This CTA's share [b0, b1) of the line. Every thread of the CTA calls it. One
+// pass over context_lens: thread t owns a contiguous run of sequences, a
+// block-wide scan of the runs' lengths on the line gives the total and every
+// run's offset, and the thread whose run holds position b0 finds its sequence.
+// Results in plan[0..4] = total, b0, b1, first sequence s0, and the line length
+// per head of the sequences before s0 (plan[3] = -1 if the share is empty).
 // red must hold one long long per warp.
 __device__ inline void plan_cta_share(const DecodeArgs& a, long long* red, long long* plan) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -71,7 +90,7 @@ __device__ inline void plan_cta_share(const DecodeArgs& a, long long* red, long 
   const int s_lo = tid * per;
   const int s_hi = s_lo + per < S ? s_lo + per : S;
   long long mine = 0;
-  for (int s = s_lo; s < s_hi; ++s) mine += unit_blocks(a.context_lens[s], mbs);
+  for (int s = s_lo; s < s_hi; ++s) mine += unit_blocks(a.context_lens[s], mbs) + a.piece_cost;
   mine *= Hkv;
   long long v = mine;
 #pragma unroll
@@ -88,15 +107,15 @@ __device__ inline void plan_cta_share(const DecodeArgs& a, long long* red, long 
     tot += red[w];
   }
   const long long excl = pre + v - mine;
-  // Only min(grid, total) CTAs take work, so every active CTA owns at least one
+  // Only active_ctas() CTAs take work, so every active CTA owns at least one
   // block and every CTA between a unit's first and last owner wrote a piece of it.
-  const long long nact = ncta < tot ? ncta : tot;
+  const long long nact = active_ctas(ncta, tot, a.piece_cost);
   const long long b0 = cta < nact ? cta * tot / nact : tot;
   const long long b1 = cta < nact ? (cta + 1) * tot / nact : tot;
   if (b0 < b1 && excl <= b0 && b0 < excl + mine) {
     long long cum = excl;
     for (int s = s_lo; s < s_hi; ++s) {
-      const long long wblk = static_cast<long long>(Hkv) * unit_blocks(a.context_lens[s], mbs);
+      const long long wblk = static_cast<long long>(Hkv) * (unit_blocks(a.context_lens[s], mbs) + a.piece_cost);
       if (b0 < cum + wblk) {
         plan[3] = s;
         plan[4] = cum / Hkv;
@@ -112,8 +131,8 @@ __device__ inline void plan_cta_share(const DecodeArgs& a, long long* red, long 
 // After this CTA wrote its piece of unit u to slot (u + cta): count the piece on
 // the unit's counter; the CTA that finishes the last piece merges all pieces
 // into the output. Called by the nthr threads that wrote the slot (tid in
-// [0, nthr)), which synchronise on named barrier bar_id. ustart is the unit's
-// first global block, nb its block count, Rs its real rows, qb its first query
+// [0, nthr)), which synchronise on named barrier bar_id. ustart is the line
+// position of the unit's first block, nb its block count, Rs its real rows, qb its first query
 // row. Counters are tagged with the call's epoch, so no workspace clearing is needed.
 template <int KV, int D>
 __device__ inline void finish_split_piece(const DecodeArgs& a, int u, long long ustart, int nb,
@@ -128,9 +147,9 @@ __device__ inline void finish_split_piece(const DecodeArgs& a, int u, long long 
   named_bar_sync(bar_id, nthr);
   if (tid == 0) {
     fence_acq_rel_gpu();
-    const long long nact = ncta < total ? ncta : total;
-    const int c_first = static_cast<int>(((ustart + 1) * nact - 1) / total);
-    const int c_last = static_cast<int>(((ustart + nb) * nact - 1) / total);
+    const long long nact = active_ctas(ncta, total, a.piece_cost);
+    const int c_first = position_owner(ustart, nact, total);
+    const int c_last = position_owner(ustart + nb - 1, nact, total);
     unsigned long long* ctr = a.piece_counts + u;
     unsigned long long cur = atomicAdd(ctr, 0ull);
     unsigned long long want;

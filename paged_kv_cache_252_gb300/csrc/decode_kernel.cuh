@@ -174,17 +174,21 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
   const long long total = plan[0], b0 = plan[1], b1 = plan[2];
   if (b0 >= b1 || plan[3] < 0) return;
 
-  // Walk state, identical in every warp: current unit (s, h), block lb within it.
+  // Walk state, identical in every warp: current unit (s, h), its first block's
+  // position ub on the work line, and the first block lb this CTA takes in it.
+  const int pc0 = a.piece_cost;
   int s = static_cast<int>(plan[3]);
   int ctx = a.context_lens[s];
   int nb = unit_blocks(ctx, mbs);
   int h, lb;
+  long long ub;
   {
     const long long off = b0 - (long long)Hkv * plan[4];
-    h = static_cast<int>(off / nb);
-    lb = static_cast<int>(off % nb);
+    h = static_cast<int>(off / (nb + pc0));
+    const int o = static_cast<int>(off % (nb + pc0));
+    lb = o > pc0 ? o - pc0 : 0;
+    ub = b0 - o + pc0;
   }
-  long long gpos = b0;
 
   if (is_producer) {
     // ------------------------------- producer ------------------------------------
@@ -192,8 +196,8 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
     const int total_rows = a.num_blocks * Hkv * kBlockSize;   // host guarantees < 2^31
     int i = 0;
     bool ok = true;
-    while (gpos < b1 && ok) {
-      const int take = static_cast<int>(min(static_cast<long long>(nb - lb), b1 - gpos));
+    while (ub < b1 && ok) {
+      const int take = static_cast<int>(min(static_cast<long long>(nb), b1 - ub)) - lb;
       const int32_t* bt = a.block_tables + static_cast<size_t>(s) * mbs + lb;
       int nxt = (lane < take) ? bt[lane] : 0;
       for (int k0 = 0; k0 < take && ok; k0 += 32) {
@@ -243,17 +247,16 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
           if (!ok) break;   // block i was not issued
         }
       }
-      gpos += take;
-      lb += take;
-      if (lb == nb) {
-        lb = 0;
-        if (++h == Hkv) {
-          h = 0;
-          ++s;
-          if (gpos < b1) {
-            ctx = a.context_lens[s];
-            nb = unit_blocks(ctx, mbs);
-          }
+      // Next unit (a piece that stops before the unit's end ended the share).
+      if (lb + take < nb) break;
+      ub += nb + pc0;
+      lb = 0;
+      if (++h == Hkv) {
+        h = 0;
+        ++s;
+        if (ub < b1) {
+          ctx = a.context_lens[s];
+          nb = unit_blocks(ctx, mbs);
         }
       }
     }
@@ -274,8 +277,8 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
   bool alive = true;
   int i = 0;
 
-  while (gpos < b1) {
-    const int take = static_cast<int>(min(static_cast<long long>(nb - lb), b1 - gpos));
+  while (ub < b1) {
+    const int take = static_cast<int>(min(static_cast<long long>(nb), b1 - ub)) - lb;
     const bool first = (lb == 0), last = (lb + take == nb);
     const bool split = !(first && last);
     const int u = s * Hkv + h;
@@ -678,21 +681,19 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
     }
 
     if (split) {
-      finish_split_piece<KV, D>(a, u, gpos - lb, nb, total, ncta, Rs, qb, h, tid, nthr_c, 3, fin);
+      finish_split_piece<KV, D>(a, u, ub, nb, total, ncta, Rs, qb, h, tid, nthr_c, 3, fin);
     }
 
-    // ---- advance the walk ----
-    gpos += take;
-    lb += take;
-    if (lb == nb) {
-      lb = 0;
-      if (++h == Hkv) {
-        h = 0;
-        ++s;
-        if (gpos < b1) {
-          ctx = a.context_lens[s];
-          nb = unit_blocks(ctx, mbs);
-        }
+    // ---- advance the walk (a piece that stops before the unit's end ended the share) ----
+    if (lb + take < nb) break;
+    ub += nb + pc0;
+    lb = 0;
+    if (++h == Hkv) {
+      h = 0;
+      ++s;
+      if (ub < b1) {
+        ctx = a.context_lens[s];
+        nb = unit_blocks(ctx, mbs);
       }
     }
   }

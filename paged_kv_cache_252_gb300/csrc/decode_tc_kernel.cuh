@@ -181,11 +181,11 @@ __device__ __forceinline__ float warp_rows_sum(float (&v)[N], int lane) {
 // Position in a CTA's share: the current piece (unit (s, h), blocks
 // [lb, lb + take) of it) and the current chunk (blocks cofs .. cofs + 7 of the piece).
 struct TcWalk {
-  long long gpos;   // global index of the piece's first block
+  long long ub;     // work-line position of the unit's first block
   long long b1;     // end of the CTA's share
   int s, h, lb, nb, ctx, take, cofs;
 
-  __device__ bool done() const { return gpos >= b1; }
+  __device__ bool done() const { return take <= 0; }
   __device__ int nblk() const { return take - cofs < kTcChunk ? take - cofs : kTcChunk; }
   __device__ bool first() const { return cofs == 0; }
   __device__ bool last() const { return cofs + kTcChunk >= take; }
@@ -194,23 +194,21 @@ struct TcWalk {
     cofs += kTcChunk;
     if (cofs < take) return;
     cofs = 0;
-    gpos += take;
-    lb += take;
-    if (lb == nb) {
-      lb = 0;
-      if (++h == a.num_kv_heads) {
-        h = 0;
-        ++s;
-        if (gpos < b1) {
-          ctx = a.context_lens[s];
-          nb = unit_blocks(ctx, a.max_blocks_per_seq);
-        }
+    if (lb + take < nb) {   // the piece stopped before the unit's end: the share is done
+      take = 0;
+      return;
+    }
+    ub += nb + a.piece_cost;
+    lb = 0;
+    if (++h == a.num_kv_heads) {
+      h = 0;
+      ++s;
+      if (ub < b1) {
+        ctx = a.context_lens[s];
+        nb = unit_blocks(ctx, a.max_blocks_per_seq);
       }
     }
-    if (gpos < b1) {
-      const long long left = b1 - gpos;
-      take = left < nb - lb ? static_cast<int>(left) : nb - lb;
-    }
+    take = ub < b1 ? (b1 - ub < nb ? static_cast<int>(b1 - ub) : nb) : 0;
   }
 };
 
@@ -473,17 +471,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (b0 < b1 && plan[3] >= 0) {
     TcWalk w0;
     {
-      const int mbs = a.max_blocks_per_seq, Hkv = a.num_kv_heads;
+      const int mbs = a.max_blocks_per_seq, Hkv = a.num_kv_heads, pc0 = a.piece_cost;
       w0.b1 = b1;
-      w0.gpos = b0;
       w0.s = static_cast<int>(plan[3]);
       w0.ctx = a.context_lens[w0.s];
       w0.nb = unit_blocks(w0.ctx, mbs);
       const long long off = b0 - static_cast<long long>(Hkv) * plan[4];
-      w0.h = static_cast<int>(off / w0.nb);
-      w0.lb = static_cast<int>(off % w0.nb);
-      const long long left = b1 - b0;
-      w0.take = left < w0.nb - w0.lb ? static_cast<int>(left) : w0.nb - w0.lb;
+      w0.h = static_cast<int>(off / (w0.nb + pc0));
+      const int o = static_cast<int>(off % (w0.nb + pc0));
+      w0.lb = o > pc0 ? o - pc0 : 0;
+      w0.ub = b0 - o + pc0;
+      w0.take = static_cast<int>(b1 - w0.ub < w0.nb ? b1 - w0.ub : w0.nb) - w0.lb;
       w0.cofs = 0;
     }
 
@@ -774,7 +772,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           named_bar_sync(2, kTcSoftmaxThreads);
           wait_o(c);
           if (alive) tc_piece_output(a, t_cols, pc, cur.h, r0, RH, t, row_inv, cta);
-          if (pc.split) tc_finish_split(a, pc, cur.gpos - cur.lb, cur.nb, total, ncta, cur.h, tid, fin);
+          if (pc.split) tc_finish_split(a, pc, cur.ub, cur.nb, total, ncta, cur.h, tid, fin);
           // The next piece starts from an empty running max.
           named_bar_sync(2, kTcSoftmaxThreads);
           if (tid < RP) row_m[mp * RP + tid] = kNoMax;

@@ -46,6 +46,7 @@ struct DecodeArgs {
   int32_t slot_floats;         // floats per partial slot
   float scale_log2;            // softmax scale * log2(e)
   uint32_t epoch;              // distinct for every call (tags the piece counters)
+  int32_t piece_cost;          // fixed cost of a unit piece, in blocks, for the CTA shares
 };
 
 
