@@ -7,6 +7,7 @@ a call fails, a :class:`PagedKVError` is raised.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -23,6 +24,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()
 _lib = None
 _workspaces: dict = {}
+_ws_bytes_cache: dict = {}
 
 
 class PagedKVError(RuntimeError):
@@ -253,8 +255,8 @@ def paged_attention_decode_int8(out, q, k_cache, v_cache, k_scale, v_scale, bloc
     _scales_shape(k_cache, k_scale, v_scale)
     Hq = int(q.shape[1])
     lib = load_library()
-    with torch.cuda.device(q.device):
-        need = int(lib.pkv_decode_workspace_bytes(S, Hq, q_per_seq, ctypes.byref(d)))
+    with _on_device(q.device):
+        need = _ws_bytes(lib, q.device, S, Hq, int(q_per_seq), d)
         if workspace is None:
             workspace = _workspace(need, q.device)
         rc = lib.pkv_paged_attention_decode_int8(
@@ -289,6 +291,23 @@ def decode_workspace_bytes(num_seqs: int, num_q_heads: int, q_per_seq: int, k_ca
                                                              ctypes.byref(d)))
 
 
+def _on_device(device):
+    """The device context for a call, entered only when the tensors are not on the current device."""
+    if device.index is None or device.index == torch.cuda.current_device():
+        return contextlib.nullcontext()
+    return torch.cuda.device(device)
+
+
+def _ws_bytes(lib, device, S, Hq, n, d) -> int:
+    """pkv_decode_workspace_bytes, remembered per device and problem shape."""
+    key = (device.index, S, Hq, n, d.num_blocks, d.block_size, d.num_kv_heads, d.head_size)
+    v = _ws_bytes_cache.get(key)
+    if v is None:
+        v = int(lib.pkv_decode_workspace_bytes(S, Hq, n, ctypes.byref(d)))
+        _ws_bytes_cache[key] = v
+    return v
+
+
 def _workspace(nbytes: int, device) -> torch.Tensor:
     key = (str(device), torch.cuda.current_stream(device).cuda_stream)
     ws = _workspaces.get(key)
@@ -315,8 +334,8 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
     Hq = int(q.shape[1])
     code = _kv_code(kv_dtype, k_cache)
     lib = load_library()
-    with torch.cuda.device(q.device):
-        need = int(lib.pkv_decode_workspace_bytes(S, Hq, q_per_seq, ctypes.byref(d)))
+    with _on_device(q.device):
+        need = _ws_bytes(lib, q.device, S, Hq, int(q_per_seq), d)
         if workspace is None:
             workspace = _workspace(need, q.device)
         rc = lib.pkv_paged_attention_decode(
@@ -345,7 +364,7 @@ def paged_attention_decode_noalloc(out, q, k_cache, v_cache, block_tables, conte
         raise PagedKVError("out and q must share a dtype")
     d, _ = _decode_shapes(out, q, k_cache, v_cache, block_tables, context_lens,
                           rows=int(context_lens.shape[0]) * int(q_per_seq))
-    with torch.cuda.device(q.device):
+    with _on_device(q.device):
         rc = load_library().pkv_paged_attention_decode_noalloc(
             _ptr(out), _ptr(q), int(context_lens.shape[0]), int(q.shape[1]), int(q_per_seq),
             _ptr(k_cache), _ptr(v_cache), _kv_code(kv_dtype, k_cache), ctypes.byref(d),
@@ -375,8 +394,8 @@ def paged_attention_decode_varlen(out, q, cu_q_lens, k_cache, v_cache, block_tab
         raise PagedKVError("cu_q_lens must have num_seqs + 1 entries")
     Hq = int(q.shape[1])
     lib = load_library()
-    with torch.cuda.device(q.device):
-        need = int(lib.pkv_decode_workspace_bytes(S, Hq, int(max_q_per_seq), ctypes.byref(d)))
+    with _on_device(q.device):
+        need = _ws_bytes(lib, q.device, S, Hq, int(max_q_per_seq), d)
         if workspace is None:
             workspace = _workspace(need, q.device)
         rc = lib.pkv_paged_attention_decode_varlen(
@@ -416,8 +435,8 @@ def paged_attention_decode_tree(out, q, tree_masks, k_cache, v_cache, block_tabl
         raise PagedKVError("tree_masks must hold one mask per query row")
     Hq = int(q.shape[1])
     lib = load_library()
-    with torch.cuda.device(q.device):
-        need = int(lib.pkv_decode_workspace_bytes(S, Hq, int(max_q_per_seq), ctypes.byref(d)))
+    with _on_device(q.device):
+        need = _ws_bytes(lib, q.device, S, Hq, int(max_q_per_seq), d)
         if workspace is None:
             workspace = _workspace(need, q.device)
         rc = lib.pkv_paged_attention_decode_tree(
