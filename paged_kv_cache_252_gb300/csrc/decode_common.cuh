@@ -2,10 +2,11 @@
 // units and the tcgen05 kernel for wide ones): the CTA's share of the batch,
 // bounded mbarrier waits, and the fused split-KV combine.
 //
-// Work partition. All (sequence, KV head, block) triples of the batch, in the
-// order sequence-major / head / block, are cut into min(grid, total) contiguous
-// equal shares, one per CTA. A CTA's share covers whole units and at most two
-// partial ones (its first and last). A unit handled whole writes its output
+// Work partition. The batch's units (sequence, KV head), sequence-major, lie on
+// a work line: each unit a fixed number of positions for its per-piece work, then
+// one position per KV block. The line is cut into contiguous equal shares, one
+// per active CTA. A CTA's share covers whole units and at most two partial ones
+// (its first and last). A unit handled whole writes its output
 // directly; a unit cut across CTAs is computed as pieces, each piece writes
 // (m, l, o) -- running max, sum of exponentials, unnormalised output, in base 2
 // -- to workspace slot (unit + cta), and the CTA that completes the unit's last

@@ -1,6 +1,7 @@
 // Paged decode attention for sm_103a: one persistent wave of CTAs splits the
-// whole batch's KV blocks evenly (a stream over (sequence, KV head, block)),
-// each CTA streaming its share through a TMA-fed shared-memory ring.
+// whole batch's work evenly (a line over (sequence, KV head, block), each unit
+// weighted with its fixed per-piece work), each CTA streaming its share through
+// a TMA-fed shared-memory ring.
 //
 // What it computes follows "AI大模型推理速度翻倍，Colossal-Inference开源发布"
 // (分页注意力算法 PagedAttention: decode attention over KV blocks reached through
@@ -20,9 +21,9 @@
 //                        tensor cores (mma.sync m16n8k16, fp32 accumulate), online
 //                        softmax in base 2 with quad shuffles. E5M2 tiles are
 //                        widened to fp16 in registers (byte << 8 is exact);
-//                        INT8 tiles too (0x64 | (b ^ 0x80) is 1024 + 128 + b,
-//                        minus 1152 is b, exactly), with each token's K scale
-//                        applied to its scores and its V scale folded into P.
+//                        INT8 tiles to code + 1152 (0x64 | (b ^ 0x80)), the bias
+//                        taken off once per row after the MMAs, with each token's
+//                        K scale applied to its scores and its V scale folded into P.
 //   Block i of the CTA goes to ring stage i mod STAGES and to block-stream
 //   i mod WB; STAGES is a multiple of WB, so each stage has a single consumer
 //   stream and every wait on its mbarrier is for the next phase in order.
