@@ -19,8 +19,10 @@ value  = algorithmic bytes of the step / device time per step (GB/s), inputs
 e2e    = the same metric through the public Python API with host buffers: the
          step's q, new K/V tokens, slot mapping, block table and lengths copied
          from pinned host memory (one packed copy), and the output copied back,
-         inside the timing; copies run on a copy stream, double-buffered, and
-         overlap the neighbouring steps' kernels as in a serving loop.
+         inside the timing; copies run on copy streams, double-buffered, and
+         overlap the neighbouring steps' kernels as in a serving loop, and the
+         steps are captured once in a CUDA graph (64 per graph) and replayed
+         (--no-graph: direct calls).
 Several KV pools are rotated so that one cycle touches more than 4x the L2.
 
 Multi-GPU: replicas only. Each rank runs the same workload on its own GPU;
@@ -326,15 +328,20 @@ def run_ours(args, rank, world, local):
         for e_ in free + out_done:
             e_.record(comp)
 
-        def e2e_step(i):
+        def e2e_step(i, captured=False):
+            """One step. Inside a graph capture it waits only on events recorded by
+            earlier steps of the same capture: earlier replays already precede it in
+            stream order."""
             p, b = i % pools, i % 2
             v = views[b]
             with torch.cuda.stream(cs_in):
-                cs_in.wait_event(free[b])
+                if not captured or i >= 2:
+                    cs_in.wait_event(free[b])
                 dev_in[b].copy_(host_in, non_blocking=True)
                 ready[b].record(cs_in)
             comp.wait_event(ready[b])
-            comp.wait_event(out_done[p])
+            if not captured or i >= pools:
+                comp.wait_event(out_done[p])
             write(v["k_new"], v["v_new"], v["s_new"], caches[p])
             decode(outs[p], v["q"], caches[p], v["bt"], v["cl"], v.get("cu"))
             free[b].record(comp)
@@ -346,22 +353,57 @@ def run_ours(args, rank, world, local):
         for i in range(args.warmup):
             e2e_step(i)
         torch.cuda.synchronize(dev)
+        graph = None
+        if not args.no_graph:
+            # A serving loop replays captured steps: capture `chunk` steps (a multiple
+            # of the buffer and pool periods) once, with the copy streams forked from
+            # and joined back into the capture, and replay it.
+            period = 2 * pools // math.gcd(2, pools)
+            chunk = period * max(1, 64 // period)
+            cap = torch.cuda.Stream(dev)
+            cap.wait_stream(comp)
+            with torch.cuda.stream(cap):          # the binding's workspace for this stream, outside the capture
+                decode(outs[0], qs[0], caches[0], bt, cl, cu)
+            comp.wait_stream(cap)
+            torch.cuda.synchronize(dev)
+            graph = torch.cuda.CUDAGraph()
+            comp_outer = comp
+            with torch.cuda.graph(graph, stream=cap):
+                comp = torch.cuda.current_stream(dev)
+                cs_in.wait_stream(comp)
+                cs_out.wait_stream(comp)
+                for i in range(chunk):
+                    e2e_step(i, captured=True)
+                comp.wait_stream(cs_in)
+                comp.wait_stream(cs_out)
+            comp = comp_outer
+            replays = max(1, -(-args.steps // chunk))
+            e2e_steps = replays * chunk
+            graph.replay()
+            torch.cuda.synchronize(dev)
         barrier(world, dev)
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a0.record(comp)
-        cs_in.wait_stream(comp)   # the first upload starts inside the timed region
-        for i in range(args.steps):
-            e2e_step(i)
-        comp.wait_stream(cs_in)
-        comp.wait_stream(cs_out)  # the last outputs are back on the host
+        if graph is not None:
+            for _ in range(replays):
+                graph.replay()
+        else:
+            e2e_steps = args.steps
+            cs_in.wait_stream(comp)   # the first upload starts inside the timed region
+            for i in range(args.steps):
+                e2e_step(i)
+            comp.wait_stream(cs_in)
+            comp.wait_stream(cs_out)  # the last outputs are back on the host
         a1.record(comp)
         torch.cuda.synchronize(dev)
         e2e_el = a0.elapsed_time(a1) / 1e3
-        e2e_job_el, e2e_job_bytes = aggregate(e2e_el, step_bytes * args.steps, world, dev)
+        e2e_job_el, e2e_job_bytes = aggregate(e2e_el, step_bytes * e2e_steps, world, dev)
         e2e = {"value": round(e2e_job_bytes / e2e_job_el / 1e9, 2), "unit": "GB/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": round(e2e_el / args.steps * 1e3, 5),
-               "copies": "one packed H2D and one D2H per step on copy streams, double-buffered"}
+               "ms_per_step": round(e2e_el / e2e_steps * 1e3, 5), "steps": e2e_steps,
+               "copies": "one packed H2D and one D2H per step on copy streams, double-buffered",
+               "launch": (f"CUDA graph of {chunk} steps, replayed {replays} times" if graph is not None
+                          else "direct calls")}
 
     if rank != 0:
         return
@@ -542,6 +584,7 @@ def main(argv=None):
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="e2e by direct calls instead of graph replays")
     ap.add_argument("--no-clocks", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:

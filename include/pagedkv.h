@@ -127,6 +127,8 @@ size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t
  *   workspace     device scratch of at least pkv_decode_workspace_bytes(...)
  *                 bytes, 16-byte aligned; contents need no initialisation. Two
  *                 calls in flight at the same time must not share a workspace.
+ *                 A call may be captured in a CUDA graph and replayed: every
+ *                 launch leaves the workspace's counters clear when it completes.
  *
  *   For each sequence s, query head hq (KV head h = hq / (num_q_heads/num_kv_heads))
  *   and query token j, with L = context_lens[s] - q_per_seq + j + 1:

@@ -134,7 +134,9 @@ __device__ inline void plan_cta_share(const DecodeArgs& a, long long* red, long 
 // into the output. Called by the nthr threads that wrote the slot (tid in
 // [0, nthr)), which synchronise on named barrier bar_id. ustart is the line
 // position of the unit's first block, nb its block count, Rs its real rows, qb its first query
-// row. Counters are tagged with the call's epoch, so no workspace clearing is needed.
+// row. Counters are tagged with the call's epoch, so no workspace clearing is
+// needed, and the CTA that completes a unit clears its counter, so a replayed
+// CUDA graph (same epoch every replay) starts from clear counters too.
 template <int KV, int D>
 __device__ inline void finish_split_piece(const DecodeArgs& a, int u, long long ustart, int nb,
                                           long long total, long long ncta, int Rs, int qb, int h,
@@ -166,7 +168,13 @@ __device__ inline void finish_split_piece(const DecodeArgs& a, int u, long long 
     fin[0] = last ? 1 : 0;
     fin[1] = c_first;
     fin[2] = c_last;
-    if (last) fence_acq_rel_gpu();   // acquire: the other CTAs' slots are read next
+    if (last) {
+      // No other CTA touches this counter again in this launch. Leave it at 0
+      // (epoch 0 is never issued, so 0 reads as "no pieces" for any later call):
+      // a replayed CUDA graph reuses its epoch and must find the counters clear.
+      *ctr = 0ull;
+      fence_acq_rel_gpu();   // acquire: the other CTAs' slots are read next
+    }
   }
   named_bar_sync(bar_id, nthr);
   if (!fin[0]) return;
