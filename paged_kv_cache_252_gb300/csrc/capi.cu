@@ -120,7 +120,7 @@ DecodeGeometry choose_geometry(int kv, int d, int rows) {
 }
 
 // Units wider than 16 rows over an E5M2 cache with head size 128 run on the
-// tcgen05 kernel: one 192-thread CTA per SM holding the widened K/V chunk
+// tcgen05 kernel: one 320-thread CTA per SM holding the widened K/V chunk
 // buffers, P^T, two query tiles and a ring of as many 32 KB chunk buffers
 // (2..4) as fit in the 227 KB a CTA may use.
 bool use_tc(int kv, int d, int rows) { return kv == kKvE5m2 && d == 128 && rows > 16; }
