@@ -154,10 +154,13 @@ int pkv_paged_attention_decode(void* out, const void* q, int32_t num_seqs,
  *
  *   cu_q_lens     [num_seqs + 1] int32, device: sequence s owns query/output rows
  *                 cu_q_lens[s] .. cu_q_lens[s+1]-1 (cu_q_lens[0] = 0); its
- *                 n_s = cu_q_lens[s+1] - cu_q_lens[s] must be in [1, max_q_per_seq].
- *                 A sequence outside that range gets no output rows and sets
+ *                 n_s = cu_q_lens[s+1] - cu_q_lens[s] must be in [1, max_q_per_seq]
+ *                 and its rows must lie in [0, num_q_rows). A sequence that breaks
+ *                 either rule gets no output rows, reads none of q, and sets
  *                 PKV_DEV_BAD_CTX.
- *   out, q        [cu_q_lens[num_seqs]][num_q_heads][head_size].
+ *   num_q_rows    rows of q and out (normally cu_q_lens[num_seqs]); >= 1 when
+ *                 num_seqs > 0.
+ *   out, q        [num_q_rows][num_q_heads][head_size].
  *   max_q_per_seq sizes the per-unit row capacity: (num_q_heads/num_kv_heads) *
  *                 max_q_per_seq <= 64; pkv_decode_workspace_bytes(num_seqs,
  *                 num_q_heads, max_q_per_seq, cache) sizes the workspace.
@@ -165,7 +168,8 @@ int pkv_paged_attention_decode(void* out, const void* q, int32_t num_seqs,
  *   Everything else is as for pkv_paged_attention_decode.
  */
 int pkv_paged_attention_decode_varlen(void* out, const void* q, const int32_t* cu_q_lens,
-                                      int32_t num_seqs, int32_t num_q_heads, int32_t max_q_per_seq,
+                                      int32_t num_q_rows, int32_t num_seqs, int32_t num_q_heads,
+                                      int32_t max_q_per_seq,
                                       const void* k_cache, const void* v_cache, pkv_dtype kv_dtype,
                                       const pkv_cache_desc* cache, const int32_t* block_tables,
                                       int32_t max_blocks_per_seq, const int32_t* context_lens,
@@ -179,18 +183,20 @@ int pkv_paged_attention_decode_varlen(void* out, const void* q, const int32_t* c
  * frameworks, section FlexFlow), and each query token may attend only to the
  * context before the drafts and to its own ancestors.
  *
- *   tree_masks    [total query rows] uint64, device, 8-byte aligned: bit i of the
+ *   tree_masks    [num_q_rows] uint64, device, 8-byte aligned: bit i of the
  *                 mask of query token j of sequence s is set when j may attend to
  *                 draft token i, i.e. position context_lens[s] - n_s + i. A token
  *                 normally sees itself (bit j). A row that sees no position gets
  *                 output 0. The causal chain is mask (2 << j) - 1.
  *   cu_q_lens     may be NULL: then every sequence has max_q_per_seq tokens
- *                 (rows s*max_q_per_seq + j); otherwise as for the _varlen call.
+ *                 (rows s*max_q_per_seq + j) and num_q_rows must be at least
+ *                 num_seqs * max_q_per_seq; otherwise as for the _varlen call.
+ *   num_q_rows    rows of q, out and tree_masks.
  *   max_q_per_seq <= 64 (one mask bit per draft token).
  *   Everything else is as for pkv_paged_attention_decode_varlen.
  */
 int pkv_paged_attention_decode_tree(void* out, const void* q, const int32_t* cu_q_lens,
-                                    const uint64_t* tree_masks, int32_t num_seqs,
+                                    const uint64_t* tree_masks, int32_t num_q_rows, int32_t num_seqs,
                                     int32_t num_q_heads, int32_t max_q_per_seq,
                                     const void* k_cache, const void* v_cache, pkv_dtype kv_dtype,
                                     const pkv_cache_desc* cache, const int32_t* block_tables,

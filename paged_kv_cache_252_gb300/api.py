@@ -62,11 +62,11 @@ def load_library():
             ctypes.c_float, vp, ctypes.c_size_t, vp, vp]
         lib.pkv_paged_attention_decode.restype = ctypes.c_int
         lib.pkv_paged_attention_decode_varlen.argtypes = [
-            vp, vp, vp, i32, i32, i32, vp, vp, ctypes.c_int, P(_CacheDesc), vp, i32, vp,
+            vp, vp, vp, i32, i32, i32, i32, vp, vp, ctypes.c_int, P(_CacheDesc), vp, i32, vp,
             ctypes.c_float, vp, ctypes.c_size_t, vp, vp]
         lib.pkv_paged_attention_decode_varlen.restype = ctypes.c_int
         lib.pkv_paged_attention_decode_tree.argtypes = [
-            vp, vp, vp, vp, i32, i32, i32, vp, vp, ctypes.c_int, P(_CacheDesc), vp, i32, vp,
+            vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, ctypes.c_int, P(_CacheDesc), vp, i32, vp,
             ctypes.c_float, vp, ctypes.c_size_t, vp, vp]
         lib.pkv_paged_attention_decode_tree.restype = ctypes.c_int
         lib.pkv_paged_attention_decode_noalloc.argtypes = [
@@ -399,7 +399,7 @@ def paged_attention_decode_varlen(out, q, cu_q_lens, k_cache, v_cache, block_tab
         if workspace is None:
             workspace = _workspace(need, q.device)
         rc = lib.pkv_paged_attention_decode_varlen(
-            _ptr(out), _ptr(q), _ptr(cu_q_lens), S, Hq, int(max_q_per_seq), _ptr(k_cache),
+            _ptr(out), _ptr(q), _ptr(cu_q_lens), int(q.shape[0]), S, Hq, int(max_q_per_seq), _ptr(k_cache),
             _ptr(v_cache), _kv_code(kv_dtype, k_cache), ctypes.byref(d), _ptr(block_tables),
             int(block_tables.shape[1]), _ptr(context_lens), float(scale), _ptr(workspace),
             int(workspace.numel() * workspace.element_size()), _ptr(device_status),
@@ -440,7 +440,7 @@ def paged_attention_decode_tree(out, q, tree_masks, k_cache, v_cache, block_tabl
         if workspace is None:
             workspace = _workspace(need, q.device)
         rc = lib.pkv_paged_attention_decode_tree(
-            _ptr(out), _ptr(q), _ptr(cu_q_lens), _ptr(tree_masks), S, Hq, int(max_q_per_seq),
+            _ptr(out), _ptr(q), _ptr(cu_q_lens), _ptr(tree_masks), int(q.shape[0]), S, Hq, int(max_q_per_seq),
             _ptr(k_cache), _ptr(v_cache), _kv_code(kv_dtype, k_cache), ctypes.byref(d),
             _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens), float(scale),
             _ptr(workspace), int(workspace.numel() * workspace.element_size()),

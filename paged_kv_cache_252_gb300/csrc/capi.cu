@@ -327,9 +327,16 @@ size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t
 
 namespace {
 
+// Rows of q / out for num_seqs sequences of q_per_seq tokens (saturated; larger
+// problems are refused by decode_impl's size checks).
+int32_t fixed_rows(int32_t num_seqs, int32_t q_per_seq) {
+  const long long r = static_cast<long long>(num_seqs) * q_per_seq;
+  return r > INT32_MAX ? INT32_MAX : static_cast<int32_t>(r);
+}
+
 // Shared body of the decode entry points; cu_q_lens null means q_per_seq query
 // tokens for every sequence.
-int decode_impl(void* out, const void* q, const int32_t* cu_q_lens,
+int decode_impl(void* out, const void* q, const int32_t* cu_q_lens, int32_t num_q_rows,
                 const unsigned long long* tree_masks, const float* k_scale, const float* v_scale,
                 int32_t num_seqs,
                 int32_t num_q_heads, int32_t q_per_seq, const void* k_cache, const void* v_cache,
@@ -357,6 +364,11 @@ int decode_impl(void* out, const void* q, const int32_t* cu_q_lens,
     return PKV_ERR_UNSUPPORTED;
   if (num_seqs == 0) return PKV_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace)
+    return PKV_ERR_INVALID_ARGUMENT;
+  // Every row the kernels may touch lies below num_q_rows: with cu_q_lens each
+  // sequence's rows are checked on the device against it; without, all
+  // num_seqs * q_per_seq rows must exist.
+  if (num_q_rows < 1 || (!cu_q_lens && static_cast<long long>(num_seqs) * q_per_seq > num_q_rows))
     return PKV_ERR_INVALID_ARGUMENT;
   if (cu_q_lens && !aligned4(cu_q_lens)) return PKV_ERR_INVALID_ARGUMENT;
   if (tree_masks && (reinterpret_cast<uintptr_t>(tree_masks) & 7u)) return PKV_ERR_INVALID_ARGUMENT;
@@ -402,6 +414,7 @@ int decode_impl(void* out, const void* q, const int32_t* cu_q_lens,
   a.block_tables = block_tables;
   a.context_lens = context_lens;
   a.cu_q_lens = cu_q_lens;
+  a.q_rows = num_q_rows;
   a.tree_masks = tree_masks;
   a.k_scale = kv_dtype == PKV_INT8 ? k_scale : nullptr;
   a.v_scale = kv_dtype == PKV_INT8 ? v_scale : nullptr;
@@ -451,28 +464,30 @@ int pkv_paged_attention_decode(void* out, const void* q, int32_t num_seqs, int32
                                const int32_t* block_tables, int32_t max_blocks_per_seq,
                                const int32_t* context_lens, float scale, void* workspace,
                                size_t workspace_bytes, int32_t* device_status, void* stream) {
-  return decode_impl(out, q, nullptr, nullptr, nullptr, nullptr, num_seqs, num_q_heads, q_per_seq, k_cache,
-                     v_cache, kv_dtype,
+  return decode_impl(out, q, nullptr, fixed_rows(num_seqs, q_per_seq), nullptr, nullptr, nullptr, num_seqs, num_q_heads,
+                     q_per_seq, k_cache, v_cache, kv_dtype,
                      cache, block_tables, max_blocks_per_seq, context_lens, scale, workspace,
                      workspace_bytes, device_status, stream);
 }
 
 int pkv_paged_attention_decode_varlen(void* out, const void* q, const int32_t* cu_q_lens,
-                                      int32_t num_seqs, int32_t num_q_heads, int32_t max_q_per_seq,
+                                      int32_t num_q_rows, int32_t num_seqs, int32_t num_q_heads,
+                                      int32_t max_q_per_seq,
                                       const void* k_cache, const void* v_cache, pkv_dtype kv_dtype,
                                       const pkv_cache_desc* cache, const int32_t* block_tables,
                                       int32_t max_blocks_per_seq, const int32_t* context_lens,
                                       float scale, void* workspace, size_t workspace_bytes,
                                       int32_t* device_status, void* stream) {
   if (num_seqs > 0 && !cu_q_lens) return PKV_ERR_INVALID_ARGUMENT;
-  return decode_impl(out, q, cu_q_lens, nullptr, nullptr, nullptr, num_seqs, num_q_heads, max_q_per_seq,
+  return decode_impl(out, q, cu_q_lens, num_q_rows, nullptr, nullptr, nullptr, num_seqs, num_q_heads,
+                     max_q_per_seq,
                      k_cache, v_cache,
                      kv_dtype, cache, block_tables, max_blocks_per_seq, context_lens, scale,
                      workspace, workspace_bytes, device_status, stream);
 }
 
 int pkv_paged_attention_decode_tree(void* out, const void* q, const int32_t* cu_q_lens,
-                                    const uint64_t* tree_masks, int32_t num_seqs,
+                                    const uint64_t* tree_masks, int32_t num_q_rows, int32_t num_seqs,
                                     int32_t num_q_heads, int32_t max_q_per_seq,
                                     const void* k_cache, const void* v_cache, pkv_dtype kv_dtype,
                                     const pkv_cache_desc* cache, const int32_t* block_tables,
@@ -481,7 +496,7 @@ int pkv_paged_attention_decode_tree(void* out, const void* q, const int32_t* cu_
                                     int32_t* device_status, void* stream) {
   if (num_seqs > 0 && !tree_masks) return PKV_ERR_INVALID_ARGUMENT;
   if (max_q_per_seq > 64) return PKV_ERR_UNSUPPORTED;
-  return decode_impl(out, q, cu_q_lens, reinterpret_cast<const unsigned long long*>(tree_masks), nullptr,
+  return decode_impl(out, q, cu_q_lens, num_q_rows, reinterpret_cast<const unsigned long long*>(tree_masks), nullptr,
                      nullptr, num_seqs, num_q_heads, max_q_per_seq, k_cache, v_cache, kv_dtype, cache,
                      block_tables, max_blocks_per_seq, context_lens, scale, workspace,
                      workspace_bytes, device_status, stream);
@@ -493,7 +508,8 @@ int pkv_paged_attention_decode_int8(void* out, const void* q, int32_t num_seqs, 
                                     const int32_t* block_tables, int32_t max_blocks_per_seq,
                                     const int32_t* context_lens, float scale, void* workspace,
                                     size_t workspace_bytes, int32_t* device_status, void* stream) {
-  return decode_impl(out, q, nullptr, nullptr, k_scale, v_scale, num_seqs, num_q_heads, q_per_seq, k_cache,
+  return decode_impl(out, q, nullptr, fixed_rows(num_seqs, q_per_seq), nullptr, k_scale, v_scale, num_seqs, num_q_heads,
+                     q_per_seq, k_cache,
                      v_cache, PKV_INT8, cache, block_tables, max_blocks_per_seq, context_lens, scale, workspace,
                      workspace_bytes, device_status, stream);
 }

@@ -287,15 +287,20 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
     const int ctx_eff = ctx < cap ? ctx : cap;
     // Query tokens of sequence s: n_s of them, rows qb.. of q/out ("nopadding"
     // packed tokens). With cu_q_lens a sequence may carry fewer than q_per_seq;
-    // a count outside [1, q_per_seq] is flagged and the sequence gets no rows.
+    // a count outside [1, q_per_seq], or rows past the end of q, is flagged and
+    // the sequence gets no rows.
     int n_s = n, qb = s * n;
     if (a.cu_q_lens) {
       qb = a.cu_q_lens[s];
       n_s = a.cu_q_lens[s + 1] - qb;
     }
-    const bool rows_ok = n_s >= 1 && n_s <= n;
+    // The sequence's rows must also lie inside q / out (a.q_rows rows).
+    const bool rows_ok = n_s >= 1 && n_s <= n && qb >= 0 && qb <= a.q_rows - n_s;
     const int Rs = rows_ok ? G * n_s : 0;          // real rows of this unit
-    if (!rows_ok) n_s = 1;
+    if (!rows_ok) {
+      n_s = 1;
+      qb = 0;
+    }
     if (first && warp == 0 && lane == 0 && (!rows_ok || ctx < n_s || ctx > cap) && a.status) {
       atomicOr(a.status, kDevBadCtx);
     }

@@ -224,15 +224,20 @@ __device__ __forceinline__ TcPiece tc_piece(const DecodeArgs& a, const TcWalk& w
   const int cap = a.max_blocks_per_seq * kBlockSize;
   p.ctx_eff = w.ctx < cap ? w.ctx : cap;
   // Query tokens of sequence s: n_s of them at rows qb.. of q/out; a count
-  // outside [1, q_per_seq] is flagged and the sequence gets no rows.
+  // outside [1, q_per_seq], or rows past the end of q, is flagged and the
+  // sequence gets no rows.
   int n_s = n, qb = w.s * n;
   if (a.cu_q_lens) {
     qb = a.cu_q_lens[w.s];
     n_s = a.cu_q_lens[w.s + 1] - qb;
   }
-  const bool rows_ok = n_s >= 1 && n_s <= n;
+  // The sequence's rows must also lie inside q / out (a.q_rows rows).
+  const bool rows_ok = n_s >= 1 && n_s <= n && qb >= 0 && qb <= a.q_rows - n_s;
   p.Rs = rows_ok ? a.group * n_s : 0;
-  if (!rows_ok) n_s = 1;
+  if (!rows_ok) {
+    n_s = 1;
+    qb = 0;
+  }
   if (w.lb == 0 && tid == 0 && (!rows_ok || w.ctx < n_s || w.ctx > cap) && a.status) {
     atomicOr(a.status, kDevBadCtx);
   }

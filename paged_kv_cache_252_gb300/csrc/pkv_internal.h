@@ -26,6 +26,7 @@ struct DecodeArgs {
   const int32_t* block_tables; // [S][max_blocks_per_seq]
   const int32_t* context_lens; // [S]
   const int32_t* cu_q_lens;    // [S+1] query-token offsets, or null: q_per_seq tokens each
+  int32_t q_rows;              // rows of q / out (and tree_masks): a sequence's rows must lie below
   const unsigned long long* tree_masks;  // [rows] draft tokens visible to each query token, or null: causal
   const float* k_scale;        // INT8 cache: [num_blocks][Hkv][16] per-row scales, else null
   const float* v_scale;

@@ -296,6 +296,33 @@ def test_varlen_rejects_bad_counts_without_faulting(orc, dev, gpu):
     assert torch.isnan(out2[1:4]).all()           # sequence 1 got no output rows
 
 
+@pytest.mark.parametrize("kv,Hq,Hkv", [("fp16", 8, 2), ("e5m2", 64, 8)], ids=["mma", "tcgen05"])
+def test_varlen_rows_past_q_are_flagged_not_read(orc, dev, gpu, kv, Hq, Hkv):
+    """cu_q_lens that send a sequence's rows past the end of q: the sequence is
+    flagged and gets no output, the others are unaffected. q and out are the first
+    rows of larger buffers, so even a missed check would stay inside memory; the
+    rows past the view must come back untouched."""
+    import paged_kv_cache_252_gb300 as pkv
+    q_lens = [2, 4, 3]
+    w = wl.custom(num_seqs=3, num_q_heads=Hq, num_kv_heads=Hkv, head_size=128, q_per_seq=4,
+                  kv_dtype=kv, context_lens=[40, 70, 33], seed=12, q_lens=q_lens)
+    vals = wl.token_values(w)
+    kc, vc, out = gpu.cuda_path(w, vals, dev)        # all 9 rows, the reference for rows 0..5
+    qbuf = torch.zeros(12, Hq, 128, dtype=torch.float16, device=dev)
+    qbuf[:9] = vals["q"].to(dev)
+    obuf = torch.full_like(qbuf, float("nan"))
+    q7, o7 = qbuf[:7], obuf[:7]                      # sequence 2 owns rows 6..8: past row 7
+    cu = torch.from_numpy(w.cu_q_lens()).to(dev)
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    cl = torch.from_numpy(w.context_lens).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    pkv.paged_attention_decode_varlen(o7, q7, cu, kc, vc, bt, cl, 4, w.scale, device_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 0x4
+    assert torch.equal(obuf[:6], out[:6])            # sequences 0 and 1 as in the full call
+    assert torch.isnan(obuf[6:]).all()               # nothing written for sequence 2 or past the view
+
+
 # ------------------------------------------------------------------------------------
 # token-tree verify
 # ------------------------------------------------------------------------------------
