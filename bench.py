@@ -230,10 +230,10 @@ def run_ours(args, rank, world, local):
         else:
             pkv.kv_cache_write(kn, vn, sn, c[0], c[1])
 
-    caches = []   # (k_cache, v_cache[, k_scale, v_scale])
+    caches = []   # (k_cache, v_cache[, scales])
     for _ in range(pools):
         kc, vc = pkv.alloc_kv_cache(w.num_blocks, w.num_kv_heads, w.head_size, w.kv_dtype, dev)
-        c = (kc, vc) + (pkv.alloc_kv_scales(w.num_blocks, w.num_kv_heads, dev) if int8 else ())
+        c = (kc, vc) + ((pkv.alloc_kv_scales(w.num_blocks, w.num_kv_heads, dev),) if int8 else ())
         write(vals["k_all"], vals["v_all"], vals["slot_all"], c)   # prefill
         caches.append(c)
     new_idx = vals["new_idx"]

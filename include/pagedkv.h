@@ -248,13 +248,15 @@ int pkv_paged_attention_decode_noalloc(void* out, const void* q, int32_t num_seq
  * both divisions in IEEE fp32; an all-zero row has scale 0 and codes 0; an
  * element's value is code * scale.
  *
- * Caches: int8 [num_blocks][num_kv_heads][16][head_size]; scales: float32
- * [num_blocks][num_kv_heads][16] (one per cached row), all 16-byte aligned.
+ * Caches: int8 [num_blocks][num_kv_heads][16][head_size]; scales: one float32
+ * array [num_blocks][num_kv_heads][2][16]: the 16 K row scales of a (block,
+ * KV head) tile, then its 16 V row scales (so one 128-byte copy brings both),
+ * all 16-byte aligned.
  * key/value: fp16 [num_tokens][num_kv_heads][head_size]. Slots as in
  * pkv_kv_cache_write (-1 skipped, other out-of-range slots skipped and flagged). */
 int pkv_kv_cache_write_int8(const void* key, const void* value, int32_t num_tokens,
                             const int32_t* slot_mapping, void* k_cache, void* v_cache,
-                            float* k_scale, float* v_scale, const pkv_cache_desc* cache,
+                            float* scales, const pkv_cache_desc* cache,
                             int32_t* device_status, void* stream);
 
 /* pkv_paged_attention_decode over an INT8 cache (q and out fp16): each token's
@@ -262,7 +264,7 @@ int pkv_kv_cache_write_int8(const void* key, const void* value, int32_t num_toke
  * Workspace as for pkv_paged_attention_decode (pkv_decode_workspace_bytes). */
 int pkv_paged_attention_decode_int8(void* out, const void* q, int32_t num_seqs, int32_t num_q_heads,
                                     int32_t q_per_seq, const void* k_cache, const void* v_cache,
-                                    const float* k_scale, const float* v_scale,
+                                    const float* scales,
                                     const pkv_cache_desc* cache, const int32_t* block_tables,
                                     int32_t max_blocks_per_seq, const int32_t* context_lens,
                                     float scale, void* workspace, size_t workspace_bytes,
@@ -340,13 +342,15 @@ int pkv_seq_add_cached(pkv_allocator* a, int64_t seq, const int32_t* tokens, int
 
 /* ==== Block copy (device) ===================================================
  * For i < n: physical block dst[i] of both caches becomes a copy of block
- * src[i] (every head's 16 rows). src and dst are DEVICE int32 arrays; ids out of
- * range are skipped and set PKV_DEV_BAD_BLOCK. The pairs must not overlap in a
- * way that reads a block after it was written in the same call. Asynchronous on
- * stream. */
-int pkv_copy_blocks(void* k_cache, void* v_cache, pkv_dtype kv_dtype, const pkv_cache_desc* cache,
-                    const int32_t* src, const int32_t* dst, int32_t n, int32_t* device_status,
-                    void* stream);
+ * src[i] (every head's 16 rows), and for an INT8 cache (kv_dtype PKV_INT8) so do
+ * the block's row scales in `scales` ([num_blocks][num_kv_heads][2][16] floats,
+ * 16-byte aligned; NULL for every other cache). src and dst are DEVICE int32
+ * arrays; ids out of range are skipped and set PKV_DEV_BAD_BLOCK. The pairs
+ * must not overlap in a way that reads a block after it was written in the same
+ * call. Asynchronous on stream. */
+int pkv_copy_blocks(void* k_cache, void* v_cache, float* scales, pkv_dtype kv_dtype,
+                    const pkv_cache_desc* cache, const int32_t* src, const int32_t* dst, int32_t n,
+                    int32_t* device_status, void* stream);
 
 /* Static description of a status code. Never NULL. */
 const char* pkv_error_string(int code);

@@ -99,12 +99,12 @@ def load_library():
         lib.pkv_prefix_insert.restype = i32
         lib.pkv_seq_add_cached.argtypes = [vp, i64, vp, i32, vp]
         lib.pkv_seq_add_cached.restype = ctypes.c_int
-        lib.pkv_copy_blocks.argtypes = [vp, vp, ctypes.c_int, P(_CacheDesc), vp, vp, i32, vp, vp]
+        lib.pkv_copy_blocks.argtypes = [vp, vp, vp, ctypes.c_int, P(_CacheDesc), vp, vp, i32, vp, vp]
         lib.pkv_copy_blocks.restype = ctypes.c_int
-        lib.pkv_kv_cache_write_int8.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, P(_CacheDesc), vp, vp]
+        lib.pkv_kv_cache_write_int8.argtypes = [vp, vp, i32, vp, vp, vp, vp, P(_CacheDesc), vp, vp]
         lib.pkv_kv_cache_write_int8.restype = ctypes.c_int
         lib.pkv_paged_attention_decode_int8.argtypes = [
-            vp, vp, i32, i32, i32, vp, vp, vp, vp, P(_CacheDesc), vp, i32, vp, ctypes.c_float, vp,
+            vp, vp, i32, i32, i32, vp, vp, vp, P(_CacheDesc), vp, i32, vp, ctypes.c_float, vp,
             ctypes.c_size_t, vp, vp]
         lib.pkv_paged_attention_decode_int8.restype = ctypes.c_int
         lib.pkv_error_string.argtypes = [ctypes.c_int]
@@ -182,10 +182,10 @@ def _decode_shapes(out, q, k_cache, v_cache, block_tables, context_lens, rows=No
     return d, S
 
 
-def _scales_shape(k_cache, k_scale, v_scale):
-    want = tuple(k_cache.shape[:3])
-    if tuple(k_scale.shape) != want or tuple(v_scale.shape) != want:
-        raise PagedKVError(f"k_scale and v_scale must be float32 {want}")
+def _scales_shape(k_cache, scales):
+    want = (int(k_cache.shape[0]), int(k_cache.shape[1]), 2, BLOCK_SIZE)
+    if tuple(scales.shape) != want or scales.dtype != torch.float32:
+        raise PagedKVError(f"scales must be float32 {want} (K then V row scales)")
 
 
 def _write_shapes(key, value, slot_mapping, k_cache, v_cache) -> _CacheDesc:
@@ -217,42 +217,41 @@ def alloc_kv_cache(num_blocks: int, num_kv_heads: int, head_size: int, kv_dtype,
 
 
 def alloc_kv_scales(num_blocks: int, num_kv_heads: int, device="cuda"):
-    """Row scales of an INT8 cache pair: float32 [num_blocks, num_kv_heads, 16] each."""
-    shape = (num_blocks, num_kv_heads, BLOCK_SIZE)
-    return (torch.zeros(shape, dtype=torch.float32, device=device),
-            torch.zeros(shape, dtype=torch.float32, device=device))
+    """Row scales of an INT8 cache pair: one float32 tensor [num_blocks, num_kv_heads, 2, 16],
+    [..., 0, t] the K scale and [..., 1, t] the V scale of token t of a block."""
+    return torch.zeros((num_blocks, num_kv_heads, 2, BLOCK_SIZE), dtype=torch.float32, device=device)
 
 
-def kv_cache_write_int8(key, value, slot_mapping, k_cache, v_cache, k_scale, v_scale, *,
+def kv_cache_write_int8(key, value, slot_mapping, k_cache, v_cache, scales, *,
                         device_status=None, stream=None):
     """Quantise fp16 key/value [T, Hkv, D] into INT8 caches and their row scales."""
     for n, t in (("key", key), ("value", value), ("slot_mapping", slot_mapping), ("k_cache", k_cache),
-                 ("v_cache", v_cache), ("k_scale", k_scale), ("v_scale", v_scale)):
+                 ("v_cache", v_cache), ("scales", scales)):
         _need_cuda_contig(n, t)
-    if key.dtype != torch.float16 or k_cache.dtype != torch.int8 or k_scale.dtype != torch.float32:
+    if key.dtype != torch.float16 or k_cache.dtype != torch.int8 or scales.dtype != torch.float32:
         raise PagedKVError("INT8 cache write takes fp16 key/value, int8 caches, float32 scales")
     if slot_mapping.dtype != torch.int32:
         raise PagedKVError("slot_mapping must be int32")
     d = _write_shapes(key, value, slot_mapping, k_cache, v_cache)
-    _scales_shape(k_cache, k_scale, v_scale)
+    _scales_shape(k_cache, scales)
     rc = load_library().pkv_kv_cache_write_int8(
         _ptr(key), _ptr(value), int(key.shape[0]), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
-        _ptr(k_scale), _ptr(v_scale), ctypes.byref(d), _ptr(device_status), _stream_handle(stream, key.device))
+        _ptr(scales), ctypes.byref(d), _ptr(device_status), _stream_handle(stream, key.device))
     _check(rc, "kv_cache_write_int8")
 
 
-def paged_attention_decode_int8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+def paged_attention_decode_int8(out, q, k_cache, v_cache, scales, block_tables, context_lens,
                                 q_per_seq: int, scale: float, *, workspace=None, device_status=None,
                                 stream=None):
     """paged_attention_decode over an INT8 cache with its row scales (q/out fp16)."""
-    for n, t in (("out", out), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("k_scale", k_scale),
-                 ("v_scale", v_scale), ("block_tables", block_tables), ("context_lens", context_lens)):
+    for n, t in (("out", out), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("scales", scales),
+                 ("block_tables", block_tables), ("context_lens", context_lens)):
         _need_cuda_contig(n, t)
     if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
         raise PagedKVError("block_tables and context_lens must be int32")
     d, S = _decode_shapes(out, q, k_cache, v_cache, block_tables, context_lens,
                           rows=int(context_lens.shape[0]) * int(q_per_seq))
-    _scales_shape(k_cache, k_scale, v_scale)
+    _scales_shape(k_cache, scales)
     Hq = int(q.shape[1])
     lib = load_library()
     with _on_device(q.device):
@@ -260,8 +259,8 @@ def paged_attention_decode_int8(out, q, k_cache, v_cache, k_scale, v_scale, bloc
         if workspace is None:
             workspace = _workspace(need, q.device)
         rc = lib.pkv_paged_attention_decode_int8(
-            _ptr(out), _ptr(q), S, Hq, int(q_per_seq), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
-            _ptr(v_scale), ctypes.byref(d), _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens),
+            _ptr(out), _ptr(q), S, Hq, int(q_per_seq), _ptr(k_cache), _ptr(v_cache), _ptr(scales),
+            ctypes.byref(d), _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens),
             float(scale), _ptr(workspace), int(workspace.numel() * workspace.element_size()),
             _ptr(device_status), _stream_handle(stream, q.device))
     _check(rc, "paged_attention_decode_int8")
@@ -537,15 +536,22 @@ class BlockAllocator:
         return int(got.value)
 
 
-def copy_blocks(k_cache, v_cache, src, dst, kv_dtype=None, *, device_status=None, stream=None):
+def copy_blocks(k_cache, v_cache, src, dst, kv_dtype=None, *, scales=None, device_status=None, stream=None):
     """Physical block dst[i] of both caches becomes a copy of block src[i]
-    (int32 device tensors of equal length)."""
+    (int32 device tensors of equal length); an INT8 cache's row scales
+    (``scales``, from alloc_kv_scales) are copied with its blocks."""
     for n_, t in (("k_cache", k_cache), ("v_cache", v_cache), ("src", src), ("dst", dst)):
         _need_cuda_contig(n_, t)
     if src.dtype != torch.int32 or dst.dtype != torch.int32 or src.numel() != dst.numel():
         raise PagedKVError("src and dst must be int32 tensors of equal length")
     d = _pair(k_cache, v_cache)
-    rc = load_library().pkv_copy_blocks(_ptr(k_cache), _ptr(v_cache), _kv_code(kv_dtype, k_cache),
+    code = _kv_code(kv_dtype, k_cache)
+    if (code == KV_INT8) != (scales is not None):
+        raise PagedKVError("an INT8 cache is copied with its scales; other caches take none")
+    if scales is not None:
+        _need_cuda_contig("scales", scales)
+        _scales_shape(k_cache, scales)
+    rc = load_library().pkv_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(scales), code,
                                         ctypes.byref(d), _ptr(src), _ptr(dst), int(src.numel()),
                                         _ptr(device_status), _stream_handle(stream, k_cache.device))
     _check(rc, "copy_blocks")

@@ -44,7 +44,7 @@ std::atomic<uint32_t> g_call_epoch{0};
 // Fixed cost of one unit piece on the work line, in KV blocks: the piece's
 // query load, epilogue and (when split) merge take about as long as streaming
 // this many blocks, so CTAs whose share starts more units get fewer blocks.
-constexpr int kPieceCost2B = 5;   // mma.sync kernel, fp16 / bf16 cache
+constexpr int kPieceCost2B = 8;   // mma.sync kernel, fp16 / bf16 cache
 constexpr int kPieceCost1B = 4;   // mma.sync kernel, E5M2 / INT8 cache
 constexpr int kPieceCostTc = 24;  // tcgen05 kernel (its epilogue reads O from tensor memory)
 int piece_cost(bool tc, int kv) {
@@ -337,7 +337,7 @@ int32_t fixed_rows(int32_t num_seqs, int32_t q_per_seq) {
 // Shared body of the decode entry points; cu_q_lens null means q_per_seq query
 // tokens for every sequence.
 int decode_impl(void* out, const void* q, const int32_t* cu_q_lens, int32_t num_q_rows,
-                const unsigned long long* tree_masks, const float* k_scale, const float* v_scale,
+                const unsigned long long* tree_masks, const float* scales,
                 int32_t num_seqs,
                 int32_t num_q_heads, int32_t q_per_seq, const void* k_cache, const void* v_cache,
                 pkv_dtype kv_dtype, const pkv_cache_desc* cache, const int32_t* block_tables,
@@ -349,9 +349,9 @@ int decode_impl(void* out, const void* q, const int32_t* cu_q_lens, int32_t num_
   if (kv_dtype != PKV_FP16 && kv_dtype != PKV_BF16 && kv_dtype != PKV_FP8_E5M2 && kv_dtype != PKV_INT8)
     return PKV_ERR_UNSUPPORTED;
   if (num_q_heads % cache->num_kv_heads != 0) return PKV_ERR_INVALID_ARGUMENT;
-  // An INT8 cache is read with its row scales, 16-byte aligned (each block's
-  // 16 scales move as one 64-byte copy).
-  if (kv_dtype == PKV_INT8 && (!k_scale || !v_scale || !aligned16(k_scale) || !aligned16(v_scale)))
+  // An INT8 cache is read with its row scales, 16-byte aligned (a block's 16 K
+  // and 16 V scales move as one 128-byte copy).
+  if (kv_dtype == PKV_INT8 && (!scales || !aligned16(scales)))
     return PKV_ERR_INVALID_ARGUMENT;
   const int group = num_q_heads / cache->num_kv_heads;
   const long long rows_ll = static_cast<long long>(group) * q_per_seq;
@@ -416,8 +416,7 @@ int decode_impl(void* out, const void* q, const int32_t* cu_q_lens, int32_t num_
   a.cu_q_lens = cu_q_lens;
   a.q_rows = num_q_rows;
   a.tree_masks = tree_masks;
-  a.k_scale = kv_dtype == PKV_INT8 ? k_scale : nullptr;
-  a.v_scale = kv_dtype == PKV_INT8 ? v_scale : nullptr;
+  a.scales = kv_dtype == PKV_INT8 ? scales : nullptr;
   a.piece_counts = reinterpret_cast<unsigned long long*>(ws);
   a.partials = reinterpret_cast<float*>(ws + desc_bytes(units));
   a.status = device_status;
@@ -464,7 +463,7 @@ int pkv_paged_attention_decode(void* out, const void* q, int32_t num_seqs, int32
                                const int32_t* block_tables, int32_t max_blocks_per_seq,
                                const int32_t* context_lens, float scale, void* workspace,
                                size_t workspace_bytes, int32_t* device_status, void* stream) {
-  return decode_impl(out, q, nullptr, fixed_rows(num_seqs, q_per_seq), nullptr, nullptr, nullptr, num_seqs, num_q_heads,
+  return decode_impl(out, q, nullptr, fixed_rows(num_seqs, q_per_seq), nullptr, nullptr, num_seqs, num_q_heads,
                      q_per_seq, k_cache, v_cache, kv_dtype,
                      cache, block_tables, max_blocks_per_seq, context_lens, scale, workspace,
                      workspace_bytes, device_status, stream);
@@ -479,7 +478,7 @@ int pkv_paged_attention_decode_varlen(void* out, const void* q, const int32_t* c
                                       float scale, void* workspace, size_t workspace_bytes,
                                       int32_t* device_status, void* stream) {
   if (num_seqs > 0 && !cu_q_lens) return PKV_ERR_INVALID_ARGUMENT;
-  return decode_impl(out, q, cu_q_lens, num_q_rows, nullptr, nullptr, nullptr, num_seqs, num_q_heads,
+  return decode_impl(out, q, cu_q_lens, num_q_rows, nullptr, nullptr, num_seqs, num_q_heads,
                      max_q_per_seq,
                      k_cache, v_cache,
                      kv_dtype, cache, block_tables, max_blocks_per_seq, context_lens, scale,
@@ -497,32 +496,32 @@ int pkv_paged_attention_decode_tree(void* out, const void* q, const int32_t* cu_
   if (num_seqs > 0 && !tree_masks) return PKV_ERR_INVALID_ARGUMENT;
   if (max_q_per_seq > 64) return PKV_ERR_UNSUPPORTED;
   return decode_impl(out, q, cu_q_lens, num_q_rows, reinterpret_cast<const unsigned long long*>(tree_masks), nullptr,
-                     nullptr, num_seqs, num_q_heads, max_q_per_seq, k_cache, v_cache, kv_dtype, cache,
+                     num_seqs, num_q_heads, max_q_per_seq, k_cache, v_cache, kv_dtype, cache,
                      block_tables, max_blocks_per_seq, context_lens, scale, workspace,
                      workspace_bytes, device_status, stream);
 }
 
 int pkv_paged_attention_decode_int8(void* out, const void* q, int32_t num_seqs, int32_t num_q_heads,
                                     int32_t q_per_seq, const void* k_cache, const void* v_cache,
-                                    const float* k_scale, const float* v_scale, const pkv_cache_desc* cache,
+                                    const float* scales, const pkv_cache_desc* cache,
                                     const int32_t* block_tables, int32_t max_blocks_per_seq,
                                     const int32_t* context_lens, float scale, void* workspace,
                                     size_t workspace_bytes, int32_t* device_status, void* stream) {
-  return decode_impl(out, q, nullptr, fixed_rows(num_seqs, q_per_seq), nullptr, k_scale, v_scale, num_seqs, num_q_heads,
+  return decode_impl(out, q, nullptr, fixed_rows(num_seqs, q_per_seq), nullptr, scales, num_seqs, num_q_heads,
                      q_per_seq, k_cache,
                      v_cache, PKV_INT8, cache, block_tables, max_blocks_per_seq, context_lens, scale, workspace,
                      workspace_bytes, device_status, stream);
 }
 
 int pkv_kv_cache_write_int8(const void* key, const void* value, int32_t num_tokens, const int32_t* slot_mapping,
-                            void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                            void* k_cache, void* v_cache, float* scales,
                             const pkv_cache_desc* cache, int32_t* device_status, void* stream) {
   if (num_tokens < 0 || !valid_cache(cache)) return PKV_ERR_INVALID_ARGUMENT;
   if (num_tokens == 0) return PKV_OK;
-  if (!key || !value || !slot_mapping || !k_cache || !v_cache || !k_scale || !v_scale)
+  if (!key || !value || !slot_mapping || !k_cache || !v_cache || !scales)
     return PKV_ERR_INVALID_ARGUMENT;
   if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache) ||
-      !aligned16(k_scale) || !aligned16(v_scale) || !aligned4(slot_mapping) ||
+      !aligned16(scales) || !aligned4(slot_mapping) ||
       (device_status && !aligned4(device_status)))
     return PKV_ERR_INVALID_ARGUMENT;
   std::lock_guard<std::mutex> lock(g_mu);
@@ -534,8 +533,7 @@ int pkv_kv_cache_write_int8(const void* key, const void* value, int32_t num_toke
   a.slot_mapping = slot_mapping;
   a.k_cache = k_cache;
   a.v_cache = v_cache;
-  a.k_scale = k_scale;
-  a.v_scale = v_scale;
+  a.scales = scales;
   a.status = device_status;
   a.num_slots = static_cast<long long>(cache->num_blocks) * kBlockSize;
   a.num_tokens = num_tokens;

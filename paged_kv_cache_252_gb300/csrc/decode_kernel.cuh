@@ -224,12 +224,11 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
               const uint32_t kdst = ring + stage * 2 * TILE;
               mbar_arrive_expect_tx(full, 2 * TILE + ((kInt8 && !bad) ? 128 : 0));
               if constexpr (kInt8) {
-                // The block's 16 K and 16 V row scales (a bad block id reads none).
+                // The block's 16 K and 16 V row scales, adjacent in memory: one
+                // 128-byte copy (a bad block id reads none).
                 if (!bad) {
-                  const size_t srow = (static_cast<size_t>(blk) * Hkv + h) * kBlockSize;
-                  const uint32_t sdst = smem_addr(smem + lay.scales + stage * 128);
-                  bulk_load(sdst, a.k_scale + srow, 64, full);
-                  bulk_load(sdst + 64, a.v_scale + srow, 64, full);
+                  const size_t stile = static_cast<size_t>(blk) * Hkv + h;
+                  bulk_load(smem_addr(smem + lay.scales + stage * 128), a.scales + stile * 32, 128, full);
                 }
               }
               if constexpr (RB == 256) {

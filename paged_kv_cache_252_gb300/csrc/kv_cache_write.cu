@@ -123,7 +123,8 @@ __global__ void __launch_bounds__(256) kv_cache_write_int8_kernel(const CacheWri
     } else {
       *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(packed);
     }
-    if (lane == 0) (is_v ? a.v_scale : a.k_scale)[row] = scale;
+    // [block][head][K, V][16]: row = (block * Hkv + head) * 16 + token
+    if (lane == 0) a.scales[(row >> 4) * 32 + (is_v ? 16 : 0) + (row & 15)] = scale;
   }
   pdl_launch_dependents();
 }

@@ -28,8 +28,7 @@ struct DecodeArgs {
   const int32_t* cu_q_lens;    // [S+1] query-token offsets, or null: q_per_seq tokens each
   int32_t q_rows;              // rows of q / out (and tree_masks): a sequence's rows must lie below
   const unsigned long long* tree_masks;  // [rows] draft tokens visible to each query token, or null: causal
-  const float* k_scale;        // INT8 cache: [num_blocks][Hkv][16] per-row scales, else null
-  const float* v_scale;
+  const float* scales;         // INT8 cache: [num_blocks][Hkv][2][16] K then V row scales, else null
   float* partials;             // split-KV partial slots
   unsigned long long* piece_counts;  // [S*Hkv]: (call epoch << 32) | pieces finished
   int32_t* status;             // optional device status word
@@ -149,8 +148,7 @@ struct CacheWriteArgs {
   int32_t num_kv_heads;
   int32_t head_size;
   int32_t kv;                  // kKvF16 / kKvBf16 / kKvE5m2 / kKvInt8
-  float* k_scale;              // INT8 cache: [num_blocks][num_kv_heads][16] row scales
-  float* v_scale;
+  float* scales;               // INT8 cache: [num_blocks][num_kv_heads][2][16] K then V row scales
 };
 
 }  // namespace pkv

@@ -31,8 +31,8 @@ def main(argv=None):
     kc, vc = api.alloc_kv_cache(w.num_blocks, w.num_kv_heads, w.head_size, w.kv_dtype, dev)
     int8 = w.kv_dtype == "int8"
     if int8:
-        ks, vs = api.alloc_kv_scales(w.num_blocks, w.num_kv_heads, dev)
-        api.kv_cache_write_int8(vals["k_all"], vals["v_all"], vals["slot_all"], kc, vc, ks, vs)
+        sc = api.alloc_kv_scales(w.num_blocks, w.num_kv_heads, dev)
+        api.kv_cache_write_int8(vals["k_all"], vals["v_all"], vals["slot_all"], kc, vc, sc)
     else:
         api.kv_cache_write(vals["k_all"], vals["v_all"], vals["slot_all"], kc, vc)
     bt = torch.from_numpy(w.block_tables).to(dev)
@@ -42,7 +42,7 @@ def main(argv=None):
     cu = torch.from_numpy(w.cu_q_lens()).to(dev) if w.q_lens is not None else None
     for _ in range(args.iters):
         if int8:
-            api.paged_attention_decode_int8(out, vals["q"], kc, vc, ks, vs, bt, cl, w.q_per_seq, w.scale,
+            api.paged_attention_decode_int8(out, vals["q"], kc, vc, sc, bt, cl, w.q_per_seq, w.scale,
                                             device_status=status)
         elif cu is not None:
             api.paged_attention_decode_varlen(out, vals["q"], cu, kc, vc, bt, cl, w.q_per_seq,

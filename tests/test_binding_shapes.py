@@ -91,12 +91,12 @@ def test_cache_write_and_int8_shapes(stub):
         api.kv_cache_write(torch.zeros(5, 2, 32, dtype=torch.float16), torch.zeros(5, 2, 32, dtype=torch.float16),
                            slots, kc, kc.clone())
     k8 = torch.zeros(4, 2, 16, 64, dtype=torch.int8)
-    ks = torch.zeros(4, 2, 16, dtype=torch.float32)
+    sc = torch.zeros(4, 2, 2, 16, dtype=torch.float32)
     with pytest.raises(_Reached):
-        api.kv_cache_write_int8(key, key.clone(), slots, k8, k8.clone(), ks, ks.clone())
-    with pytest.raises(api.PagedKVError):
-        api.kv_cache_write_int8(key, key.clone(), slots, k8, k8.clone(), ks[:3].contiguous(), ks.clone())
+        api.kv_cache_write_int8(key, key.clone(), slots, k8, k8.clone(), sc)
+    with pytest.raises(api.PagedKVError):   # the old two-array shape
+        api.kv_cache_write_int8(key, key.clone(), slots, k8, k8.clone(), sc[:, :, 0].contiguous())
     c = _case(kv=torch.int8)
     with pytest.raises(api.PagedKVError):   # scales of another pool size
-        api.paged_attention_decode_int8(c["out"], c["q"], c["k_cache"], c["v_cache"], ks, ks.clone(),
+        api.paged_attention_decode_int8(c["out"], c["q"], c["k_cache"], c["v_cache"], sc,
                                         c["block_tables"], c["context_lens"], 2, 0.125)

@@ -19,32 +19,38 @@ def dev():
     return torch.device("cuda:0")
 
 
-@pytest.mark.parametrize("kv,D", [("fp16", 128), ("bf16", 64), ("e5m2", 128)])
+@pytest.mark.parametrize("kv,D", [("fp16", 128), ("bf16", 64), ("e5m2", 128), ("int8", 128)])
 def test_copy_blocks_bit_exact(dev, kv, D):
     import paged_kv_cache_252_gb300 as pkv
     nb, Hkv = 40, 4
     kc, vc = pkv.alloc_kv_cache(nb, Hkv, D, kv, dev)
     g = torch.Generator(device="cpu").manual_seed(5)
-    for c in (kc, vc):
+    sc = pkv.alloc_kv_scales(nb, Hkv, dev) if kv == "int8" else None
+    for c in (kc, vc) + ((sc,) if sc is not None else ()):
         c.view(torch.uint8).copy_(torch.randint(0, 256, c.view(torch.uint8).shape, generator=g,
                                                 dtype=torch.uint8).to(dev))
     k0, v0 = kc.clone(), vc.clone()
+    s0 = sc.clone() if sc is not None else None
     perm = torch.randperm(nb, generator=g)
     src, dst = perm[:12].to(torch.int32), perm[12:24].to(torch.int32)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    pkv.copy_blocks(kc, vc, src.to(dev), dst.to(dev), device_status=status)
+    pkv.copy_blocks(kc, vc, src.to(dev), dst.to(dev), scales=sc, device_status=status)
     torch.cuda.synchronize()
     ek, ev = k0.clone(), v0.clone()
     ek[dst.long().to(dev)] = k0[src.long().to(dev)]
     ev[dst.long().to(dev)] = v0[src.long().to(dev)]
     assert torch.equal(kc.view(torch.uint8), ek.view(torch.uint8))
     assert torch.equal(vc.view(torch.uint8), ev.view(torch.uint8))
+    if sc is not None:
+        es = s0.clone()
+        es[dst.long().to(dev)] = s0[src.long().to(dev)]
+        assert torch.equal(sc.view(torch.uint8), es.view(torch.uint8))
     assert int(status.item()) == 0
     # an out-of-range id is skipped and flagged
     bad_src = torch.tensor([nb + 3, int(src[0])], dtype=torch.int32, device=dev)
     bad_dst = torch.tensor([int(dst[0]), -1], dtype=torch.int32, device=dev)
     before = kc.clone()
-    pkv.copy_blocks(kc, vc, bad_src, bad_dst, device_status=status)
+    pkv.copy_blocks(kc, vc, bad_src, bad_dst, scales=sc, device_status=status)
     torch.cuda.synchronize()
     assert int(status.item()) & 0x2 and torch.equal(kc.view(torch.uint8), before.view(torch.uint8))
 

@@ -26,17 +26,24 @@ def gpu(dev):
 
 
 def _gpu_caches(w, vals, dev, status=None):
-    """Prefill tokens, then the step's new tokens, through the INT8 cache write."""
+    """Prefill tokens, then the step's new tokens, through the INT8 cache write.
+    Returns the caches and the one scales tensor [nb, Hkv, 2, 16] (K, then V)."""
     import paged_kv_cache_252_gb300 as pkv
     kc, vc = pkv.alloc_kv_cache(w.num_blocks, w.num_kv_heads, w.head_size, "int8", dev)
-    ks, vs = pkv.alloc_kv_scales(w.num_blocks, w.num_kv_heads, dev)
+    sc = pkv.alloc_kv_scales(w.num_blocks, w.num_kv_heads, dev)
     k_all, v_all, slots = vals["k_all"].to(dev), vals["v_all"].to(dev), vals["slot_all"].to(dev)
     pre = torch.from_numpy(wl.prefill_mask(w)).to(dev)
     for m in (pre, ~pre):
         if bool(m.any()):
             pkv.kv_cache_write_int8(k_all[m].contiguous(), v_all[m].contiguous(), slots[m].contiguous(),
-                                    kc, vc, ks, vs, device_status=status)
-    return kc, vc, ks, vs
+                                    kc, vc, sc, device_status=status)
+    return kc, vc, sc
+
+
+def _split_scales(sc):
+    """The GPU's scales tensor as the oracle's separate K and V arrays [nb, Hkv, 16]."""
+    a = sc.cpu().numpy()
+    return a[:, :, 0, :], a[:, :, 1, :]
 
 
 def _oracle_caches(orc, w, vals):
@@ -53,19 +60,20 @@ def _oracle_caches(orc, w, vals):
 def _check(orc, gpu, w, dev, *, seqs=None, values_device="cpu"):
     import paged_kv_cache_252_gb300 as pkv
     vals = wl.token_values(w, device=values_device)
-    kc, vc, ks, vs = _gpu_caches(w, vals, dev)
+    kc, vc, sc = _gpu_caches(w, vals, dev)
     q = vals["q"].to(dev)
     out = torch.full_like(q, float("nan"))
     bt = torch.from_numpy(w.block_tables).to(dev)
     cl = torch.from_numpy(w.context_lens).to(dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    pkv.paged_attention_decode_int8(out, q, kc, vc, ks, vs, bt, cl, w.q_per_seq, w.scale, device_status=status)
+    pkv.paged_attention_decode_int8(out, q, kc, vc, sc, bt, cl, w.q_per_seq, w.scale, device_status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
+    ks, vs = _split_scales(sc)
     vals = {k: v.cpu() for k, v in vals.items()}
     okc, ovc, oks, ovs = _oracle_caches(orc, w, vals)
     assert np.array_equal(kc.cpu().numpy(), okc) and np.array_equal(vc.cpu().numpy(), ovc)
-    assert np.array_equal(ks.cpu().numpy(), oks) and np.array_equal(vs.cpu().numpy(), ovs)
+    assert np.array_equal(ks, oks) and np.array_equal(vs, ovs)
     ref, _, rc = orc.paged_attention(bits16(vals["q"]), 0, w.q_per_seq, okc, ovc, 3, w.block_tables,
                                      w.context_lens, w.scale, seqs=seqs, num_threads=orc.hardware_threads(),
                                      k_scale=oks, v_scale=ovs)
@@ -88,9 +96,9 @@ def test_int8_cache_write_bit_exact_on_hard_rows(orc, dev):
         key = torch.from_numpy(x).to(dev)
         val = torch.from_numpy(x[::-1].copy()).to(dev)
         kc, vc = pkv.alloc_kv_cache(nb, Hkv, D, "int8", dev)
-        ks, vs = pkv.alloc_kv_scales(nb, Hkv, dev)
+        sc = pkv.alloc_kv_scales(nb, Hkv, dev)
         status = torch.zeros(1, dtype=torch.int32, device=dev)
-        pkv.kv_cache_write_int8(key, val, torch.from_numpy(slots).to(dev), kc, vc, ks, vs, device_status=status)
+        pkv.kv_cache_write_int8(key, val, torch.from_numpy(slots).to(dev), kc, vc, sc, device_status=status)
         torch.cuda.synchronize()
         okc = np.zeros((nb, Hkv, 16, D), np.int8)
         ovc = np.zeros_like(okc)
@@ -99,10 +107,11 @@ def test_int8_cache_write_bit_exact_on_hard_rows(orc, dev):
         assert orc.kv_cache_write_int8(x.view(np.uint16), x[::-1].copy().view(np.uint16), slots,
                                        okc, ovc, oks, ovs) == 0
         assert np.array_equal(kc.cpu().numpy(), okc) and np.array_equal(vc.cpu().numpy(), ovc)
-        assert np.array_equal(ks.cpu().numpy(), oks) and np.array_equal(vs.cpu().numpy(), ovs)
+        ks, vs = _split_scales(sc)
+        assert np.array_equal(ks, oks) and np.array_equal(vs, ovs)
         assert int(status.item()) == 0
         bad = torch.tensor([nb * 16 + 2], dtype=torch.int32, device=dev)
-        pkv.kv_cache_write_int8(key[:1].contiguous(), val[:1].contiguous(), bad, kc, vc, ks, vs,
+        pkv.kv_cache_write_int8(key[:1].contiguous(), val[:1].contiguous(), bad, kc, vc, sc,
                                 device_status=status)
         torch.cuda.synchronize()
         assert int(status.item()) & 0x1
@@ -140,14 +149,14 @@ def test_int8_bad_block_is_flagged_not_faulted(orc, dev, gpu):
     w = wl.custom(num_seqs=3, num_q_heads=8, num_kv_heads=2, head_size=128, q_per_seq=1, kv_dtype="int8",
                   context_lens=[40, 70, 9], seed=6)
     vals = wl.token_values(w)
-    kc, vc, ks, vs = _gpu_caches(w, vals, dev)
+    kc, vc, sc = _gpu_caches(w, vals, dev)
     bt = torch.from_numpy(w.block_tables).to(dev)
     bt[0, 1] = w.num_blocks + 3
     cl = torch.from_numpy(w.context_lens).to(dev)
     q = vals["q"].to(dev)
     out = torch.empty_like(q)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    pkv.paged_attention_decode_int8(out, q, kc, vc, ks, vs, bt, cl, 1, w.scale, device_status=status)
+    pkv.paged_attention_decode_int8(out, q, kc, vc, sc, bt, cl, 1, w.scale, device_status=status)
     torch.cuda.synchronize()
     assert int(status.item()) & 0x2
     okc, ovc, oks, ovs = _oracle_caches(orc, w, vals)
