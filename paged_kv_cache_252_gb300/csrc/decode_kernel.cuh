@@ -196,6 +196,8 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
     const uint64_t pol = l2_policy_evict_first();
     const int total_rows = a.num_blocks * Hkv * kBlockSize;   // host guarantees < 2^31
     int i = 0;
+    int pst = 0;           // i % stages
+    uint32_t pwrap = 0;    // (i / stages) & 1
     bool ok = true;
     while (ub < b1 && ok) {
       const int take = static_cast<int>(min(static_cast<long long>(nb), b1 - ub)) - lb;
@@ -209,9 +211,8 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
           const int blk = __shfl_sync(0xffffffffu, cur, k);
           int good = ok ? 1 : 0;
           if (lane == 0 && good) {
-            const int stage = i % stages;
-            if (i >= stages &&
-                !wait_or_abort(bars + 8 * (stages + stage), ((i / stages) - 1) & 1, abort_flag)) {
+            const int stage = pst;
+            if (i >= stages && !wait_or_abort(bars + 8 * (stages + stage), pwrap ^ 1u, abort_flag)) {
               good = 0;
               *abort_flag = 1;
               if (a.status) atomicOr(a.status, kDevTimeout);
@@ -245,6 +246,10 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
           }
           ok = __shfl_sync(0xffffffffu, good, 0) != 0;
           if (!ok) break;   // block i was not issued
+          if (++pst == stages) {
+            pst = 0;
+            pwrap ^= 1u;
+          }
         }
       }
       // Next unit (a piece that stops before the unit's end ended the share).
@@ -276,6 +281,10 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
   const int row_base = wr * 8 * NTW;
   bool alive = true;
   int i = 0;
+  // This block-stream takes the blocks ib = wb, wb + WB, ... of the share in order;
+  // their ring stage and phase advance by WB blocks at a time (stages is a multiple of WB).
+  int cst = wb;          // ib % stages of the stream's next block
+  uint32_t cph = 0;      // (ib / stages) & 1
 
   while (ub < b1) {
     const int take = static_cast<int>(min(static_cast<long long>(nb), b1 - ub)) - lb;
@@ -400,9 +409,13 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
 
     const int k_first = ((wb - (i % WB)) % WB + WB) % WB;
     for (int k = k_first; k < take; k += WB) {
-      const int ib = i + k;
-      const int stage = ib % stages;
-      const uint32_t parity = static_cast<uint32_t>((ib / stages) & 1);
+      const int stage = cst;
+      const uint32_t parity = cph;
+      cst += WB;
+      if (cst >= stages) {
+        cst -= stages;
+        cph ^= 1u;
+      }
       const uint32_t kt = ring + stage * 2 * TILE, vt = kt + TILE;
       if (alive && !wait_or_abort(bars + 8 * stage, parity, abort_flag)) {
         alive = false;

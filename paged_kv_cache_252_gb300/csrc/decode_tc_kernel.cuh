@@ -496,6 +496,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int total_rows = a.num_blocks * a.num_kv_heads * kBlockSize;   // host guarantees < 2^31
       TcWalk w = w0;
       int c = 0;
+      int buf = 0;          // c % nbuf
+      uint32_t wrap = 0;    // (c / nbuf) & 1
       while (!w.done()) {
         const int nbk = w.nblk();
         const int32_t* bt = a.block_tables + static_cast<size_t>(w.s) * a.max_blocks_per_seq + w.lb + w.cofs;
@@ -505,8 +507,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int k = 0; k < kTcChunk; ++k) blk[k] = __shfl_sync(0xffffffffu, mine, k);
         int good = 1;
         if (lane == 0) {
-          const int buf = c % nbuf;
-          if (c >= nbuf && !tc_wait(bars + 8 * (nbuf + buf), ((c / nbuf) - 1) & 1, abort_flag)) {
+          if (c >= nbuf && !tc_wait(bars + 8 * (nbuf + buf), wrap ^ 1u, abort_flag)) {
             good = 0;
             *abort_flag = 1;
             if (a.status) atomicOr(a.status, kDevTimeout);
@@ -529,6 +530,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         if (__shfl_sync(0xffffffffu, good, 0) == 0) break;   // chunk c was not issued
         ++c;
+        if (++buf == nbuf) {
+          buf = 0;
+          wrap ^= 1u;
+        }
         w.advance(a);
       }
       // Drain: every copy issued into this CTA's shared memory lands before exit.
@@ -631,6 +636,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       TcWalk cur = w0;
       TcPiece pc = tc_piece(a, cur, tid);
       int c = 0, piece = 0;
+      int buf_next = 1;          // (c + 1) % nbuf (nbuf >= 2)
+      uint32_t wrap_next = 0;    // ((c + 1) / nbuf) & 1
 
       // Prologue: chunk 0 and the first piece's queries.
       {
@@ -662,7 +669,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           pn = tc_piece(a, nxt, tid);
           tc_copy_q<RP, kTcSoftmaxThreads>(a, pn, nxt.h, tid, qst + ((piece + 1) & 1) * 2 * kRowsHalf);
         }
-        const int buf_next = (c + 1) % nbuf;
         const uint8_t* ring_next = ring + buf_next * CHUNK_BYTES;
         const bool valid_next =
             has_next && (t >> 4) < nxt.nblk() && nxt.first_token() + t < pn.ctx_eff;
@@ -681,7 +687,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // (2) K of chunk c+1 into K buffer (c+1) % 2, last read by S(c-1) (complete):
         //     S(c+1) overlaps the softmax below
         if (has_next) {
-          wait_bar(bars + 8 * buf_next, ((c + 1) / nbuf) & 1);
+          wait_bar(bars + 8 * buf_next, wrap_next);
           if (alive) widen_e5m2_half_row_tmem(ring_next, t, hh, valid_next, t_lane + kTcKCol + ((c + 1) & 1) * 64);
           cp_async_wait_all();
           fence_proxy_async_smem();
@@ -790,6 +796,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         cur = nxt;
         ++c;
+        if (++buf_next == nbuf) {
+          buf_next = 0;
+          wrap_next ^= 1u;
+        }
       }
     }
   }
