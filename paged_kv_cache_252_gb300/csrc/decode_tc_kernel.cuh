@@ -547,6 +547,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t id_o = idesc_kind_f16(128, RP, 0, 1, 0);   // V^T (MN-major) x P^T (K-major)
         const uint32_t t_o = tmem + kTcOCol;
         const uint32_t v16a = smem_addr(v16), pa = smem_addr(pst), qa = smem_addr(qst);
+        // Descriptors of the buffers' first atoms, built once: a later atom is the same
+        // descriptor with its address field (bits 0..13, 16-byte units) advanced, and
+        // every shared-memory address here stays below 2^18 bytes, so the field never carries.
+        const uint64_t dq0 = smem_desc_sw128(qa, 0, 1024), dq1 = smem_desc_sw128(qa + 2 * kRowsHalf, 0, 1024);
+        const uint64_t dv0 = smem_desc_sw128(v16a, kHalf, 1024), dv1 = smem_desc_sw128(v16a + kWide, kHalf, 1024);
+        const uint64_t dp = smem_desc_sw128(pa, 0, 1024);
         TcWalk w = w0;
         int c = 0, piece = 0;
         bool prev = false, prev_first = false, ok = true;
@@ -556,12 +562,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // S^T(c) = K(c) Q^T: S and K buffer c % 2
             if (!(ok = tc_wait(bar_kready, c & 1, abort_flag))) break;
             tc_fence_after_sync();
-            const uint32_t qsel = qa + (piece & 1) * 2 * kRowsHalf;
+            const uint64_t dqs = (piece & 1) ? dq1 : dq0;
             const uint32_t t_s = tmem + (c & 1) * kTcSCols;
             const uint32_t t_k = tmem + kTcKCol + (c & 1) * 64;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-              const uint64_t db = smem_desc_sw128(qsel + (kk >> 2) * kRowsHalf + (kk & 3) * 32, 0, 1024);
+              const uint64_t db = dqs + (((kk >> 2) * kRowsHalf + (kk & 3) * 32) >> 4);
               tc_mma_f16_ts(t_s, t_k + kk * 8, db, id_s, kk > 0 ? 1u : 0u);
             }
             tc_commit(bar_sfull);
@@ -570,12 +576,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // O^T += V(c-1)^T P^T
             if (!(ok = tc_wait(bar_pvready, (c - 1) & 1, abort_flag))) break;
             tc_fence_after_sync();
-            const uint32_t vsel = v16a + ((c - 1) & 1) * kWide;
+            const uint64_t dvs = ((c - 1) & 1) ? dv1 : dv0;
 #pragma unroll
             for (int kk = 0; kk < kTcChunk; ++kk) {
-              const uint64_t db = smem_desc_sw128(pa + (kk >> 2) * kRowsHalf + (kk & 3) * 32, 0, 1024);
-              tc_mma_f16_ss(t_o, smem_desc_sw128(vsel + kk * 2048, kHalf, 1024), db, id_o,
-                            (kk > 0 || !prev_first) ? 1u : 0u);
+              const uint64_t db = dp + (((kk >> 2) * kRowsHalf + (kk & 3) * 32) >> 4);
+              tc_mma_f16_ss(t_o, dvs + ((kk * 2048) >> 4), db, id_o, (kk > 0 || !prev_first) ? 1u : 0u);
             }
             tc_commit(bar_odone);
           }
