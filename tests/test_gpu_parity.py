@@ -1,9 +1,10 @@
 """CUDA path vs the CPU oracle, through the C ABI (Python binding = marshalling only).
 
 Cache writes must match the oracle's cache image bit for bit; attention outputs
-must satisfy |gpu - oracle| <= 2e-3 + 1e-2*|oracle| element-wise (fp64 oracle;
-for E5M2 the oracle reads the same E5M2 bytes, which the cache check proves
-identical).
+must meet the parity gate of tests/_gpu.py: max |gpu - oracle| <= 2e-3 over every
+element and max relative error <= 1e-2 over elements with |oracle| >= 0.2 (fp64
+oracle; an E5M2 cache is read by the oracle from the same bytes, which the cache
+check proves identical; bf16 outputs take the absolute gate below |oracle| 0.5).
 """
 import numpy as np
 import pytest
@@ -212,7 +213,7 @@ def test_empty_batch_is_a_no_op(dev):
 
 
 # ------------------------------------------------------------------------------------
-# the five workloads: reduced sizes in full, full sizes on sampled sequences
+# the five workloads: reduced sizes, and full sizes over every sequence
 # ------------------------------------------------------------------------------------
 
 REDUCED = {
@@ -229,20 +230,12 @@ def test_workload_reduced_full_parity(orc, dev, gpu, key):
     gpu.full_check(orc, w, dev)
 
 
-def _sample(w, k, seed=0):
-    lens = w.context_lens
-    rng = np.random.default_rng(seed)
-    pick = {int(np.argmax(lens)), int(np.argmin(lens))}
-    pick |= set(int(x) for x in rng.choice(w.num_seqs, size=min(k, w.num_seqs), replace=False))
-    return sorted(pick)
-
-
-@pytest.mark.parametrize("key,k", [("8b", 6), ("8b_fp8", 6), ("long", 1), ("70b_spec", 8)])
-def test_workload_full_size_sampled_parity(orc, dev, gpu, key, k):
-    """Full-size workload in the bench's launch configuration: every cache byte is
-    compared; outputs of sampled sequences (longest, shortest, random) against the oracle."""
+@pytest.mark.parametrize("key", ["8b", "8b_fp8", "long", "70b_spec"])
+def test_workload_full_size_parity(orc, dev, gpu, key):
+    """Full-size workload in the bench's launch configuration: every cache byte and
+    every output element of every sequence against the oracle."""
     w = wl.by_name(key)
-    gpu.full_check(orc, w, dev, seqs=_sample(w, k), values_device=dev)
+    gpu.full_check(orc, w, dev, values_device=dev)
 
 
 # ------------------------------------------------------------------------------------
@@ -272,9 +265,8 @@ def test_mixed_workload_reduced(orc, dev, gpu):
     gpu.full_check(orc, wl.reduced(wl.by_name("mixed"), num_seqs=12), dev)
 
 
-def test_mixed_workload_full_size_sampled(orc, dev, gpu):
-    w = wl.by_name("mixed")
-    gpu.full_check(orc, w, dev, seqs=_sample(w, 6), values_device=dev)
+def test_mixed_workload_full_size(orc, dev, gpu):
+    gpu.full_check(orc, wl.by_name("mixed"), dev, values_device=dev)
 
 
 def test_varlen_rejects_bad_counts_without_faulting(orc, dev, gpu):
@@ -365,4 +357,4 @@ def test_tree_verify_parity(orc, dev, gpu, case):
         kw["cu_q_lens"] = w.cu_q_lens()
     ref, _, rc = gpu.oracle_attention(orc, w, vals, okc, ovc, **kw)
     assert rc == 0
-    gpu.compare(out, ref)
+    gpu.compare(out, ref, label=f"tree {kv} D{D} G{Hq // Hkv} q_lens {q_lens}")

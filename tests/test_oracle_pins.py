@@ -509,6 +509,27 @@ def test_int8_codes_are_nearest_and_span_the_row(orc):
     assert np.all(np.abs(xf - codes * scales[..., None].astype(np.float64)) <= 0.5 * scales[..., None] * (1 + 1e-5))
 
 
+def test_int8_golden_ties(orc):
+    """Hand-worked rows (tests/golden/int8_ties.json) whose x / scale values are exact
+    ties: the codes pin round-half-to-even (half away from zero or truncation fail)."""
+    with open(os.path.join(GOLDEN, "int8_ties.json")) as f:
+        g = json.load(f)
+    D = g["head_size"]
+    rows = g["rows"]
+    x = np.zeros((len(rows), 1, D), np.float16)
+    for i, r in enumerate(rows):
+        for idx, val, _, _ in r["elements"]:
+            x[i, 0, idx] = np.float16(val)
+    codes, scales = _int8_rows(orc, x)
+    for i, r in enumerate(rows):
+        assert scales[i, 0] == np.float32(r["scale"])
+        want = np.zeros(D, np.int8)
+        for idx, _, code, why in r["elements"]:
+            want[idx] = code
+            assert codes[i, 0, idx] == code, f"row {i} element {idx}: {why}"
+        assert np.array_equal(codes[i, 0], want)
+
+
 def test_int8_attention_matches_sdpa_on_the_dequantised_cache(orc):
     w = wl.custom(num_seqs=4, num_q_heads=8, num_kv_heads=2, head_size=64, q_per_seq=2, kv_dtype="int8",
                   context_lens=[2, 17, 40, 77], seed=42)
