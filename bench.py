@@ -21,8 +21,10 @@ e2e    = the same metric through the public Python API with host buffers: the
          from pinned host memory (one packed copy), and the output copied back,
          inside the timing; copies run on copy streams, double-buffered, and
          overlap the neighbouring steps' kernels as in a serving loop, and the
-         steps are captured once in a CUDA graph (64 per graph) and replayed
+         --steps steps are captured once in a CUDA graph and replayed
          (--no-graph: direct calls).
+per_config = the decode op of each other workload (8b_fp8, 8b_int8, long,
+         70b_spec, mixed), timed in the same run with CUDA events.
 Several KV pools are rotated so that one cycle touches more than 4x the L2.
 
 Multi-GPU: replicas only. Each rank runs the same workload on its own GPU;
@@ -37,6 +39,7 @@ import math
 import os
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -102,8 +105,8 @@ class ClockSampler:
         self.path = None
 
     def start(self):
-        os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        fd, self.path = tempfile.mkstemp(prefix="pkv_clocks_", suffix=".csv")
+        os.close(fd)
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
@@ -121,7 +124,10 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        return summarize_clocks(open(self.path).read().splitlines())
+        with open(self.path) as f:
+            lines = f.read().splitlines()
+        os.unlink(self.path)
+        return summarize_clocks(lines)
 
 
 def summarize_clocks(lines):
@@ -208,6 +214,130 @@ def profiled_traffic(config: str):
 # our implementation
 # ---------------------------------------------------------------------------------
 
+def l2_bytes(dev=None) -> int:
+    """L2 size of the device (the GB300's when no device is visible)."""
+    if dev is not None or torch.cuda.is_available():
+        props = torch.cuda.get_device_properties(dev if dev is not None else 0)
+        return int(getattr(props, "L2_cache_size", 126 << 20))
+    return 126 << 20
+
+
+def pool_count(w, l2: int, pools_arg: int = 0) -> int:
+    """KV pools rotated so that one cycle touches more than 4x the L2."""
+    return pools_arg or max(2, math.ceil(4 * l2 / w.kv_bytes_read()))
+
+
+def bench_config(w, pools: int, l2: int, world: int) -> dict:
+    """The `config` object of the JSON line (identical in both arms)."""
+    return {**w.describe(), "l2_policy": f"{pools} KV pools rotated, "
+            f"{pools * w.kv_bytes_read() / 1e9:.2f} GB per cycle > 4x L2 ({l2 / 1e6:.0f} MB)",
+            "parallelism": f"replicas x{world}"}
+
+
+class Prepared:
+    """One workload resident on the device: `pools` prefilled KV caches, the step's
+    new tokens, block table, lengths, and per-pool query/output buffers."""
+
+    def __init__(self, w, dev, pools: int):
+        import paged_kv_cache_252_gb300 as pkv
+        from paged_kv_cache_252_gb300 import workloads as wl
+        self.pkv, self.w, self.dev, self.pools = pkv, w, dev, pools
+        self.int8 = w.kv_dtype == "int8"
+        vals = wl.token_values(w, device=dev)
+        self.caches = []   # (k_cache, v_cache[, scales])
+        for _ in range(pools):
+            kc, vc = pkv.alloc_kv_cache(w.num_blocks, w.num_kv_heads, w.head_size, w.kv_dtype, dev)
+            c = (kc, vc) + ((pkv.alloc_kv_scales(w.num_blocks, w.num_kv_heads, dev),) if self.int8 else ())
+            self.write(vals["k_all"], vals["v_all"], vals["slot_all"], c)   # prefill
+            self.caches.append(c)
+        new_idx = vals["new_idx"]
+        self.k_new = vals["k_all"][new_idx].contiguous()
+        self.v_new = vals["v_all"][new_idx].contiguous()
+        self.s_new = vals["slot_all"][new_idx].contiguous()
+        self.bt = torch.from_numpy(w.block_tables).to(dev)
+        self.cl = torch.from_numpy(w.context_lens).to(dev)
+        self.cu = torch.from_numpy(w.cu_q_lens()).to(dev) if w.q_lens is not None else None
+        self.qs = [vals["q"].clone() for _ in range(pools)]
+        self.outs = [torch.empty_like(vals["q"]) for _ in range(pools)]
+        del vals
+        torch.cuda.synchronize(dev)
+        self.kv_bytes = w.kv_bytes_read()
+        self.attn_bytes = self.kv_bytes + w.q_out_bytes()
+        self.step_bytes = self.attn_bytes + w.write_bytes()
+
+    def write(self, kn, vn, sn, c):
+        if self.int8:
+            self.pkv.kv_cache_write_int8(kn, vn, sn, *c)
+        else:
+            self.pkv.kv_cache_write(kn, vn, sn, c[0], c[1])
+
+    def decode(self, o, q, c, bt, cl, cu):
+        w, pkv = self.w, self.pkv
+        if self.int8:
+            pkv.paged_attention_decode_int8(o, q, *c, bt, cl, w.q_per_seq, w.scale)
+        elif cu is not None:
+            pkv.paged_attention_decode_varlen(o, q, cu, c[0], c[1], bt, cl, w.q_per_seq, w.scale)
+        else:
+            pkv.paged_attention_decode(o, q, c[0], c[1], bt, cl, w.q_per_seq, w.scale)
+
+    def step(self, i):
+        """One step: the new tokens' cache write, then decode attention (2 launches)."""
+        p = i % self.pools
+        self.write(self.k_new, self.v_new, self.s_new, self.caches[p])
+        self.decode_pool(p)
+
+    def decode_pool(self, p):
+        self.decode(self.outs[p], self.qs[p], self.caches[p], self.bt, self.cl, self.cu)
+
+    def time_decode(self, n: int) -> float:
+        """Mean seconds per decode launch over n launches (rotating pools), an event
+        pair on the launching stream around each launch."""
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        torch.cuda.synchronize(self.dev)
+        for i in range(n):
+            evs[i][0].record()
+            self.decode_pool(i % self.pools)
+            evs[i][1].record()
+        torch.cuda.synchronize(self.dev)
+        return float(np.mean([a.elapsed_time(b) for a, b in evs])) / 1e3
+
+
+# The other workloads, measured as decode-op timings in the same run.
+PER_CONFIG = ["8b_fp8", "8b_int8", "long", "70b_spec", "mixed"]
+
+
+def measure_per_config(keys, dev, peak, min_launches=50, min_seconds=1.0):
+    """Decode-op time per launch of each workload (CUDA events, at least min_launches
+    launches and about min_seconds of launches each), with the clocks sampled during
+    each timing loop."""
+    from paged_kv_cache_252_gb300 import workloads as wl
+    res = {}
+    l2 = l2_bytes(dev)
+    for key in keys:
+        w = wl.by_name(key)
+        P = Prepared(w, dev, pool_count(w, l2))
+        for i in range(5):
+            P.decode_pool(i % P.pools)
+        est = P.time_decode(20)
+        n = max(min_launches, int(math.ceil(min_seconds / max(est, 1e-6))))
+        n = (n + P.pools - 1) // P.pools * P.pools
+        sampler = ClockSampler(dev.index)
+        sampler.start()
+        t = P.time_decode(n)
+        clocks = sampler.stop()
+        achieved = P.attn_bytes / t / 1e9
+        res[key] = {"workload": w.name, "kv_dtype": w.kv_dtype, "launches": n,
+                    "us_per_launch": round(t * 1e6, 3),
+                    "achieved_gbs": round(achieved, 2), "frac": round(achieved / peak, 4),
+                    "algorithmic_bytes_per_launch": int(P.attn_bytes),
+                    "seq_steps_per_s": round(w.num_seqs / t, 1),
+                    "tokens_per_s": round(w.num_new_tokens / t, 1),
+                    "clocks": clocks}
+        del P
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args, rank, world, local):
     import paged_kv_cache_252_gb300 as pkv
     from paged_kv_cache_252_gb300 import workloads as wl
@@ -216,56 +346,13 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(dev)
     pkv.load_library()
     w = wl.by_name(args.config)
-    vals = wl.token_values(w, device=dev)
-    props = torch.cuda.get_device_properties(dev)
-    l2 = int(getattr(props, "L2_cache_size", 128 << 20))
-    kv_bytes = w.kv_bytes_read()
-    pools = args.pools or max(2, math.ceil(4 * l2 / kv_bytes))
-
-    int8 = w.kv_dtype == "int8"
-
-    def write(kn, vn, sn, c):
-        if int8:
-            pkv.kv_cache_write_int8(kn, vn, sn, *c)
-        else:
-            pkv.kv_cache_write(kn, vn, sn, c[0], c[1])
-
-    caches = []   # (k_cache, v_cache[, scales])
-    for _ in range(pools):
-        kc, vc = pkv.alloc_kv_cache(w.num_blocks, w.num_kv_heads, w.head_size, w.kv_dtype, dev)
-        c = (kc, vc) + ((pkv.alloc_kv_scales(w.num_blocks, w.num_kv_heads, dev),) if int8 else ())
-        write(vals["k_all"], vals["v_all"], vals["slot_all"], c)   # prefill
-        caches.append(c)
-    new_idx = vals["new_idx"]
-    k_new = vals["k_all"][new_idx].contiguous()
-    v_new = vals["v_all"][new_idx].contiguous()
-    s_new = vals["slot_all"][new_idx].contiguous()
-    bt = torch.from_numpy(w.block_tables).to(dev)
-    cl = torch.from_numpy(w.context_lens).to(dev)
-    cu = torch.from_numpy(w.cu_q_lens()).to(dev) if w.q_lens is not None else None
-    qs = [vals["q"].clone() for _ in range(pools)]
-    outs = [torch.empty_like(vals["q"]) for _ in range(pools)]
-    del vals
-    torch.cuda.synchronize(dev)
-
-    def decode(o, q, c, bt_, cl_, cu_):
-        if int8:
-            pkv.paged_attention_decode_int8(o, q, *c, bt_, cl_, w.q_per_seq, w.scale)
-        elif cu_ is not None:
-            pkv.paged_attention_decode_varlen(o, q, cu_, c[0], c[1], bt_, cl_, w.q_per_seq, w.scale)
-        else:
-            pkv.paged_attention_decode(o, q, c[0], c[1], bt_, cl_, w.q_per_seq, w.scale)
-
-    def step(i):
-        p = i % pools
-        write(k_new, v_new, s_new, caches[p])
-        decode(outs[p], qs[p], caches[p], bt, cl, cu)
-
-    step_bytes = kv_bytes + w.q_out_bytes() + w.write_bytes()
-    attn_bytes = kv_bytes + w.q_out_bytes()
+    l2 = l2_bytes(dev)
+    pools = pool_count(w, l2, args.pools)
+    P = Prepared(w, dev, pools)
+    step_bytes, attn_bytes = P.step_bytes, P.attn_bytes
 
     for i in range(args.warmup):
-        step(i)
+        P.step(i)
     torch.cuda.synchronize(dev)
     barrier(world, dev)
 
@@ -276,7 +363,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize(dev)
     e0.record()
     for i in range(args.steps):
-        step(i)
+        P.step(i)
     e1.record()
     torch.cuda.synchronize(dev)
     clocks = sampler.stop() if sampler else None
@@ -286,14 +373,7 @@ def run_ours(args, rank, world, local):
 
     # Decode op alone (one decode launch, split-KV combine fused), per-launch CUDA events on its stream.
     n_r = max(args.steps, 50)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_r)]
-    for i in range(n_r):
-        p = i % pools
-        evs[i][0].record()
-        decode(outs[p], qs[p], caches[p], bt, cl, cu)
-        evs[i][1].record()
-    torch.cuda.synchronize(dev)
-    dec_s = float(np.mean([a.elapsed_time(b) for a, b in evs])) / 1e3
+    dec_s = P.time_decode(n_r)
 
     # End to end through the public API with pinned host buffers, run the way a
     # serving loop runs it: each step's inputs travel in one packed host->device
@@ -303,9 +383,11 @@ def run_ours(args, rank, world, local):
     # inside the timed region.
     e2e = None
     if not args.no_e2e:
-        named = [("q", qs[0]), ("k_new", k_new), ("v_new", v_new), ("s_new", s_new), ("bt", bt), ("cl", cl)]
-        if cu is not None:
-            named.append(("cu", cu))
+        caches, outs, qs = P.caches, P.outs, P.qs
+        named = [("q", qs[0]), ("k_new", P.k_new), ("v_new", P.v_new), ("s_new", P.s_new), ("bt", P.bt),
+                 ("cl", P.cl)]
+        if P.cu is not None:
+            named.append(("cu", P.cu))
         layout, off = [], 0
         for n, t in named:
             nbytes = t.numel() * t.element_size()
@@ -342,8 +424,8 @@ def run_ours(args, rank, world, local):
             comp.wait_event(ready[b])
             if not captured or i >= pools:
                 comp.wait_event(out_done[p])
-            write(v["k_new"], v["v_new"], v["s_new"], caches[p])
-            decode(outs[p], v["q"], caches[p], v["bt"], v["cl"], v.get("cu"))
+            P.write(v["k_new"], v["v_new"], v["s_new"], caches[p])
+            P.decode(outs[p], v["q"], caches[p], v["bt"], v["cl"], v.get("cu"))
             free[b].record(comp)
             with torch.cuda.stream(cs_out):
                 cs_out.wait_event(free[b])
@@ -354,16 +436,15 @@ def run_ours(args, rank, world, local):
             e2e_step(i)
         torch.cuda.synchronize(dev)
         graph = None
+        e2e_steps = args.steps
         if not args.no_graph:
-            # A serving loop replays captured steps: capture `chunk` steps (a multiple
-            # of the buffer and pool periods) once, with the copy streams forked from
-            # and joined back into the capture, and replay it.
-            period = 2 * pools // math.gcd(2, pools)
-            chunk = period * max(1, 64 // period)
+            # A serving loop replays captured steps: the timed steps are captured
+            # once as one graph, with the copy streams forked from and joined back
+            # into the capture, replayed once untimed and once timed.
             cap = torch.cuda.Stream(dev)
             cap.wait_stream(comp)
             with torch.cuda.stream(cap):          # the binding's workspace for this stream, outside the capture
-                decode(outs[0], qs[0], caches[0], bt, cl, cu)
+                P.decode(outs[0], qs[0], caches[0], P.bt, P.cl, P.cu)
             comp.wait_stream(cap)
             torch.cuda.synchronize(dev)
             graph = torch.cuda.CUDAGraph()
@@ -372,25 +453,21 @@ def run_ours(args, rank, world, local):
                 comp = torch.cuda.current_stream(dev)
                 cs_in.wait_stream(comp)
                 cs_out.wait_stream(comp)
-                for i in range(chunk):
+                for i in range(e2e_steps):
                     e2e_step(i, captured=True)
                 comp.wait_stream(cs_in)
                 comp.wait_stream(cs_out)
             comp = comp_outer
-            replays = max(1, -(-args.steps // chunk))
-            e2e_steps = replays * chunk
             graph.replay()
             torch.cuda.synchronize(dev)
         barrier(world, dev)
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a0.record(comp)
         if graph is not None:
-            for _ in range(replays):
-                graph.replay()
+            graph.replay()
         else:
-            e2e_steps = args.steps
             cs_in.wait_stream(comp)   # the first upload starts inside the timed region
-            for i in range(args.steps):
+            for i in range(e2e_steps):
                 e2e_step(i)
             comp.wait_stream(cs_in)
             comp.wait_stream(cs_out)  # the last outputs are back on the host
@@ -402,12 +479,18 @@ def run_ours(args, rank, world, local):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": round(e2e_el / e2e_steps * 1e3, 5), "steps": e2e_steps,
                "copies": "one packed H2D and one D2H per step on copy streams, double-buffered",
-               "launch": (f"CUDA graph of {chunk} steps, replayed {replays} times" if graph is not None
+               "launch": (f"CUDA graph of the {e2e_steps} steps, replayed once" if graph is not None
                           else "direct calls")}
 
+    peak, peak_kind = measured_peaks()
+    per_config = None
+    if not args.no_per_config and world == 1:
+        keys = [k for k in PER_CONFIG if k != args.config]
+        del P
+        torch.cuda.empty_cache()
+        per_config = measure_per_config(keys, dev, peak)
     if rank != 0:
         return
-    peak, peak_kind = measured_peaks()
     achieved = attn_bytes / dec_s / 1e9
     cpu = None if (args.no_cpu_baseline or world > 1) else cpu_baseline(w, args.cpu_budget_s)
     value = job_bytes / job_elapsed / 1e9
@@ -426,9 +509,7 @@ def run_ours(args, rank, world, local):
         "vs_baseline": None,
         "dtype": dtype,
         "data": "synthetic (seeded N(0,1) K/V/q, shuffled block pool)",
-        "config": {**w.describe(), "l2_policy": f"{pools} KV pools rotated, "
-                   f"{pools * kv_bytes / 1e9:.2f} GB per cycle > 4x L2 ({l2 / 1e6:.0f} MB)",
-                   "parallelism": f"replicas x{world}"},
+        "config": bench_config(w, pools, l2, world),
         "seq_steps_per_s": round(w.num_seqs * world * args.steps / job_elapsed, 1),
         "tokens_per_s": round(w.num_new_tokens * world * args.steps / job_elapsed, 1),
         "pct_of_hbm_peak": round(100 * value / peak, 2),
@@ -437,11 +518,13 @@ def run_ours(args, rank, world, local):
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,
                      "traffic": profiled_traffic(args.config),
                      "algorithmic_bytes_per_launch": int(attn_bytes),
-                     "us_per_launch": round(dec_s * 1e6, 3)},
+                     "us_per_launch": round(dec_s * 1e6, 3), "launches_timed": n_r},
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        # per step: the cache write and the decode, one launch each
+        "gpu_launches": 2 * args.steps,
         "clocks": clocks,
         "cpu_baseline": cpu,
+        "per_config": per_config,
     }
     print(json.dumps(line), flush=True)
 
@@ -565,7 +648,7 @@ def run_reference(args, rank, world, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1) K/V/q, shuffled block pool)",
-        "config": {**w.describe(), "parallelism": "cpu oracle"},
+        "config": bench_config(w, pool_count(w, l2_bytes()), l2_bytes(), world),
         "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": f"{len(seqs)} of {w.num_seqs} sequences per step"},
         "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -586,6 +669,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="e2e by direct calls instead of graph replays")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the decode-op timings of the other workloads")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -63,3 +63,17 @@ def test_clock_summary():
 def test_warmup_floor():
     with pytest.raises(SystemExit):
         bench.main(["--warmup", "2"])
+
+
+def test_reference_arm_reports_the_same_config():
+    """Both arms describe the workload with one function, so their `config`
+    objects are identical for the same workload, L2 size and rank count."""
+    from paged_kv_cache_252_gb300 import workloads as wl
+    for key in ("8b", "70b_spec", "long"):
+        w = wl.by_name(key)
+        l2 = 126 << 20
+        pools = bench.pool_count(w, l2)
+        assert pools >= 2 and pools * w.kv_bytes_read() > 4 * l2
+        a = bench.bench_config(w, pools, l2, 1)
+        b = bench.bench_config(wl.by_name(key), bench.pool_count(wl.by_name(key), l2), l2, 1)
+        assert a == b and a["workload"] == w.name and "l2_policy" in a
