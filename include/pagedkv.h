@@ -15,7 +15,9 @@
  * Conventions for every call
  *   - All pointers are DEVICE pointers unless stated otherwise. The caller owns
  *     every buffer; the library allocates no device memory and keeps no state
- *     besides a per-device cache of device properties.
+ *     besides a per-device cache of device properties and kernel attributes,
+ *     filled on first use. cudaDeviceReset discards what that cache describes:
+ *     do not call the library on a device after resetting it in the same process.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream). Calls are
  *     asynchronous: they enqueue kernels and return.
  *   - Return value: PKV_OK (0) or a negative pkv_status. Arguments are checked on
@@ -129,6 +131,11 @@ size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t
  *                 calls in flight at the same time must not share a workspace.
  *                 A call may be captured in a CUDA graph and replayed: every
  *                 launch leaves the workspace's counters clear when it completes.
+ *                 The counters are tagged with a per-call number, so counters
+ *                 left by an earlier call read as clear; a replayed graph reuses
+ *                 its call's number, so after a launch that reported
+ *                 PKV_DEV_TIMEOUT (its counters may be left part-way) zero the
+ *                 workspace (e.g. cudaMemsetAsync) before replaying that graph.
  *
  *   For each sequence s, query head hq (KV head h = hq / (num_q_heads/num_kv_heads))
  *   and query token j, with L = context_lens[s] - q_per_seq + j + 1:
@@ -219,16 +226,21 @@ int pkv_paged_attention_decode_tree(void* out, const void* q, const int32_t* cu_
  *   - Limit: a problem whose pkv_decode_workspace_bytes(...) exceeds
  *     PKV_NOALLOC_SCRATCH_BYTES is rejected with PKV_ERR_WORKSPACE_TOO_SMALL
  *     before anything is launched (use pkv_paged_attention_decode with your own
- *     workspace for it).
+ *     workspace for it). Arguments the regular entry point refuses get the
+ *     status it returns for them.
  *   - The buffer occupies PKV_NOALLOC_SCRATCH_BYTES of device memory on every
  *     device where the library's module holding it is loaded, until the process
  *     exits.
  *   - The first call on a device looks up the buffer's device address (with
  *     that device current); make that first call before any stream capture.
  *   - Every call shares the one buffer and keeps the previous call's contents
- *     in it (nothing in it needs to start at zero). Calls whose kernels overlap
- *     on the GPU (different streams, or concurrent host threads) race on it;
- *     serialise them.
+ *     in it. Partial results are rewritten by each call; the split-KV counters
+ *     start at zero when the module loads and are tagged with each call's
+ *     number, so a counter an earlier call left behind (even one that reported
+ *     PKV_DEV_TIMEOUT) reads as clear. Calls whose kernels overlap on the GPU
+ *     (different streams, or concurrent host threads) race on it; serialise them.
+ *   - The address is looked up once per device and kept (see cudaDeviceReset
+ *     above).
  */
 #define PKV_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 

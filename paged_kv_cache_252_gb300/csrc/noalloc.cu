@@ -16,6 +16,7 @@
 // cudaGetSymbolAddress while that device is current, and later calls reuse it.
 #include <cuda_runtime.h>
 
+#include <cstdint>
 #include <mutex>
 
 #include "pagedkv.h"
@@ -69,13 +70,25 @@ extern "C" int pkv_paged_attention_decode_noalloc(void* out, const void* q, int3
                                       context_lens, scale, nullptr, 0, device_status, stream);
   }
   const size_t need = pkv_decode_workspace_bytes(num_seqs, num_q_heads, q_per_seq, cache);
-  if (need == 0) return PKV_ERR_INVALID_ARGUMENT;
+  if (need == 0) {
+    // The shape was refused (invalid, unsupported, or no device). Let the regular
+    // entry point's host checks pick the status it would return: it is given a
+    // workspace of 0 bytes, so it returns before any launch whatever the outcome
+    // (the stand-in pointer is never dereferenced).
+    return pkv_paged_attention_decode(out, q, num_seqs, num_q_heads, q_per_seq, k_cache, v_cache,
+                                      kv_dtype, cache, block_tables, max_blocks_per_seq, context_lens,
+                                      scale, reinterpret_cast<void*>(static_cast<uintptr_t>(256)), 0,
+                                      device_status, stream);
+  }
   // The problem needs more scratch than the built-in buffer holds.
   if (need > kScratchBytes) return PKV_ERR_WORKSPACE_TOO_SMALL;
   void* scratch = nullptr;
   if (int rc = scratch_for_current_device(&scratch)) return rc;
-  // The decode path writes every scratch word it later reads (unit descriptors
-  // and partial results), so nothing in the buffer has to start at zero.
+  // Partial results are written before they are read. The split-KV piece
+  // counters are not: they are read and bumped with atomics, and stay correct
+  // because each is tagged with the call's epoch (a counter left by an earlier
+  // call reads as zero), the array starts zeroed when the module loads, and the
+  // CTA that completes a unit puts its counter back to zero.
   return pkv_paged_attention_decode(out, q, num_seqs, num_q_heads, q_per_seq, k_cache, v_cache,
                                     kv_dtype, cache, block_tables, max_blocks_per_seq, context_lens,
                                     scale, scratch, kScratchBytes, device_status, stream);
