@@ -282,6 +282,27 @@ int pkv_paged_attention_decode_int8(void* out, const void* q, int32_t num_seqs, 
                                     float scale, void* workspace, size_t workspace_bytes,
                                     int32_t* device_status, void* stream);
 
+/* The mixed-batch and token-tree calls over an INT8 cache: arguments as for
+ * pkv_paged_attention_decode_varlen and pkv_paged_attention_decode_tree (q and
+ * out fp16), plus the cache's row scales as for pkv_paged_attention_decode_int8.
+ * A batch that mixes plain decode rows and verify rows ("nopadding" packed
+ * tokens, Continuous Batching section of the Colossal-Inference release page)
+ * over the INT8 cache of the LMDeploy section of the inference-framework survey. */
+int pkv_paged_attention_decode_int8_varlen(void* out, const void* q, const int32_t* cu_q_lens,
+                                           int32_t num_q_rows, int32_t num_seqs, int32_t num_q_heads,
+                                           int32_t max_q_per_seq, const void* k_cache, const void* v_cache,
+                                           const float* scales, const pkv_cache_desc* cache,
+                                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                           const int32_t* context_lens, float scale, void* workspace,
+                                           size_t workspace_bytes, int32_t* device_status, void* stream);
+int pkv_paged_attention_decode_int8_tree(void* out, const void* q, const int32_t* cu_q_lens,
+                                         const uint64_t* tree_masks, int32_t num_q_rows, int32_t num_seqs,
+                                         int32_t num_q_heads, int32_t max_q_per_seq, const void* k_cache,
+                                         const void* v_cache, const float* scales, const pkv_cache_desc* cache,
+                                         const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                         const int32_t* context_lens, float scale, void* workspace,
+                                         size_t workspace_bytes, int32_t* device_status, void* stream);
+
 /* ==== Block pool (host side) =================================================
  *
  * "AI 大模型推理优化技术详解", 2.1.2 Paged Attention: each sequence's KV cache is

@@ -40,13 +40,15 @@ def library_path() -> str:
     return os.path.join(_HERE, "libpagedkv.so")
 
 
-def load_library():
-    """Load libpagedkv.so (built in-tree by ``__graft_entry__.build()``)."""
+def load_library(path: str | None = None):
+    """Load libpagedkv.so (built in-tree by ``__graft_entry__.build()``). A profiling
+    tool may pass the path of a variant build of the same library instead; the
+    first load wins for the rest of the process."""
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
-        path = library_path()
+        path = path or library_path()
         if not os.path.exists(path):
             raise PagedKVError(f"{path} is missing: build the CUDA library first "
                                "(python -c 'import __graft_entry__ as g; g.build()')")
@@ -107,6 +109,14 @@ def load_library():
             vp, vp, i32, i32, i32, vp, vp, vp, P(_CacheDesc), vp, i32, vp, ctypes.c_float, vp,
             ctypes.c_size_t, vp, vp]
         lib.pkv_paged_attention_decode_int8.restype = ctypes.c_int
+        lib.pkv_paged_attention_decode_int8_varlen.argtypes = [
+            vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, P(_CacheDesc), vp, i32, vp, ctypes.c_float, vp,
+            ctypes.c_size_t, vp, vp]
+        lib.pkv_paged_attention_decode_int8_varlen.restype = ctypes.c_int
+        lib.pkv_paged_attention_decode_int8_tree.argtypes = [
+            vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, P(_CacheDesc), vp, i32, vp, ctypes.c_float, vp,
+            ctypes.c_size_t, vp, vp]
+        lib.pkv_paged_attention_decode_int8_tree.restype = ctypes.c_int
         lib.pkv_error_string.argtypes = [ctypes.c_int]
         lib.pkv_error_string.restype = ctypes.c_char_p
         lib.pkv_version.restype = ctypes.c_int
@@ -373,12 +383,22 @@ def paged_attention_decode_noalloc(out, q, k_cache, v_cache, block_tables, conte
     return out
 
 
+def _int8_scales(code, k_cache, scales):
+    """An INT8 cache is read with its row scales; other caches take none."""
+    if (code == KV_INT8) != (scales is not None):
+        raise PagedKVError("an INT8 cache is read with its scales (alloc_kv_scales); other caches take none")
+    if scales is not None:
+        _need_cuda_contig("scales", scales)
+        _scales_shape(k_cache, scales)
+
+
 def paged_attention_decode_varlen(out, q, cu_q_lens, k_cache, v_cache, block_tables, context_lens,
-                                  max_q_per_seq: int, scale: float, kv_dtype=None, *,
+                                  max_q_per_seq: int, scale: float, kv_dtype=None, *, scales=None,
                                   workspace=None, device_status=None, stream=None):
     """Decode attention for a batch whose sequences carry different numbers of query
     tokens, packed without padding: sequence s owns rows cu_q_lens[s]..cu_q_lens[s+1]-1
-    of q/out ([total_rows, Hq, D]), 1 <= n_s <= max_q_per_seq, causal among its tokens."""
+    of q/out ([total_rows, Hq, D]), 1 <= n_s <= max_q_per_seq, causal among its tokens.
+    An INT8 cache takes its row scales (``scales``)."""
     for nm, t in (("out", out), ("q", q), ("cu_q_lens", cu_q_lens), ("k_cache", k_cache),
                   ("v_cache", v_cache), ("block_tables", block_tables), ("context_lens", context_lens)):
         _need_cuda_contig(nm, t)
@@ -391,29 +411,38 @@ def paged_attention_decode_varlen(out, q, cu_q_lens, k_cache, v_cache, block_tab
                           max_rows=int(context_lens.shape[0]) * int(max_q_per_seq))
     if cu_q_lens.dim() != 1 or int(cu_q_lens.shape[0]) != S + 1:
         raise PagedKVError("cu_q_lens must have num_seqs + 1 entries")
+    code = _kv_code(kv_dtype, k_cache)
+    _int8_scales(code, k_cache, scales)
     Hq = int(q.shape[1])
     lib = load_library()
     with _on_device(q.device):
         need = _ws_bytes(lib, q.device, S, Hq, int(max_q_per_seq), d)
         if workspace is None:
             workspace = _workspace(need, q.device)
-        rc = lib.pkv_paged_attention_decode_varlen(
-            _ptr(out), _ptr(q), _ptr(cu_q_lens), int(q.shape[0]), S, Hq, int(max_q_per_seq), _ptr(k_cache),
-            _ptr(v_cache), _kv_code(kv_dtype, k_cache), ctypes.byref(d), _ptr(block_tables),
-            int(block_tables.shape[1]), _ptr(context_lens), float(scale), _ptr(workspace),
-            int(workspace.numel() * workspace.element_size()), _ptr(device_status),
-            _stream_handle(stream, q.device))
+        ws = (_ptr(workspace), int(workspace.numel() * workspace.element_size()))
+        if code == KV_INT8:
+            rc = lib.pkv_paged_attention_decode_int8_varlen(
+                _ptr(out), _ptr(q), _ptr(cu_q_lens), int(q.shape[0]), S, Hq, int(max_q_per_seq),
+                _ptr(k_cache), _ptr(v_cache), _ptr(scales), ctypes.byref(d), _ptr(block_tables),
+                int(block_tables.shape[1]), _ptr(context_lens), float(scale), *ws, _ptr(device_status),
+                _stream_handle(stream, q.device))
+        else:
+            rc = lib.pkv_paged_attention_decode_varlen(
+                _ptr(out), _ptr(q), _ptr(cu_q_lens), int(q.shape[0]), S, Hq, int(max_q_per_seq),
+                _ptr(k_cache), _ptr(v_cache), code, ctypes.byref(d), _ptr(block_tables),
+                int(block_tables.shape[1]), _ptr(context_lens), float(scale), *ws, _ptr(device_status),
+                _stream_handle(stream, q.device))
     _check(rc, "paged_attention_decode_varlen")
     return out
 
 
 def paged_attention_decode_tree(out, q, tree_masks, k_cache, v_cache, block_tables, context_lens,
                                 max_q_per_seq: int, scale: float, kv_dtype=None, *, cu_q_lens=None,
-                                workspace=None, device_status=None, stream=None):
+                                scales=None, workspace=None, device_status=None, stream=None):
     """Speculative verify of a token tree: tree_masks (int64/uint64, one per query row)
     bit i lets a query token attend to its sequence's draft token i; the context before
     the drafts is always visible. cu_q_lens as for paged_attention_decode_varlen, or
-    None for max_q_per_seq tokens per sequence."""
+    None for max_q_per_seq tokens per sequence. An INT8 cache takes its row scales."""
     for nm, t in (("out", out), ("q", q), ("tree_masks", tree_masks), ("k_cache", k_cache),
                   ("v_cache", v_cache), ("block_tables", block_tables), ("context_lens", context_lens)):
         _need_cuda_contig(nm, t)
@@ -432,18 +461,27 @@ def paged_attention_decode_tree(out, q, tree_masks, k_cache, v_cache, block_tabl
             raise PagedKVError("cu_q_lens must be int32 with num_seqs + 1 entries")
     if tree_masks.dim() != 1 or int(tree_masks.shape[0]) != int(q.shape[0]):
         raise PagedKVError("tree_masks must hold one mask per query row")
+    code = _kv_code(kv_dtype, k_cache)
+    _int8_scales(code, k_cache, scales)
     Hq = int(q.shape[1])
     lib = load_library()
     with _on_device(q.device):
         need = _ws_bytes(lib, q.device, S, Hq, int(max_q_per_seq), d)
         if workspace is None:
             workspace = _workspace(need, q.device)
-        rc = lib.pkv_paged_attention_decode_tree(
-            _ptr(out), _ptr(q), _ptr(cu_q_lens), _ptr(tree_masks), int(q.shape[0]), S, Hq, int(max_q_per_seq),
-            _ptr(k_cache), _ptr(v_cache), _kv_code(kv_dtype, k_cache), ctypes.byref(d),
-            _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens), float(scale),
-            _ptr(workspace), int(workspace.numel() * workspace.element_size()),
-            _ptr(device_status), _stream_handle(stream, q.device))
+        ws = (_ptr(workspace), int(workspace.numel() * workspace.element_size()))
+        if code == KV_INT8:
+            rc = lib.pkv_paged_attention_decode_int8_tree(
+                _ptr(out), _ptr(q), _ptr(cu_q_lens), _ptr(tree_masks), int(q.shape[0]), S, Hq,
+                int(max_q_per_seq), _ptr(k_cache), _ptr(v_cache), _ptr(scales), ctypes.byref(d),
+                _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens), float(scale), *ws,
+                _ptr(device_status), _stream_handle(stream, q.device))
+        else:
+            rc = lib.pkv_paged_attention_decode_tree(
+                _ptr(out), _ptr(q), _ptr(cu_q_lens), _ptr(tree_masks), int(q.shape[0]), S, Hq,
+                int(max_q_per_seq), _ptr(k_cache), _ptr(v_cache), code, ctypes.byref(d),
+                _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens), float(scale), *ws,
+                _ptr(device_status), _stream_handle(stream, q.device))
     _check(rc, "paged_attention_decode_tree")
     return out
 

@@ -40,6 +40,10 @@ DeviceState g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 std::atomic<uint32_t> g_call_epoch{0};
+#ifdef PKV_TIMELINE
+unsigned long long* g_timeline = nullptr;   // profiling build: per-CTA event buffer
+int g_timeline_ctas = 0;
+#endif
 
 // Fixed cost of one unit piece on the work line, in KV blocks: the piece's
 // query load, epilogue and (when split) merge take about as long as streaming
@@ -241,6 +245,18 @@ cudaError_t launch(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStrea
 
 extern "C" {
 
+#ifdef PKV_TIMELINE
+// Profiling build only (not part of the public header): decode launches after
+// this call record per-CTA event times into buf ([max_ctas][8] uint64, device
+// memory owned by the caller; NULL detaches). See pkv_timeline.cuh.
+int pkv_timeline_attach(unsigned long long* buf, int32_t max_ctas) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_timeline = max_ctas > 0 ? buf : nullptr;
+  g_timeline_ctas = buf ? max_ctas : 0;
+  return PKV_OK;
+}
+#endif
+
 int pkv_version(void) { return 100; }
 
 const char* pkv_error_string(int code) {
@@ -439,6 +455,10 @@ int decode_impl(void* out, const void* q, const int32_t* cu_q_lens, int32_t num_
   if (ep == 0) ep = ++g_call_epoch;
   a.epoch = ep;
   a.piece_cost = piece_cost(g.tc != 0, kv_dtype);
+#ifdef PKV_TIMELINE
+  a.timeline = g_timeline;
+  a.timeline_ctas = g_timeline_ctas;
+#endif
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   void* dargs[5] = {&tmk, &tmv, &tmk1, &tmv1, &a};
@@ -511,6 +531,33 @@ int pkv_paged_attention_decode_int8(void* out, const void* q, int32_t num_seqs, 
                      q_per_seq, k_cache,
                      v_cache, PKV_INT8, cache, block_tables, max_blocks_per_seq, context_lens, scale, workspace,
                      workspace_bytes, device_status, stream);
+}
+
+int pkv_paged_attention_decode_int8_varlen(void* out, const void* q, const int32_t* cu_q_lens,
+                                           int32_t num_q_rows, int32_t num_seqs, int32_t num_q_heads,
+                                           int32_t max_q_per_seq, const void* k_cache, const void* v_cache,
+                                           const float* scales, const pkv_cache_desc* cache,
+                                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                           const int32_t* context_lens, float scale, void* workspace,
+                                           size_t workspace_bytes, int32_t* device_status, void* stream) {
+  if (num_seqs > 0 && !cu_q_lens) return PKV_ERR_INVALID_ARGUMENT;
+  return decode_impl(out, q, cu_q_lens, num_q_rows, nullptr, scales, num_seqs, num_q_heads, max_q_per_seq,
+                     k_cache, v_cache, PKV_INT8, cache, block_tables, max_blocks_per_seq, context_lens, scale,
+                     workspace, workspace_bytes, device_status, stream);
+}
+
+int pkv_paged_attention_decode_int8_tree(void* out, const void* q, const int32_t* cu_q_lens,
+                                         const uint64_t* tree_masks, int32_t num_q_rows, int32_t num_seqs,
+                                         int32_t num_q_heads, int32_t max_q_per_seq, const void* k_cache,
+                                         const void* v_cache, const float* scales, const pkv_cache_desc* cache,
+                                         const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                         const int32_t* context_lens, float scale, void* workspace,
+                                         size_t workspace_bytes, int32_t* device_status, void* stream) {
+  if (num_seqs > 0 && !tree_masks) return PKV_ERR_INVALID_ARGUMENT;
+  if (max_q_per_seq > 64) return PKV_ERR_UNSUPPORTED;
+  return decode_impl(out, q, cu_q_lens, num_q_rows, reinterpret_cast<const unsigned long long*>(tree_masks),
+                     scales, num_seqs, num_q_heads, max_q_per_seq, k_cache, v_cache, PKV_INT8, cache, block_tables,
+                     max_blocks_per_seq, context_lens, scale, workspace, workspace_bytes, device_status, stream);
 }
 
 int pkv_kv_cache_write_int8(const void* key, const void* value, int32_t num_tokens, const int32_t* slot_mapping,

@@ -100,3 +100,17 @@ def test_cache_write_and_int8_shapes(stub):
     with pytest.raises(api.PagedKVError):   # scales of another pool size
         api.paged_attention_decode_int8(c["out"], c["q"], c["k_cache"], c["v_cache"], sc,
                                         c["block_tables"], c["context_lens"], 2, 0.125)
+
+
+def test_int8_scales_go_with_an_int8_cache_only():
+    """The varlen and tree calls take scales exactly when the cache is INT8 (checked
+    before anything reaches the library)."""
+    import paged_kv_cache_252_gb300 as pkv
+    import pytest as _pt
+    q = torch.zeros(2, 4, 64, dtype=torch.float16)
+    kc8 = torch.zeros(4, 2, 16, 64, dtype=torch.int8)
+    with _pt.raises(pkv.PagedKVError):
+        pkv.api._int8_scales(pkv.api.KV_INT8, kc8, None)
+    with _pt.raises(pkv.PagedKVError):
+        pkv.api._int8_scales(pkv.api.KV_FP16, kc8, torch.zeros(4, 2, 2, 16))
+    pkv.api._int8_scales(pkv.api.KV_FP16, kc8, None)

@@ -160,3 +160,91 @@ def test_int8_bad_block_is_flagged_not_faulted(orc, dev, gpu):
     ref, _, _ = orc.paged_attention(bits16(vals["q"]), 0, 1, okc, ovc, 3, w.block_tables, w.context_lens,
                                     w.scale, seqs=[1, 2], k_scale=oks, v_scale=ovs)
     gpu.compare(out, ref, rows=[1, 2])
+
+
+# ------------------------------------------------------------------------------------
+# INT8 cache under the mixed-batch (per-sequence query counts) and token-tree calls
+# ------------------------------------------------------------------------------------
+
+def _check_packed(orc, gpu, w, dev, *, tree_masks=None, values_device="cpu"):
+    """Varlen (w.q_lens set) or token-tree decode over an INT8 cache against the oracle
+    on the same codes and scales."""
+    import paged_kv_cache_252_gb300 as pkv
+    vals = wl.token_values(w, device=values_device)
+    kc, vc, sc = _gpu_caches(w, vals, dev)
+    q = vals["q"].to(dev)
+    out = torch.full_like(q, float("nan"))
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    cl = torch.from_numpy(w.context_lens).to(dev)
+    cu = torch.from_numpy(w.cu_q_lens()).to(dev) if w.q_lens is not None else None
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    if tree_masks is None:
+        pkv.paged_attention_decode_varlen(out, q, cu, kc, vc, bt, cl, w.q_per_seq, w.scale, scales=sc,
+                                          device_status=status)
+    else:
+        tm = torch.from_numpy(tree_masks.view(np.int64)).to(dev)
+        pkv.paged_attention_decode_tree(out, q, tm, kc, vc, bt, cl, w.q_per_seq, w.scale, cu_q_lens=cu,
+                                        scales=sc, device_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ks, vs = _split_scales(sc)
+    vals = {k: v.cpu() for k, v in vals.items()}
+    okc, ovc, oks, ovs = _oracle_caches(orc, w, vals)
+    assert np.array_equal(kc.cpu().numpy(), okc) and np.array_equal(vc.cpu().numpy(), ovc)
+    assert np.array_equal(ks, oks) and np.array_equal(vs, ovs)
+    ref, _, rc = orc.paged_attention(bits16(vals["q"]), 0, w.q_per_seq, okc, ovc, 3, w.block_tables,
+                                     w.context_lens, w.scale, num_threads=orc.hardware_threads(),
+                                     cu_q_lens=w.cu_q_lens(), tree_masks=tree_masks, k_scale=oks, v_scale=ovs)
+    assert rc == 0
+    kind = "varlen" if tree_masks is None else "tree"
+    return gpu.compare(out, ref, label=f"{w.name} int8 {kind} D{w.head_size} G{w.group} n<={w.q_per_seq}")
+
+
+INT8_VARLEN = [
+    # (D, Hq, Hkv, q_lens)
+    (128, 32, 8, [1, 4, 1, 1, 4, 2, 1, 3]),
+    (64, 16, 4, [2, 1, 4, 1, 1, 3]),
+    (128, 64, 8, [4, 1, 2, 4, 1]),
+    (64, 8, 1, [1, 8, 3, 1, 5, 2]),
+]
+
+
+@pytest.mark.parametrize("case", INT8_VARLEN, ids=[f"D{c[0]}-G{c[1] // c[2]}" for c in INT8_VARLEN])
+def test_int8_varlen_parity(orc, dev, gpu, case):
+    D, Hq, Hkv, q_lens = case
+    lens = [max(l, ql) for l, ql in zip([1, 17, 300, 16, 64, 1000, 33, 129], q_lens)]
+    w = wl.custom(num_seqs=len(q_lens), num_q_heads=Hq, num_kv_heads=Hkv, head_size=D,
+                  q_per_seq=max(q_lens), kv_dtype="int8", context_lens=lens, seed=3300 + D + Hq,
+                  q_lens=q_lens)
+    _check_packed(orc, gpu, w, dev)
+
+
+INT8_TREES = [
+    # (D, Hq, Hkv, q_lens or uniform n)
+    (128, 64, 8, 4),
+    (128, 32, 8, [5, 1, 8, 3, 2]),
+    (64, 8, 4, [16, 3, 9]),
+]
+
+
+@pytest.mark.parametrize("case", INT8_TREES, ids=[f"D{c[0]}-G{c[1] // c[2]}" for c in INT8_TREES])
+def test_int8_tree_verify_parity(orc, dev, gpu, case):
+    D, Hq, Hkv, ql = case
+    S = 5 if isinstance(ql, int) else len(ql)
+    q_lens = [ql] * S if isinstance(ql, int) else ql
+    lens = [max(l, n) for l, n in zip([20, 1, 300, 33, 1200], q_lens)]
+    w = wl.custom(num_seqs=S, num_q_heads=Hq, num_kv_heads=Hkv, head_size=D, q_per_seq=max(q_lens),
+                  kv_dtype="int8", context_lens=lens, seed=3500 + D,
+                  q_lens=None if isinstance(ql, int) else q_lens)
+    _check_packed(orc, gpu, w, dev, tree_masks=wl.random_tree_masks(q_lens, seed=13 + D))
+
+
+def test_int8_mixed_workload_full_size(orc, dev, gpu):
+    """The mixed decode/verify batch of the 8B layer (1 or 4 query tokens per
+    sequence) over an INT8 cache, every output element."""
+    m = wl.by_name("mixed")
+    w = wl.make_workload("mixed_8b_decode_verify_int8", num_seqs=m.num_seqs, num_q_heads=m.num_q_heads,
+                         num_kv_heads=m.num_kv_heads, head_size=m.head_size, q_per_seq=m.q_per_seq,
+                         kv_dtype="int8", scale=m.scale, seed=m.seed, context_lens=m.context_lens,
+                         q_lens=m.q_lens)
+    _check_packed(orc, gpu, w, dev, values_device=dev)
