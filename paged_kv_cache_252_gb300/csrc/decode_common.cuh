@@ -19,6 +19,7 @@
 
 #include "pkv_internal.h"
 #include "pkv_ptx.cuh"
+#include "pkv_timeline.cuh"
 
 namespace pkv {
 
@@ -129,75 +130,42 @@ __device__ inline void plan_cta_share(const DecodeArgs& a, long long* red, long 
   __syncthreads();
 }
 
-// After this CTA wrote its piece of unit u to slot (u + cta): count the piece on
-// the unit's counter; the CTA that finishes the last piece merges all pieces
-// into the output. Called by the nthr threads that wrote the slot (tid in
-// [0, nthr)), which synchronise on named barrier bar_id. ustart is the line
-// position of the unit's first block, nb its block count, Rs its real rows, qb its first query
-// row. Counters are tagged with the call's epoch, so no workspace clearing is
-// needed, and the CTA that completes a unit clears its counter, so a replayed
-// CUDA graph (same epoch every replay) starts from clear counters too.
+// Merge the pieces of unit u into its output rows: M = max m, L = sum l 2^(m-M),
+// out = sum o 2^(m-M) / L over the pieces of CTAs c_first..c_last, in that order,
+// accumulated online. Each piece comes from its workspace slot (unit + cta),
+// except that when own_o is not null the piece of CTA c_first (this CTA) is read
+// from shared memory (o at own_o[r * own_stride + d], m and l at own_ml[r] and
+// own_ml[rows + r]) -- the same values its slot would hold, combined in the same
+// order, so either way gives the same output bits. A thread reads four slots per
+// step, so their loads are in flight together instead of one round trip per slot.
 template <int KV, int D>
-__device__ inline void finish_split_piece(const DecodeArgs& a, int u, long long ustart, int nb,
-                                          long long total, long long ncta, int Rs, int qb, int h,
-                                          int tid, int nthr, int bar_id, volatile int* fin) {
+__device__ inline void merge_split_pieces(const DecodeArgs& a, int u, int c_first, int c_last,
+                                          const float* own_o, int own_stride, const float* own_ml,
+                                          int Rs, int qb, int h, int tid, int nthr) {
   constexpr float kNegInf = -INFINITY;
   const int R = a.rows, G = a.group, Hq = a.num_q_heads;
-  // The barrier orders every thread's slot writes before thread 0's device-scope
-  // release fence, which makes them visible before the counter update; the CTA
-  // that sees the final count acquires the other CTAs' slots through the same
-  // fence after its atomic.
-  named_bar_sync(bar_id, nthr);
-  if (tid == 0) {
-    fence_acq_rel_gpu();
-    const long long nact = active_ctas(ncta, total, a.piece_cost);
-    const int c_first = position_owner(ustart, nact, total);
-    const int c_last = position_owner(ustart + nb - 1, nact, total);
-    unsigned long long* ctr = a.piece_counts + u;
-    unsigned long long cur = atomicAdd(ctr, 0ull);
-    unsigned long long want;
-    for (;;) {
-      want = (static_cast<uint32_t>(cur >> 32) == a.epoch)
-                 ? cur + 1ull
-                 : ((static_cast<unsigned long long>(a.epoch) << 32) | 1ull);
-      const unsigned long long prev = atomicCAS(ctr, cur, want);
-      if (prev == cur) break;
-      cur = prev;
-    }
-    const bool last = static_cast<int>(want & 0xffffffffull) == c_last - c_first + 1;
-    fin[0] = last ? 1 : 0;
-    fin[1] = c_first;
-    fin[2] = c_last;
-    if (last) {
-      // No other CTA touches this counter again in this launch. Leave it at 0
-      // (epoch 0 is never issued, so 0 reads as "no pieces" for any later call):
-      // a replayed CUDA graph reuses its epoch and must find the counters clear.
-      *ctr = 0ull;
-      fence_acq_rel_gpu();   // acquire: the other CTAs' slots are read next
-    }
-  }
-  named_bar_sync(bar_id, nthr);
-  if (!fin[0]) return;
-  // Merge: out = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c with M = max_c m_c,
-  // accumulated online (the running max moves as slots are read). A thread reads
-  // four slots per step, so their loads are in flight together instead of one
-  // round trip per slot.
-  const int c_first = fin[1], c_last = fin[2];
   const int ooff = partial_o_offset(R);
   const float* base = a.partials + static_cast<size_t>(u) * a.slot_floats;   // slot of CTA c: + c * slot_floats
+  const int c_read = own_o ? c_first + 1 : c_first;                           // first slot read from memory
 #pragma unroll 1
   for (int idx = tid; idx < Rs * (D / 4); idx += nthr) {
     const int r = idx / (D / 4), d4 = idx - (idx / (D / 4)) * (D / 4);
     float M = kNegInf, L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (own_o) {
+      // Combining the first piece into the empty state gives exactly its own values.
+      M = own_ml[r];
+      L = own_ml[R + r];
+      acc = *reinterpret_cast<const float4*>(own_o + r * own_stride + d4 * 4);
+    }
 #pragma unroll 1
-    for (int c0 = c_first; c0 <= c_last; c0 += 4) {
+    for (int c0 = c_read; c0 <= c_last; c0 += 4) {
       float mc[4], lc[4];
       float4 oc[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const bool live = c0 + k <= c_last;
-        const float* P = base + static_cast<size_t>(live ? c0 + k : c_first) * a.slot_floats;
+        const float* P = base + static_cast<size_t>(live ? c0 + k : c_read) * a.slot_floats;
         mc[k] = live ? __ldcg(P + r) : kNegInf;
         lc[k] = live ? __ldcg(P + R + r) : 0.f;
         oc[k] = live ? __ldcg(reinterpret_cast<const float4*>(P + ooff + r * D + d4 * 4))
@@ -223,6 +191,150 @@ __device__ inline void finish_split_piece(const DecodeArgs& a, int u, long long 
     pk.x = pack_p<KV>(acc.x * inv, acc.y * inv);
     pk.y = pack_p<KV>(acc.z * inv, acc.w * inv);
     *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + dst) = pk;
+  }
+}
+
+// CTAs that hold pieces of a unit whose first block is at line position ustart
+// (nb blocks): c_first .. c_last.
+__device__ __forceinline__ void unit_owners(const DecodeArgs& a, long long ustart, int nb, long long total,
+                                            long long ncta, int* c_first, int* c_last) {
+  const long long nact = active_ctas(ncta, total, a.piece_cost);
+  *c_first = position_owner(ustart, nact, total);
+  *c_last = position_owner(ustart + nb - 1, nact, total);
+}
+
+// Count a published piece on unit u's counter (thread 0 only; the slot writes of
+// the CTA are ordered before it by the caller's barrier and the release fence
+// here). cur is a guess of the counter's value; a wrong guess costs one more CAS,
+// which returns the actual value. Counters are tagged with the call's epoch, so
+// no workspace clearing is needed: a counter left by an earlier call reads as
+// zero. Returns true for the piece that completes the unit (then with acquire
+// ordering for the other CTAs' slots).
+__device__ __forceinline__ bool count_published_piece(const DecodeArgs& a, int u, unsigned long long cur,
+                                                      int c_first, int c_last) {
+  fence_acq_rel_gpu();
+  unsigned long long* ctr = a.piece_counts + u;
+  const unsigned long long tag = static_cast<unsigned long long>(a.epoch) << 32;
+  unsigned long long want;
+  for (;;) {
+    want = (static_cast<uint32_t>(cur >> 32) == a.epoch) ? cur + 1ull : (tag | 1ull);
+    const unsigned long long prev = atomicCAS(ctr, cur, want);
+    if (prev == cur) break;
+    cur = prev;
+  }
+  const bool last = static_cast<int>(want & 0xffffffffull) == c_last - c_first + 1;
+  if (last) fence_acq_rel_gpu();   // acquire: the other CTAs' slots are read next
+  return last;
+}
+
+// After this CTA wrote its piece of unit u to slot (u + cta): count the piece on
+// the unit's counter; the CTA that finishes the last piece merges all pieces
+// into the output. Called by the nthr threads that wrote the slot (tid in
+// [0, nthr)), which synchronise on named barrier bar_id. ustart is the line
+// position of the unit's first block, nb its block count, Rs its real rows, qb its first query
+// row. The CTA that completes a unit clears its counter after the merge (no
+// other CTA touches it again in this launch), so a replayed CUDA graph (same
+// epoch every replay) starts from clear counters too.
+template <int KV, int D>
+__device__ inline void finish_split_piece(const DecodeArgs& a, int u, long long ustart, int nb,
+                                          long long total, long long ncta, int Rs, int qb, int h,
+                                          int tid, int nthr, int bar_id, volatile int* fin) {
+  // The barrier orders every thread's slot writes before thread 0's release fence.
+  named_bar_sync(bar_id, nthr);
+  if (tid == 0) {
+    int c_first, c_last;
+    unit_owners(a, ustart, nb, total, ncta, &c_first, &c_last);
+    // The CTA holding the unit's first block reaches this piece at the end of its
+    // share and is most likely the last to arrive (every other piece counted);
+    // any other CTA most likely the first (a cleared counter).
+    const unsigned long long guess =
+        (static_cast<int>(blockIdx.x) == c_first)
+            ? ((static_cast<unsigned long long>(a.epoch) << 32) | static_cast<unsigned long long>(c_last - c_first))
+            : 0ull;
+    const bool last = count_published_piece(a, u, guess, c_first, c_last);
+    fin[0] = last ? 1 : 0;
+    fin[1] = c_first;
+    fin[2] = c_last;
+    PKV_TL(a, kTlCounted);
+  }
+  named_bar_sync(bar_id, nthr);
+  if (!fin[0]) return;
+  merge_split_pieces<KV, D>(a, u, fin[1], fin[2], nullptr, 0, nullptr, Rs, qb, h, tid, nthr);
+  if (tid == 0) {
+    a.piece_counts[u] = 0ull;
+    PKV_TL(a, kTlMerged);
+  }
+}
+
+// The same for a piece whose merged partial is still in shared memory (o at
+// own_o[r * own_stride + d], m and l at own_ml[r], own_ml[rows + r]). The CTA
+// holding the unit's first block usually finishes the unit: it first tries to
+// count its piece as the completing one without publishing it; when that
+// succeeds it merges from its own shared memory and the other CTAs' slots, so
+// neither its slot write nor the fence that publishes it is on its critical
+// path. Otherwise (or on any other CTA) the piece is written to its slot and
+// counted as in finish_split_piece. cur_slot is 8 bytes of shared memory.
+template <int KV, int D>
+__device__ inline void finish_split_piece_smem(const DecodeArgs& a, int u, long long ustart, int nb,
+                                               long long total, long long ncta, int Rs, int qb, int h,
+                                               int tid, int nthr, int bar_id, volatile int* fin,
+                                               volatile unsigned long long* cur_slot, const float* own_o,
+                                               int own_stride, const float* own_ml) {
+  const int R = a.rows;
+  const int cta = static_cast<int>(blockIdx.x);
+  named_bar_sync(bar_id, nthr);   // the piece's merged partial is complete in shared memory
+  if (tid == 0) {
+    int c_first, c_last;
+    unit_owners(a, ustart, nb, total, ncta, &c_first, &c_last);
+    int state = 0;                 // 0: publish, then count; 1: counted as the completing piece
+    unsigned long long cur = 0ull;
+    if (cta == c_first) {
+      unsigned long long* ctr = a.piece_counts + u;
+      const unsigned long long all_others =
+          (static_cast<unsigned long long>(a.epoch) << 32) | static_cast<unsigned long long>(c_last - c_first);
+      const unsigned long long prev = atomicCAS(ctr, all_others, all_others + 1ull);
+      if (prev == all_others) {
+        state = 1;
+        fence_acq_rel_gpu();       // acquire: the other CTAs' slots are read next
+        PKV_TL(a, kTlCounted);
+      } else {
+        cur = prev;                // counted nothing: publish, then count from this value
+      }
+    }
+    fin[0] = state;
+    fin[1] = c_first;
+    fin[2] = c_last;
+    *cur_slot = cur;
+  }
+  named_bar_sync(bar_id, nthr);
+  const int c_first = fin[1], c_last = fin[2];
+  if (fin[0] == 0) {
+    float* P = a.partials + static_cast<size_t>(u + cta) * a.slot_floats;
+    const int ooff = partial_o_offset(R);
+#pragma unroll 1
+    for (int idx = tid; idx < Rs * (D / 4); idx += nthr) {
+      const int r = idx / (D / 4), d4 = idx - (idx / (D / 4)) * (D / 4);
+      if (d4 == 0) {
+        P[r] = own_ml[r];
+        P[R + r] = own_ml[R + r];
+      }
+      *reinterpret_cast<float4*>(P + ooff + r * D + d4 * 4) =
+          *reinterpret_cast<const float4*>(own_o + r * own_stride + d4 * 4);
+    }
+    named_bar_sync(bar_id, nthr);  // every slot write before thread 0's release fence
+    if (tid == 0) {
+      const bool last = count_published_piece(a, u, *cur_slot, c_first, c_last);
+      fin[0] = last ? 2 : 3;
+      PKV_TL(a, kTlCounted);
+    }
+    named_bar_sync(bar_id, nthr);
+    if (fin[0] == 3) return;
+  }
+  merge_split_pieces<KV, D>(a, u, c_first, c_last, fin[0] == 1 ? own_o : nullptr, own_stride, own_ml, Rs, qb,
+                            h, tid, nthr);
+  if (tid == 0) {
+    a.piece_counts[u] = 0ull;
+    PKV_TL(a, kTlMerged);
   }
 }
 

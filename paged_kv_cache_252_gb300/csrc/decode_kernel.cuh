@@ -47,6 +47,7 @@
 #include "decode_common.cuh"
 #include "pkv_internal.h"
 #include "pkv_ptx.cuh"
+#include "pkv_timeline.cuh"
 
 namespace pkv {
 
@@ -136,10 +137,13 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
   long long* red = reinterpret_cast<long long*>(smem + lay.misc);   // [10] block-reduce scratch
   long long* plan = red + 10;                                      // total, b0, b1, s0, cum0
   volatile int* abort_flag = reinterpret_cast<volatile int*>(plan + 5);
-  volatile int* fin = reinterpret_cast<volatile int*>(plan + 6);   // is_last, first CTA, last CTA
+  volatile int* fin = reinterpret_cast<volatile int*>(plan + 6);   // split-finish state, first CTA, last CTA
+  volatile unsigned long long* fin_cur = reinterpret_cast<volatile unsigned long long*>(plan + 8);
+  float* fin_ml = reinterpret_cast<float*>(smem + lay.fin_ml);     // a split piece's merged m[R], l[R]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool is_producer = (warp == NC);
+  if (tid == 0) PKV_TL(a, kTlStart);
 
   if (tid == 0) {
     for (int k = 0; k < stages; ++k) {
@@ -171,6 +175,7 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
 
   plan_cta_share(a, red, plan);
   pdl_launch_dependents();
+  if (tid == 0) PKV_TL(a, kTlPlanned);
 
   const long long total = plan[0], b0 = plan[1], b1 = plan[2];
   if (b0 >= b1 || plan[3] < 0) return;
@@ -242,6 +247,7 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
                 tma_load_2d(kdst, &tm_k, 0, row, full, pol);
                 tma_load_2d(kdst + TILE, &tm_v, 0, row, full, pol);
               }
+              if (i == 0) PKV_TL(a, kTlFirstIssue);
             }
           }
           ok = __shfl_sync(0xffffffffu, good, 0) != 0;
@@ -265,6 +271,7 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
         }
       }
     }
+    if (lane == 0) PKV_TL(a, kTlLastIssue);
     // Drain: every copy issued into this CTA's shared memory lands before exit.
     if (lane == 0) {
       for (int k = (i > stages ? i - stages : 0); k < i; ++k) {
@@ -285,6 +292,9 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
   // their ring stage and phase advance by WB blocks at a time (stages is a multiple of WB).
   int cst = wb;          // ib % stages of the stream's next block
   uint32_t cph = 0;      // (ib / stages) & 1
+#ifdef PKV_TIMELINE
+  unsigned long long tl_blocks = 0, tl_pieces = 0;
+#endif
 
   while (ub < b1) {
     const int take = static_cast<int>(min(static_cast<long long>(nb), b1 - ub)) - lb;
@@ -422,6 +432,10 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
         *abort_flag = 1;
         if (lane == 0 && a.status) atomicOr(a.status, kDevTimeout);
       }
+#ifdef PKV_TIMELINE
+      if (tid == 0 && tl_blocks == 0) PKV_TL(a, kTlFirstData);
+      tl_blocks += (tid == 0);
+#endif
       // A warp whose rows are all padding for this sequence (fewer query tokens
       // than the unit's row capacity) only waits for and releases its stages.
       if (alive && row_base < Rs) {
@@ -607,7 +621,11 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
       __syncwarp();
       if (lane == 0) mbar_arrive(bars + 8 * (stages + stage));
     }
+    if (tid == 0) PKV_TL(a, kTlLastData);
     i += take;
+#ifdef PKV_TIMELINE
+    ++tl_pieces;
+#endif
 
     // ---- merge the WB block streams of this piece ----
     if constexpr (kInt8) {
@@ -689,17 +707,21 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
         pk.y = pack_p<KV>(acc.z * inv, acc.w * inv);
         *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + dst) = pk;
       } else {
-        float* P = a.partials + static_cast<size_t>(u + cta) * a.slot_floats;
+        // A split piece keeps its merged partial in shared memory: o in place of
+        // block-stream 0's rows (only this thread reads or writes these four
+        // values), m and l beside.
+        *reinterpret_cast<float4*>(mrg_o + static_cast<size_t>(r) * (D + 4) + d4 * 4) = acc;
         if (d4 == 0) {
-          P[r] = M;
-          P[R + r] = lsum;
+          fin_ml[r] = M;
+          fin_ml[R + r] = lsum;
         }
-        *reinterpret_cast<float4*>(P + partial_o_offset(R) + r * D + d4 * 4) = acc;
       }
     }
 
+    if (tid == 0) PKV_TL(a, kTlPieceOut);
     if (split) {
-      finish_split_piece<KV, D>(a, u, ub, nb, total, ncta, Rs, qb, h, tid, nthr_c, 3, fin);
+      finish_split_piece_smem<KV, D>(a, u, ub, nb, total, ncta, Rs, qb, h, tid, nthr_c, 3, fin, fin_cur, mrg_o,
+                                     D + 4, fin_ml);
     }
 
     // ---- advance the walk (a piece that stops before the unit's end ended the share) ----
@@ -715,6 +737,12 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
       }
     }
   }
+#ifdef PKV_TIMELINE
+  if (tid == 0) {
+    PKV_TL(a, kTlExit);
+    PKV_TL_SET(a, kTlInfo, sm_id() | (tl_pieces << 16) | (tl_blocks << 32));
+  }
+#endif
 }
 
 }  // namespace pkv

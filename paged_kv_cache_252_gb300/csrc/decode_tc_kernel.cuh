@@ -56,6 +56,7 @@
 #include "pkv_internal.h"
 #include "pkv_ptx.cuh"
 #include "pkv_tc.cuh"
+#include "pkv_timeline.cuh"
 
 namespace pkv {
 
@@ -439,6 +440,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   volatile int* fin = abort_flag + 1;                               // is_last, first CTA, last CTA
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) PKV_TL(a, kTlStart);
 
   if (tid == 0) {
     for (int k = 0; k < nbuf; ++k) {
@@ -471,6 +473,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   pdl_wait_prior_grid();
   tc_plan(a, red, plan);
   pdl_launch_dependents();
+  if (tid == 0) PKV_TL(a, kTlPlanned);
 
   const long long total = plan[0], b0 = plan[1], b1 = plan[2];
   if (b0 < b1 && plan[3] >= 0) {
@@ -526,6 +529,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tma_load_2d(kdst + kTcChunk * TILE + k * TILE, &tm_v, 0, row, full, pol);
               }
             }
+            if (c == 0) PKV_TL(a, kTlFirstIssue);
           }
         }
         if (__shfl_sync(0xffffffffu, good, 0) == 0) break;   // chunk c was not issued
@@ -536,6 +540,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         w.advance(a);
       }
+      if (lane == 0) PKV_TL(a, kTlLastIssue);
       // Drain: every copy issued into this CTA's shared memory lands before exit.
       if (lane == 0) {
         for (int k = (c > nbuf ? c - nbuf : 0); k < c; ++k) mbar_wait(bars + 8 * (k % nbuf), (k / nbuf) & 1);
@@ -648,6 +653,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       {
         tc_copy_q<RP, kTcSoftmaxThreads>(a, pc, cur.h, tid, qst);
         wait_bar(bars, 0);
+        if (tid == 0) PKV_TL(a, kTlFirstData);
         const bool valid = (t >> 4) < cur.nblk() && cur.first_token() + t < pc.ctx_eff;
         if (alive) {
           widen_e5m2_half_row_tmem(ring, t, hh, valid, t_lane + kTcKCol);
@@ -788,6 +794,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           named_bar_sync(2, kTcSoftmaxThreads);
           wait_o(c);
           if (alive) tc_piece_output(a, t_cols, pc, cur.h, r0, RH, t, row_inv, cta);
+          if (tid == 0) PKV_TL(a, kTlPieceOut);
           if (pc.split) tc_finish_split(a, pc, cur.ub, cur.nb, total, ncta, cur.h, tid, fin);
           // The next piece starts from an empty running max.
           named_bar_sync(2, kTcSoftmaxThreads);
@@ -799,6 +806,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           pc = pn;
           ++piece;
         }
+        if (tid == 0 && cur.last()) PKV_TL(a, kTlLastData);
         cur = nxt;
         ++c;
         if (++buf_next == nbuf) {
@@ -806,6 +814,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           wrap_next ^= 1u;
         }
       }
+#ifdef PKV_TIMELINE
+      if (tid == 0) {
+        PKV_TL(a, kTlExit);
+        PKV_TL_SET(a, kTlInfo, sm_id() | (static_cast<unsigned long long>(piece + 1) << 16) |
+                                   (static_cast<unsigned long long>(c) * kTcChunk << 32));
+      }
+#endif
     }
   }
 

@@ -47,6 +47,10 @@ struct DecodeArgs {
   float scale_log2;            // softmax scale * log2(e)
   uint32_t epoch;              // distinct for every call (tags the piece counters)
   int32_t piece_cost;          // fixed cost of a unit piece, in blocks, for the CTA shares
+#ifdef PKV_TIMELINE
+  unsigned long long* timeline;  // profiling build only: per-CTA event times (pkv_timeline.cuh)
+  int32_t timeline_ctas;
+#endif
 };
 
 
@@ -76,7 +80,7 @@ __host__ __device__ constexpr int partial_slot_floats(int rows, int d) {
 // Shared-memory layout of the decode kernel, relative to a 1024-aligned base.
 // An INT8 cache adds, per ring stage, the 16 K and 16 V row scales (128 bytes).
 struct DecodeSmem {
-  size_t ring, scales, bars, qs, mrg_o, mrg_ml, misc, total;
+  size_t ring, scales, bars, qs, mrg_o, mrg_ml, fin_ml, misc, total;
 };
 // The merge buffers hold only the unit's real rows (rows <= 8*ntw*wr).
 __host__ __device__ inline DecodeSmem decode_smem_layout(int kv, int d, int ntw, int wr, int wb,
@@ -90,8 +94,9 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int kv, int d, int ntw,
   s.qs = (s.qs + 15) & ~(size_t)15;
   s.mrg_o = s.qs + (size_t)rows_pad * (d * 2 + 16);
   s.mrg_ml = s.mrg_o + (size_t)wb * rows * (d + 4) * 4;
-  s.misc = s.mrg_ml + (size_t)((wb * rows * 2 * 4 + 15) & ~15);
-  s.total = s.misc + 256;   // block-reduce scratch, CTA plan, abort flag
+  s.fin_ml = s.mrg_ml + (size_t)((wb * rows * 2 * 4 + 15) & ~15);   // a split piece's merged m, l
+  s.misc = s.fin_ml + (size_t)((rows * 2 * 4 + 15) & ~15);
+  s.total = s.misc + 256;   // block-reduce scratch, CTA plan, abort flag, split-finish state
   return s;
 }
 
