@@ -78,3 +78,21 @@ def test_noalloc_rejects_problems_beyond_its_buffer(dev):
     rc = lib.pkv_paged_attention_decode_noalloc(fake, fake, S, 64, 8, fake, fake, 0, ctypes.byref(desc),
                                                 fake, 4, fake, ctypes.c_float(0.1), None, None)
     assert rc == -3   # PKV_ERR_WORKSPACE_TOO_SMALL, nothing launched
+
+
+@pytest.mark.parametrize("case", ["rows_over_64", "heads_not_divisible", "bad_head_size"])
+def test_noalloc_refused_shapes_get_the_regular_status(dev, case):
+    """A shape the library refuses gets the same status from the no-alloc entry
+    point as from the regular one (nothing is launched by either)."""
+    from paged_kv_cache_252_gb300.api import _CacheDesc, load_library
+    lib = load_library()
+    Hq, Hkv, D, n = {"rows_over_64": (128, 1, 128, 1), "heads_not_divisible": (12, 8, 128, 1),
+                     "bad_head_size": (8, 2, 96, 1)}[case]
+    desc = _CacheDesc(64, 16, Hkv, D)
+    fake = ctypes.c_void_p(256)
+    ws = ctypes.c_void_p(1 << 20)
+    reg = lib.pkv_paged_attention_decode(fake, fake, 4, Hq, n, fake, fake, 0, ctypes.byref(desc), fake, 4,
+                                         fake, ctypes.c_float(0.1), ws, ctypes.c_size_t(1 << 30), None, None)
+    na = lib.pkv_paged_attention_decode_noalloc(fake, fake, 4, Hq, n, fake, fake, 0, ctypes.byref(desc),
+                                                fake, 4, fake, ctypes.c_float(0.1), None, None)
+    assert reg < 0 and na == reg, (reg, na)
