@@ -15,7 +15,14 @@ Workloads (seeded, synthetic; see paged_kv_cache_252_gb300/workloads.py):
 
 value  = algorithmic bytes of the step / device time per step (GB/s), inputs
          resident in HBM. Algorithmic bytes: every visible token's K and V once,
-         q in, out out, plus the cache write's reads and writes.
+         q in, out out, plus the cache write's reads and writes. The K timed
+         steps are captured as one CUDA graph and replayed (as a serving loop
+         replays its decode steps); the same steps issued one by one from Python
+         are reported beside (ms_per_step_host_issued).
+roofline = the decode launch alone: algorithmic bytes / mean time per launch,
+         from CUDA events around graphs of back-to-back launches (the binding's
+         Python time per call is about the kernel's, so launches issued one by
+         one with an event pair each, also reported, partly time the host).
 e2e    = the same metric through the public Python API with host buffers: the
          step's q, new K/V tokens, slot mapping, block table and lengths copied
          from pinned host memory (one packed copy), and the output copied back,
@@ -289,9 +296,11 @@ class Prepared:
     def decode_pool(self, p):
         self.decode(self.outs[p], self.qs[p], self.caches[p], self.bt, self.cl, self.cu)
 
-    def time_decode(self, n: int) -> float:
-        """Mean seconds per decode launch over n launches (rotating pools), an event
-        pair on the launching stream around each launch."""
+    def time_decode_host_issued(self, n: int) -> float:
+        """Mean seconds per decode launch over n launches issued one by one from
+        Python (rotating pools), an event pair on the launching stream around each.
+        When the binding's per-call host time exceeds the kernel's, the GPU idles
+        between the first event and the launch and this overstates the kernel."""
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
         torch.cuda.synchronize(self.dev)
         for i in range(n):
@@ -300,6 +309,50 @@ class Prepared:
             evs[i][1].record()
         torch.cuda.synchronize(self.dev)
         return float(np.mean([a.elapsed_time(b) for a, b in evs])) / 1e3
+
+    def graph_of(self, n: int, body):
+        """A CUDA graph of body(0), ..., body(n-1) (library calls only), captured on
+        a side stream. One call runs on that stream before the capture, so the
+        binding's workspace for it exists outside the capture."""
+        cur = torch.cuda.current_stream(self.dev)
+        s = torch.cuda.Stream(self.dev)
+        s.wait_stream(cur)
+        with torch.cuda.stream(s):
+            body(0)
+        cur.wait_stream(s)
+        torch.cuda.synchronize(self.dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for i in range(n):
+                body(i)
+        torch.cuda.synchronize(self.dev)
+        return g
+
+    def time_graph(self, g, replays: int = 1) -> float:
+        """Seconds for `replays` back-to-back replays of g, an event pair on the
+        current stream around them (after one untimed replay that uploads it)."""
+        cur = torch.cuda.current_stream(self.dev)
+        g.replay()
+        torch.cuda.synchronize(self.dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(cur)
+        for _ in range(replays):
+            g.replay()
+        b.record(cur)
+        torch.cuda.synchronize(self.dev)
+        return a.elapsed_time(b) / 1e3
+
+    def time_decode(self, n: int, per_graph: int = 200):
+        """Mean seconds per decode launch over about n launches run back to back from
+        CUDA graphs of up to per_graph launches (rotating pools), as a serving loop
+        replays them; returns (seconds per launch, launches timed)."""
+        k = min(per_graph, n)
+        k = max(self.pools, (k + self.pools - 1) // self.pools * self.pools)
+        replays = max(1, -(-n // k))
+        g = self.graph_of(k, lambda i: self.decode_pool(i % self.pools))
+        t = self.time_graph(g, replays)
+        del g
+        return t / (k * replays), k * replays
 
 
 # The other workloads, measured as decode-op timings in the same run.
@@ -318,16 +371,17 @@ def measure_per_config(keys, dev, peak, min_launches=50, min_seconds=1.0):
         P = Prepared(w, dev, pool_count(w, l2))
         for i in range(5):
             P.decode_pool(i % P.pools)
-        est = P.time_decode(20)
+        est, _ = P.time_decode(20)
         n = max(min_launches, int(math.ceil(min_seconds / max(est, 1e-6))))
-        n = (n + P.pools - 1) // P.pools * P.pools
         sampler = ClockSampler(dev.index)
         sampler.start()
-        t = P.time_decode(n)
+        t, n = P.time_decode(n)
         clocks = sampler.stop()
+        t_host = P.time_decode_host_issued(min_launches)
         achieved = P.attn_bytes / t / 1e9
         res[key] = {"workload": w.name, "kv_dtype": w.kv_dtype, "launches": n,
                     "us_per_launch": round(t * 1e6, 3),
+                    "us_per_launch_host_issued": round(t_host * 1e6, 3),
                     "achieved_gbs": round(achieved, 2), "frac": round(achieved / peak, 4),
                     "algorithmic_bytes_per_launch": int(P.attn_bytes),
                     "seq_steps_per_s": round(w.num_seqs / t, 1),
@@ -354,6 +408,14 @@ def run_ours(args, rank, world, local):
     for i in range(args.warmup):
         P.step(i)
     torch.cuda.synchronize(dev)
+
+    # The K timed steps run as one CUDA graph replay (as a serving loop replays its
+    # decode steps), so the binding's host time does not enter the measurement; the
+    # graph is captured and replayed once untimed first.
+    g_steps = P.graph_of(args.steps, P.step) if not args.no_graph else None
+    if g_steps is not None:
+        g_steps.replay()
+    torch.cuda.synchronize(dev)
     barrier(world, dev)
 
     sampler = ClockSampler(local) if not args.no_clocks else None
@@ -362,18 +424,35 @@ def run_ours(args, rank, world, local):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
     e0.record()
-    for i in range(args.steps):
-        P.step(i)
+    if g_steps is not None:
+        g_steps.replay()
+    else:
+        for i in range(args.steps):
+            P.step(i)
     e1.record()
     torch.cuda.synchronize(dev)
     clocks = sampler.stop() if sampler else None
     barrier(world, dev)
     elapsed = e0.elapsed_time(e1) / 1e3
     job_elapsed, job_bytes = aggregate(elapsed, step_bytes * args.steps, world, dev)
+    del g_steps
 
-    # Decode op alone (one decode launch, split-KV combine fused), per-launch CUDA events on its stream.
-    n_r = max(args.steps, 50)
-    dec_s = P.time_decode(n_r)
+    # The same K steps issued one by one from Python (reported beside: the binding's
+    # per-call host time is close to the kernel's, so this is partly host-bound).
+    torch.cuda.synchronize(dev)
+    h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    h0.record()
+    for i in range(args.steps):
+        P.step(i)
+    h1.record()
+    torch.cuda.synchronize(dev)
+    host_issued_step_s = h0.elapsed_time(h1) / 1e3 / args.steps
+
+    # Decode op alone (one decode launch, split-KV combine fused): CUDA events on its
+    # stream around graphs of back-to-back launches; and, beside it, launches issued
+    # one by one from Python with an event pair around each.
+    dec_s, n_r = P.time_decode(max(args.steps, 50))
+    dec_host_s = P.time_decode_host_issued(max(args.steps, 50))
 
     # End to end through the public API with pinned host buffers, run the way a
     # serving loop runs it: each step's inputs travel in one packed host->device
@@ -504,6 +583,9 @@ def run_ours(args, rank, world, local):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(elapsed / args.steps * 1e3, 5),
+        "ms_per_step_host_issued": round(host_issued_step_s * 1e3, 5),
+        "launch": ("the K steps as one CUDA graph replay" if not args.no_graph
+                   else "the K steps issued one by one from Python"),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -518,7 +600,9 @@ def run_ours(args, rank, world, local):
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,
                      "traffic": profiled_traffic(args.config),
                      "algorithmic_bytes_per_launch": int(attn_bytes),
-                     "us_per_launch": round(dec_s * 1e6, 3), "launches_timed": n_r},
+                     "us_per_launch": round(dec_s * 1e6, 3), "launches_timed": n_r,
+                     "timing": "CUDA events around graphs of back-to-back decode launches",
+                     "us_per_launch_host_issued": round(dec_host_s * 1e6, 3)},
         "e2e": e2e,
         # per step: the cache write and the decode, one launch each
         "gpu_launches": 2 * args.steps,
@@ -667,7 +751,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-graph", action="store_true", help="e2e by direct calls instead of graph replays")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="steps and e2e by direct calls instead of graph replays")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the decode-op timings of the other workloads")
