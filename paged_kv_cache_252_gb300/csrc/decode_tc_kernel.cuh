@@ -497,6 +497,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // ------------------------------- producer ----------------------------------
       const uint64_t pol = l2_policy_evict_first();
       const int total_rows = a.num_blocks * a.num_kv_heads * kBlockSize;   // host guarantees < 2^31
+#ifdef PKV_TIMELINE
+      long long tl_prod_wait = 0;
+      const long long tl_prod0 = clock64();
+#endif
       TcWalk w = w0;
       int c = 0;
       int buf = 0;          // c % nbuf
@@ -510,7 +514,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int k = 0; k < kTcChunk; ++k) blk[k] = __shfl_sync(0xffffffffu, mine, k);
         int good = 1;
         if (lane == 0) {
+#ifdef PKV_TIMELINE
+          const long long tl_w0 = clock64();
+          const bool tl_ok = c < nbuf || tc_wait(bars + 8 * (nbuf + buf), wrap ^ 1u, abort_flag);
+          tl_prod_wait += clock64() - tl_w0;
+          if (!tl_ok) {
+            PKV_TL_TIMEOUT(a, 0x70, c);
+#else
           if (c >= nbuf && !tc_wait(bars + 8 * (nbuf + buf), wrap ^ 1u, abort_flag)) {
+#endif
             good = 0;
             *abort_flag = 1;
             if (a.status) atomicOr(a.status, kDevTimeout);
@@ -540,7 +552,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         w.advance(a);
       }
-      if (lane == 0) PKV_TL(a, kTlLastIssue);
+      if (lane == 0) {
+        PKV_TL(a, kTlLastIssue);
+#ifdef PKV_TIMELINE
+        PKV_TL_SET(a, kTlProdWait, tl_prod_wait);
+        PKV_TL_SET(a, kTlProdTotal, clock64() - tl_prod0);
+#endif
+      }
       // Drain: every copy issued into this CTA's shared memory lands before exit.
       if (lane == 0) {
         for (int k = (c > nbuf ? c - nbuf : 0); k < c; ++k) mbar_wait(bars + 8 * (k % nbuf), (k / nbuf) & 1);
@@ -561,11 +579,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         TcWalk w = w0;
         int c = 0, piece = 0;
         bool prev = false, prev_first = false, ok = true;
+#ifdef PKV_TIMELINE
+        long long tl_wk = 0, tl_wpv = 0;
+        const long long tl_mma0 = clock64();
+#endif
         for (;;) {
           const bool cur = !w.done();
           if (cur) {
             // S^T(c) = K(c) Q^T: S and K buffer c % 2
-            if (!(ok = tc_wait(bar_kready, c & 1, abort_flag))) break;
+#ifdef PKV_TIMELINE
+            const long long tl_t0 = clock64();
+#endif
+            ok = tc_wait(bar_kready, c & 1, abort_flag);
+#ifdef PKV_TIMELINE
+            tl_wk += clock64() - tl_t0;
+#endif
+            if (!ok) {
+              PKV_TL_TIMEOUT(a, 0x61, c);
+              break;
+            }
             tc_fence_after_sync();
             const uint64_t dqs = (piece & 1) ? dq1 : dq0;
             const uint32_t t_s = tmem + (c & 1) * kTcSCols;
@@ -579,7 +611,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           if (prev) {
             // O^T += V(c-1)^T P^T
-            if (!(ok = tc_wait(bar_pvready, (c - 1) & 1, abort_flag))) break;
+#ifdef PKV_TIMELINE
+            const long long tl_t1 = clock64();
+#endif
+            ok = tc_wait(bar_pvready, (c - 1) & 1, abort_flag);
+#ifdef PKV_TIMELINE
+            tl_wpv += clock64() - tl_t1;
+#endif
+            if (!ok) {
+              PKV_TL_TIMEOUT(a, 0x63, c);
+              break;
+            }
             tc_fence_after_sync();
             const uint64_t dvs = ((c - 1) & 1) ? dv1 : dv0;
 #pragma unroll
@@ -600,6 +642,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           *abort_flag = 1;
           if (a.status) atomicOr(a.status, kDevTimeout);
         }
+#ifdef PKV_TIMELINE
+        PKV_TL_SET(a, kTlMmaWaitK, tl_wk);
+        PKV_TL_SET(a, kTlMmaWaitPV, tl_wpv);
+        PKV_TL_SET(a, kTlMmaTotal, clock64() - tl_mma0);
+#endif
         // Every MMA issued above completes before the tensor memory is released.
         tc_commit(bar_final);
         mbar_wait(bar_final, 0);
@@ -617,6 +664,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bool alive = true;
       int o_waited = -1;
       int mp = 0;   // current running-max buffer
+      int c = 0;
 
       auto wait_bar = [&](uint32_t bar, uint32_t parity) {
         if (!alive) return;
@@ -625,6 +673,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           alive = false;
           *abort_flag = 1;
           if (lane == 0 && a.status) atomicOr(a.status, kDevTimeout);
+          if (lane == 0) PKV_TL_TIMEOUT(a, 0x40 + (bar - bars) / 8, c);
         }
       };
       auto wait_o = [&](int k) {
@@ -645,7 +694,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
       TcWalk cur = w0;
       TcPiece pc = tc_piece(a, cur, tid);
-      int c = 0, piece = 0;
+      int piece = 0;
       int buf_next = 1;          // (c + 1) % nbuf (nbuf >= 2)
       uint32_t wrap_next = 0;    // ((c + 1) / nbuf) & 1
 
@@ -669,6 +718,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
 
+#ifdef PKV_TIMELINE
+      PKV_TL_STEP_BEGIN;
+#endif
       while (!cur.done()) {
         TcWalk nxt = cur;
         nxt.advance(a);
@@ -686,6 +738,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
         // (1) scores of chunk c, rows r0 .. r0+RH-1, from S buffer c % 2
         uint32_t sv[RH];
+        PKV_TL_STEP(0);
         wait_bar(bar_sfull, c & 1);
         if (alive) {
           tc_fence_after_sync();
@@ -697,8 +750,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
         // (2) K of chunk c+1 into K buffer (c+1) % 2, last read by S(c-1) (complete):
         //     S(c+1) overlaps the softmax below
+        PKV_TL_STEP(1);
         if (has_next) {
           wait_bar(bars + 8 * buf_next, wrap_next);
+          PKV_TL_STEP(2);
           if (alive) widen_e5m2_half_row_tmem(ring_next, t, hh, valid_next, t_lane + kTcKCol + ((c + 1) & 1) * 64);
           cp_async_wait_all();
           fence_proxy_async_smem();
@@ -706,6 +761,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (alive) mbar_arrive(bar_kready);
         }
 
+        PKV_TL_STEP(3);
         // (3) scores in base 2, masked; does any exceed its row's running max by the slack?
         const int p = cur.first_token() + t;
         const bool valid = (t >> 4) < cur.nblk() && p < pc.ctx_eff;
@@ -729,7 +785,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                          fmaxf(x[4 * k4 + 2] - m4.z, x[4 * k4 + 3] - m4.w)));
           }
         }
-        if (bar_red_or(1, kTcSoftmaxThreads, excess > kRescaleSlack)) {
+        const bool rare = bar_red_or(1, kTcSoftmaxThreads, excess > kRescaleSlack);
+        PKV_TL_STEP(4);
+        if (rare) {
           // Rare: the running maxima move to this chunk's maxima, and what the
           // rows accumulated so far is rescaled.
           if (alive) tc_chunk_maxima(t_cols + (c & 1) * kTcSCols, vis, scale_log2, red_m, RP, q, r0, RH, lane);
@@ -744,8 +802,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int k = 0; k < RH; ++k) l_run[k] *= row_alpha[r0 + k];
         }
 
+        PKV_TL_STEP(5);
         // (4) P^T of chunk c: K-major [token half][row][128 B]; the buffer was read by O(c-1).
         if (c > 0) wait_o(c - 1);
+        PKV_TL_STEP(6);
         if (alive) {
           const float* mrow = row_m + mp * RP + r0;
 #pragma unroll
@@ -767,6 +827,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
 
+        PKV_TL_STEP(7);
         // (5) V of chunk c+1 (its buffer was read by O(c-1)); release the ring buffer.
         if (has_next) {
           if (alive) widen_e5m2_half_row(ring_next + kTcChunk * TILE, v16 + ((c + 1) & 1) * kWide, t, hh, valid_next);
@@ -777,6 +838,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_before_sync();
         if (alive) mbar_arrive(bar_pvready);
 
+        PKV_TL_STEP(8);
         // (6) end of a piece: normalise and write, or write the split partial.
         if (cur.last()) {
           {
@@ -807,6 +869,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ++piece;
         }
         if (tid == 0 && cur.last()) PKV_TL(a, kTlLastData);
+        PKV_TL_STEP(9);
         cur = nxt;
         ++c;
         if (++buf_next == nbuf) {
@@ -816,6 +879,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
 #ifdef PKV_TIMELINE
       if (tid == 0) {
+        PKV_TL_STEP_FLUSH(a);
         PKV_TL(a, kTlExit);
         PKV_TL_SET(a, kTlInfo, sm_id() | (static_cast<unsigned long long>(piece + 1) << 16) |
                                    (static_cast<unsigned long long>(c) * kTcChunk << 32));

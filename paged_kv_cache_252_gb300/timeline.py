@@ -28,7 +28,12 @@ from . import workloads as wl
 
 EVENTS = ["start", "planned", "first_issue", "last_issue", "first_data", "last_data", "exit"]
 LATE = ["piece_out", "counted", "merged"]   # events 8..10: the last piece's epilogue
-NEV = 12                                     # 64-bit words per CTA (pkv_timeline.cuh)
+NEV = 28                                     # 64-bit words per CTA (pkv_timeline.cuh)
+# tcgen05 kernel: cycles per chunk of the softmax loop's steps (thread 0), the MMA
+# thread's waits and the producer's wait for a free ring buffer (words 12..26)
+STEP_NAMES = ["top: next chunk / queries", "wait S + read scores", "wait ring (next chunk)",
+              "widen K (next chunk)", "scores, max vote", "rare rescale", "wait O (previous chunk)",
+              "exp2 + write P", "widen V (next chunk)", "end of piece"]
 MAX_CTAS = 4096
 
 
@@ -130,6 +135,21 @@ def summarize(w, rows, event_us: float | None = None) -> str:
             d = v[ok] - ld[ok]
             q = np.percentile(d, [0, 10, 50, 90, 100])
             lines.append(f"| {name} - last_data ({int(ok.sum())} CTAs) | " + " | ".join(f"{x:.2f}" for x in q) + " |")
+    steps = rows[:, 12:12 + len(STEP_NAMES)].astype(np.float64)
+    chunks = ((info >> 32) // 8).astype(np.float64)          # tcgen05 kernel: blocks / 8 per chunk
+    if steps[busy].sum() > 0:
+        per = steps[busy] / np.maximum(chunks[busy], 1)[:, None]
+        lines += ["", "tcgen05 chunk loop, SM cycles per chunk (median over CTAs):",
+                  "| step (softmax thread 0) | cycles |", "|---|---|"]
+        for k, name in enumerate(STEP_NAMES):
+            lines.append(f"| {name} | {np.median(per[:, k]):.0f} |")
+        lines.append(f"| total | {np.median(per.sum(axis=1)):.0f} |")
+        mma = rows[busy, 22:25].astype(np.float64) / np.maximum(chunks[busy], 1)[:, None]
+        prod = rows[busy, 25:27].astype(np.float64) / np.maximum(chunks[busy], 1)[:, None]
+        lines += [f"MMA thread per chunk: waiting for K {np.median(mma[:, 0]):.0f}, for P/V "
+                  f"{np.median(mma[:, 1]):.0f}, loop total {np.median(mma[:, 2]):.0f} cycles",
+                  f"producer per chunk: waiting for a free buffer {np.median(prod[:, 0]):.0f}, loop total "
+                  f"{np.median(prod[:, 1]):.0f} cycles"]
     ex = rel[busy, 6]
     span = np.nanmax(rel[:, 6])
     ramp = np.nanmedian(rel[busy, 4])
