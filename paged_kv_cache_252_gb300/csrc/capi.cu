@@ -48,9 +48,19 @@ int g_timeline_ctas = 0;
 // Fixed cost of one unit piece on the work line, in KV blocks: the piece's
 // query load, epilogue and (when split) merge take about as long as streaming
 // this many blocks, so CTAs whose share starts more units get fewer blocks.
-constexpr int kPieceCost2B = 8;   // mma.sync kernel, fp16 / bf16 cache
-constexpr int kPieceCost1B = 4;   // mma.sync kernel, E5M2 / INT8 cache
-constexpr int kPieceCostTc = 24;  // tcgen05 kernel (its epilogue reads O from tensor memory)
+// (Compile-time overridable for tuning sweeps.)
+#ifndef PKV_PIECE_COST_2B
+#define PKV_PIECE_COST_2B 8
+#endif
+#ifndef PKV_PIECE_COST_1B
+#define PKV_PIECE_COST_1B 8
+#endif
+#ifndef PKV_PIECE_COST_TC
+#define PKV_PIECE_COST_TC 24
+#endif
+constexpr int kPieceCost2B = PKV_PIECE_COST_2B;   // mma.sync kernel, fp16 / bf16 cache
+constexpr int kPieceCost1B = PKV_PIECE_COST_1B;   // mma.sync kernel, E5M2 / INT8 cache
+constexpr int kPieceCostTc = PKV_PIECE_COST_TC;   // tcgen05 kernel (its epilogue reads O from tensor memory)
 int piece_cost(bool tc, int kv) {
   if (tc) return kPieceCostTc;
   return (kv == PKV_FP8_E5M2 || kv == PKV_INT8) ? kPieceCost1B : kPieceCost2B;
