@@ -260,7 +260,9 @@ int pkv_paged_attention_decode_noalloc(void* out, const void* q, int32_t num_seq
  * both divisions in IEEE fp32; an all-zero row has scale 0 and codes 0; an
  * element's value is code * scale.
  *
- * Caches: int8 [num_blocks][num_kv_heads][16][head_size]; scales: one float32
+ * Caches: one byte per element, [num_blocks][num_kv_heads][16][head_size],
+ * each code stored in offset binary: byte = code + 128 (1..255; the decode
+ * kernel widens it to fp16 with one byte permute); scales: one float32
  * array [num_blocks][num_kv_heads][2][16]: the 16 K row scales of a (block,
  * KV head) tile, then its 16 V row scales (so one 128-byte copy brings both),
  * all 16-byte aligned.

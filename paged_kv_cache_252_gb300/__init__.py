@@ -23,5 +23,5 @@ from .api import (  # noqa: F401
     paged_attention_decode_noalloc, decode_workspace_bytes,
     library_path, load_library, alloc_kv_cache, PagedKVError,
     BlockAllocator, copy_blocks,
-    alloc_kv_scales, kv_cache_write_int8, paged_attention_decode_int8,
+    alloc_kv_scales, kv_cache_write_int8, paged_attention_decode_int8, int8_codes,
 )

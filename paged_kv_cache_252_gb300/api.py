@@ -218,12 +218,17 @@ def _need_cuda_contig(name, t):
 
 def alloc_kv_cache(num_blocks: int, num_kv_heads: int, head_size: int, kv_dtype,
                    device="cuda", zero: bool = True):
-    """Allocate a K/V cache pair [num_blocks, num_kv_heads, 16, head_size]."""
+    """Allocate a K/V cache pair [num_blocks, num_kv_heads, 16, head_size]. An INT8
+    cache is a torch.int8 tensor whose bytes hold the codes in offset binary
+    (byte = code + 128; :func:`int8_codes` reads them back). ``zero`` fills the
+    caches with the value 0 (for INT8: code 0, byte 0x80)."""
     code = _NAMES[kv_dtype] if isinstance(kv_dtype, str) else int(kv_dtype)
     dt = {KV_FP16: torch.float16, KV_BF16: torch.bfloat16, KV_E5M2: torch.uint8, KV_INT8: torch.int8}[code]
-    mk = torch.zeros if zero else torch.empty
     shape = (num_blocks, num_kv_heads, BLOCK_SIZE, head_size)
-    return mk(shape, dtype=dt, device=device), mk(shape, dtype=dt, device=device)
+    if not zero:
+        return torch.empty(shape, dtype=dt, device=device), torch.empty(shape, dtype=dt, device=device)
+    fill = -128 if code == KV_INT8 else 0   # int8 -128 is the byte 0x80
+    return (torch.full(shape, fill, dtype=dt, device=device), torch.full(shape, fill, dtype=dt, device=device))
 
 
 def alloc_kv_scales(num_blocks: int, num_kv_heads: int, device="cuda"):
@@ -232,9 +237,18 @@ def alloc_kv_scales(num_blocks: int, num_kv_heads: int, device="cuda"):
     return torch.zeros((num_blocks, num_kv_heads, 2, BLOCK_SIZE), dtype=torch.float32, device=device)
 
 
+def int8_codes(cache: torch.Tensor) -> torch.Tensor:
+    """The signed codes of an INT8 cache, whose bytes are stored in offset binary
+    (byte = code + 128): a torch.int8 tensor of the same shape and device."""
+    if cache.dtype != torch.int8:
+        raise PagedKVError("int8_codes reads an INT8 cache (torch.int8)")
+    return (cache.view(torch.uint8).to(torch.int16) - 128).to(torch.int8)
+
+
 def kv_cache_write_int8(key, value, slot_mapping, k_cache, v_cache, scales, *,
                         device_status=None, stream=None):
-    """Quantise fp16 key/value [T, Hkv, D] into INT8 caches and their row scales."""
+    """Quantise fp16 key/value [T, Hkv, D] into INT8 caches (codes in offset binary,
+    byte = code + 128) and their row scales."""
     for n, t in (("key", key), ("value", value), ("slot_mapping", slot_mapping), ("k_cache", k_cache),
                  ("v_cache", v_cache), ("scales", scales)):
         _need_cuda_contig(n, t)

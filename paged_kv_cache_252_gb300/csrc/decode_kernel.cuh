@@ -21,7 +21,8 @@
 //                        tensor cores (mma.sync m16n8k16, fp32 accumulate), online
 //                        softmax in base 2 with quad shuffles. E5M2 tiles are
 //                        widened to fp16 in registers (byte << 8 is exact);
-//                        INT8 tiles to code + 1152 (0x64 | (b ^ 0x80)), the bias
+//                        INT8 tiles (offset-binary bytes u = code + 128) to
+//                        code + 1152 (0x64 | u, one byte permute), the bias
 //                        taken off once per row after the MMAs, with each token's
 //                        K scale applied to its scores and its V scale folded into P.
 //   Block i of the CTA goes to ring stage i mod STAGES and to block-stream
@@ -74,11 +75,11 @@ __device__ __forceinline__ uint32_t swz(uint32_t off) {
 }
 
 // Two bytes of a tile register as an fp16 pair: E5M2 (the byte is the fp16
-// pattern's top byte) or INT8 (r holds the bytes XOR 0x80: 0x64 | u is the
-// fp16 value 1024 + u = code + kI8Bias). sel_e5m2 places the two chosen bytes
-// as fp16 high bytes; sel_i8 picks the same two. The INT8 bias is not taken
-// off element by element: q . (c + bias) and sum_t P_t (c_t + bias) are
-// corrected once per row by bias * sum(q) and bias * sum_t P_t.
+// pattern's top byte) or INT8 (the byte is the offset-binary code u = code + 128,
+// and 0x64 | u is the fp16 value 1024 + u = code + kI8Bias). sel_e5m2 places the
+// two chosen bytes as fp16 high bytes; sel_i8 picks the same two. The INT8 bias
+// is not taken off element by element: q . (c + bias) and sum_t P_t (c_t + bias)
+// are corrected once per row by bias * sum(q) and bias * sum_t P_t.
 constexpr float kI8Bias = 1152.f;
 template <int KV>
 __device__ __forceinline__ uint32_t widen_pair(uint32_t r, uint32_t sel_e5m2, uint32_t sel_i8) {
@@ -86,15 +87,6 @@ __device__ __forceinline__ uint32_t widen_pair(uint32_t r, uint32_t sel_e5m2, ui
     return __byte_perm(r, 0x64646464u, sel_i8);
   } else {
     return __byte_perm(r, 0, sel_e5m2);
-  }
-}
-
-template <int KV>
-__device__ __forceinline__ uint32_t byte_bias(uint32_t r) {
-  if constexpr (KV == kKvInt8) {
-    return r ^ 0x80808080u;
-  } else {
-    return r;
   }
 }
 
@@ -479,7 +471,6 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
               uint32_t r0, r1, r2, r3;
               ldsm_x4(kt + swz<RB>(tile_off<RB>(tok, ch)), r0, r1, r2, r3);
               // Widen bytes (0,1) and (2,3) of each register to fp16 pairs.
-              r0 = byte_bias<KV>(r0); r1 = byte_bias<KV>(r1); r2 = byte_bias<KV>(r2); r3 = byte_bias<KV>(r3);
               const uint32_t k0 = widen_pair<KV>(r0, 0x1404, 0x4140), k2 = widen_pair<KV>(r0, 0x3424, 0x4342);
               const uint32_t k1 = widen_pair<KV>(r1, 0x1404, 0x4140), k3 = widen_pair<KV>(r1, 0x3424, 0x4342);
               const uint32_t k4 = widen_pair<KV>(r2, 0x1404, 0x4140), k6 = widen_pair<KV>(r2, 0x3424, 0x4342);
@@ -604,7 +595,6 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
               ldsm_x4_t(vt + swz<RB>(tile_off<RB>(tok, ch)), r0, r1, r2, r3);
               // Transposed load of byte pairs: register = {V[2c][2g], V[2c][2g+1],
               // V[2c+1][2g], V[2c+1][2g+1]}; m-row g <-> d 2g, m-row g+8 <-> d 2g+1.
-              r0 = byte_bias<KV>(r0); r1 = byte_bias<KV>(r1); r2 = byte_bias<KV>(r2); r3 = byte_bias<KV>(r3);
               const uint32_t v0 = widen_pair<KV>(r0, 0x2404, 0x4240), v1 = widen_pair<KV>(r0, 0x3414, 0x4341);
               const uint32_t v2 = widen_pair<KV>(r1, 0x2404, 0x4240), v3 = widen_pair<KV>(r1, 0x3414, 0x4341);
               const uint32_t v4 = widen_pair<KV>(r2, 0x2404, 0x4240), v5 = widen_pair<KV>(r2, 0x3414, 0x4341);

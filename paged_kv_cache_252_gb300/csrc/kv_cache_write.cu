@@ -72,7 +72,9 @@ const void* kv_cache_write_kernel_ptr() { return reinterpret_cast<const void*>(&
 // for LMDeploy; the codec is ours): one warp quantises one (token, head) row of
 // K or V. scale = max|x| / 127 and code = round-half-even(x / scale) clamped to
 // [-127, 127]; both divisions are IEEE fp32 (__fdiv_rn), so the codes do not
-// depend on compiler flags. An all-zero row gets scale 0 and codes 0.
+// depend on compiler flags. An all-zero row gets scale 0 and codes 0. Codes are
+// stored in offset binary (byte = code + 128), which the decode kernel widens
+// to fp16 with a single byte permute.
 __global__ void __launch_bounds__(256) kv_cache_write_int8_kernel(const CacheWriteArgs a) {
   pdl_wait_prior_grid();
   const int lane = threadIdx.x & 31;
@@ -113,11 +115,11 @@ __global__ void __launch_bounds__(256) kv_cache_write_int8_kernel(const CacheWri
         qv = fmaxf(qv, -127.0f);
         qv = fminf(qv, 127.0f);
       }
-      packed |= (static_cast<uint32_t>(static_cast<int>(qv)) & 0xFFu) << (8 * i);
+      packed |= static_cast<uint32_t>(static_cast<int>(qv) + 128) << (8 * i);
     }
     const long long blk = slot / kBlockSize, off = slot - blk * kBlockSize;
     const long long row = (blk * a.num_kv_heads + h) * kBlockSize + off;
-    int8_t* dst = static_cast<int8_t*>(is_v ? a.v_cache : a.k_cache) + row * a.head_size + lane * per_lane;
+    uint8_t* dst = static_cast<uint8_t*>(is_v ? a.v_cache : a.k_cache) + row * a.head_size + lane * per_lane;
     if (per_lane == 4) {
       *reinterpret_cast<uint32_t*>(dst) = packed;
     } else {

@@ -73,7 +73,7 @@ def _check(orc, gpu, w, dev, *, seqs=None, values_device="cpu"):
     ks, vs = _split_scales(sc)
     vals = {k: v.cpu() for k, v in vals.items()}
     okc, ovc, oks, ovs = _oracle_caches(orc, w, vals)
-    assert np.array_equal(kc.cpu().numpy(), okc) and np.array_equal(vc.cpu().numpy(), ovc)
+    assert np.array_equal(pkv.int8_codes(kc).cpu().numpy(), okc) and np.array_equal(pkv.int8_codes(vc).cpu().numpy(), ovc)
     assert np.array_equal(ks, oks) and np.array_equal(vs, ovs)
     ref, _, rc = orc.paged_attention(bits16(vals["q"]), 0, w.q_per_seq, okc, ovc, 3, w.block_tables,
                                      w.context_lens, w.scale, seqs=seqs, num_threads=orc.hardware_threads(),
@@ -107,7 +107,7 @@ def test_int8_cache_write_bit_exact_on_hard_rows(orc, dev):
         ovs = np.zeros_like(oks)
         assert orc.kv_cache_write_int8(x.view(np.uint16), x[::-1].copy().view(np.uint16), slots,
                                        okc, ovc, oks, ovs) == 0
-        assert np.array_equal(kc.cpu().numpy(), okc) and np.array_equal(vc.cpu().numpy(), ovc)
+        assert np.array_equal(pkv.int8_codes(kc).cpu().numpy(), okc) and np.array_equal(pkv.int8_codes(vc).cpu().numpy(), ovc)
         ks, vs = _split_scales(sc)
         assert np.array_equal(ks, oks) and np.array_equal(vs, ovs)
         assert int(status.item()) == 0
@@ -190,7 +190,7 @@ def _check_packed(orc, gpu, w, dev, *, tree_masks=None, values_device="cpu"):
     ks, vs = _split_scales(sc)
     vals = {k: v.cpu() for k, v in vals.items()}
     okc, ovc, oks, ovs = _oracle_caches(orc, w, vals)
-    assert np.array_equal(kc.cpu().numpy(), okc) and np.array_equal(vc.cpu().numpy(), ovc)
+    assert np.array_equal(pkv.int8_codes(kc).cpu().numpy(), okc) and np.array_equal(pkv.int8_codes(vc).cpu().numpy(), ovc)
     assert np.array_equal(ks, oks) and np.array_equal(vs, ovs)
     ref, _, rc = orc.paged_attention(bits16(vals["q"]), 0, w.q_per_seq, okc, ovc, 3, w.block_tables,
                                      w.context_lens, w.scale, num_threads=orc.hardware_threads(),
