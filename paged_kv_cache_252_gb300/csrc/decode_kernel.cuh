@@ -352,15 +352,15 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
     }
 
     // INT8: kI8Bias * sum_d q[r][d] for this lane's rows (the 8 lanes of a row
-    // group each add D/8 dimensions), and the running sum of the P values the
-    // P V product uses, scaled by the V scales (lsv), for the output's bias.
-    float kq[NTW][2], lsv[NTW][2];
+    // group each add D/8 dimensions). The output's bias, kI8Bias times the running
+    // sum of the (V-scaled) P values the P V product uses, accumulates on the tensor
+    // core (o_bias: the P V product with every V element replaced by kI8Bias).
+    float kq[NTW][2];
 #pragma unroll
     for (int nt = 0; nt < NTW; ++nt)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         kq[nt][e] = 0.f;
-        lsv[nt][e] = 0.f;
         if constexpr (kInt8) {
           const uint8_t* qr = qs + (row_base + nt * 8 + 2 * c4 + e) * QS + g8 * (D / 4);
           float acc = 0.f;
@@ -383,6 +383,7 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
 
     float m_run[NTW][2], l_run[NTW][2];
     float o_acc[MT][NTW][4];
+    float o_bias[kInt8 ? NTW : 1][4];   // INT8: kI8Bias * sum of P per row (rows 2c4, 2c4+1, 2c4, 2c4+1)
     // Visibility of the n_s query (draft) tokens: the context before them,
     // positions < cb, is visible to every row; draft token i (position cb + i) is
     // visible to query token j when bit i of j's mask is set. Without tree masks
@@ -407,6 +408,7 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
       for (int mt = 0; mt < MT; ++mt) {
         o_acc[mt][nt][0] = o_acc[mt][nt][1] = o_acc[mt][nt][2] = o_acc[mt][nt][3] = 0.f;
       }
+      if constexpr (kInt8) o_bias[nt][0] = o_bias[nt][1] = o_bias[nt][2] = o_bias[nt][3] = 0.f;
     }
 
     const int k_first = ((wb - (i % WB)) % WB + WB) % WB;
@@ -533,12 +535,6 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
           // which is exactly the B operand of O^T += V^T P^T.
           const uint32_t h01 = pack_p<KV>(pv[0] * sv_lo, pv[1] * sv_lo);
           const uint32_t h23 = pack_p<KV>(pv[2] * sv_hi, pv[3] * sv_hi);
-          if constexpr (kInt8) {
-            const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
-            const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
-            lsv[nt][0] = lsv[nt][0] * alpha[nt][0] + (f01.x + f23.x);
-            lsv[nt][1] = lsv[nt][1] * alpha[nt][1] + (f01.y + f23.y);
-          }
           pb[nt][0] = movmatrix_t(h01);
           pb[nt][1] = movmatrix_t(h23);
           if constexpr (KV == kKvBf16) {
@@ -567,6 +563,15 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
               o_acc[mt][nt][2] *= alpha[nt][0];
               o_acc[mt][nt][3] *= alpha[nt][1];
             }
+          if constexpr (kInt8) {
+#pragma unroll
+            for (int nt = 0; nt < NTW; ++nt) {
+              o_bias[nt][0] *= alpha[nt][0];
+              o_bias[nt][1] *= alpha[nt][1];
+              o_bias[nt][2] *= alpha[nt][0];
+              o_bias[nt][3] *= alpha[nt][1];
+            }
+          }
         }
 
         // ---- O^T (head_size x rows) += V^T P^T ----
@@ -605,6 +610,13 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
                 mma_f16(o_acc[2 * mp + 1][nt], v4, v5, v6, v7, pb[nt][0], pb[nt][1]);
               }
             }
+            if constexpr (kInt8) {
+              // The bias product: every element of the A operand is kI8Bias (fp16 0x6480).
+              constexpr uint32_t kBias2 = 0x64806480u;
+#pragma unroll
+              for (int nt = 0; nt < NTW; ++nt)
+                mma_f16(o_bias[nt], kBias2, kBias2, kBias2, kBias2, pb[nt][0], pb[nt][1]);
+            }
           }
         }
       }
@@ -623,18 +635,9 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
 #pragma unroll
       for (int nt = 0; nt < NTW; ++nt)
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float t = lsv[nt][e];
-          t += __shfl_xor_sync(0xffffffffu, t, 4);
-          t += __shfl_xor_sync(0xffffffffu, t, 8);
-          t += __shfl_xor_sync(0xffffffffu, t, 16);
-          const float b = kI8Bias * t;
+        for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            o_acc[mt][nt][e] -= b;
-            o_acc[mt][nt][2 + e] -= b;
-          }
-        }
+          for (int e = 0; e < 4; ++e) o_acc[mt][nt][e] -= o_bias[nt][e];
     }
 #pragma unroll
     for (int nt = 0; nt < NTW; ++nt)
