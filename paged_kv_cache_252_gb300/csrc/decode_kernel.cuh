@@ -447,12 +447,26 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
           fence_proxy_async_smem();
         }
 
+        // INT8: this lane's K and V row scales (tokens g8 and g8+8 of the block),
+        // loaded before the S^T MMAs so that their latency overlaps them.
+        float sc_k_lo = 0.f, sc_k_hi = 0.f, sc_v_lo = 0.f, sc_v_hi = 0.f;
+        if constexpr (kInt8) {
+          const uint32_t sca = smem_addr(smem + lay.scales + stage * 128) + 4 * g8;
+          sc_k_lo = lds_f32_early(sca);
+          sc_k_hi = lds_f32_early(sca + 32);
+          sc_v_lo = lds_f32_early(sca + 64);
+          sc_v_hi = lds_f32_early(sca + 96);
+        }
+
         // ---- S^T (16 tokens x 8*NTW rows) = K Q^T, two independent chains ----
+        // (INT8: the first chain starts from -kq, which takes the K bias off the scores.)
         float sa[2][NTW][4];
 #pragma unroll
-        for (int x = 0; x < 2; ++x)
-#pragma unroll
-          for (int nt = 0; nt < NTW; ++nt) sa[x][nt][0] = sa[x][nt][1] = sa[x][nt][2] = sa[x][nt][3] = 0.f;
+        for (int nt = 0; nt < NTW; ++nt) {
+          sa[0][nt][0] = sa[0][nt][2] = -kq[nt][0];
+          sa[0][nt][1] = sa[0][nt][3] = -kq[nt][1];
+          sa[1][nt][0] = sa[1][nt][1] = sa[1][nt][2] = sa[1][nt][3] = 0.f;
+        }
         {
           const int mi = lane >> 3;
           const int tok = (lane & 7) + 8 * (mi & 1);
@@ -494,11 +508,10 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
         // where the stage may hold stale scales); the sums use the unscaled P.
         float sk_lo = a.scale_log2, sk_hi = a.scale_log2, sv_lo = 1.f, sv_hi = 1.f;
         if constexpr (kInt8) {
-          const float* sc = reinterpret_cast<const float*>(smem + lay.scales + stage * 128);
-          sk_lo *= sc[g8];
-          sk_hi *= sc[g8 + 8];
-          sv_lo = p_lo < ctx_eff ? sc[16 + g8] : 0.f;
-          sv_hi = p_hi < ctx_eff ? sc[16 + g8 + 8] : 0.f;
+          sk_lo *= sc_k_lo;
+          sk_hi *= sc_k_hi;
+          sv_lo = p_lo < ctx_eff ? sc_v_lo : 0.f;
+          sv_hi = p_hi < ctx_eff ? sc_v_hi : 0.f;
         }
         uint32_t pb[NTW][2];
         uint32_t pb_lo[NTW][2];   // bf16 only: P - bf16(P), a second bf16 term
@@ -508,8 +521,8 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
           float pv[4];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            float x_lo = ((sa[0][nt][e] + sa[1][nt][e]) - kq[nt][e]) * sk_lo;
-            float x_hi = ((sa[0][nt][2 + e] + sa[1][nt][2 + e]) - kq[nt][e]) * sk_hi;
+            float x_lo = (sa[0][nt][e] + sa[1][nt][e]) * sk_lo;
+            float x_hi = (sa[0][nt][2 + e] + sa[1][nt][2 + e]) * sk_hi;
             if (masked) {
               const bool v_lo = p_lo < cb || (p_lo < ctx_eff && p_lo - cb < 64 &&
                                                ((vis[nt][e] >> (p_lo - cb)) & 1ull));

@@ -145,6 +145,15 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// A 32-bit shared-memory load issued where it stands in the instruction stream
+// (volatile: the compiler does not sink it towards its first use), so that its
+// latency overlaps the work in between.
+__device__ __forceinline__ float lds_f32_early(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+
 // ---- warp-level matrix data movement ---------------------------------------------
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                         uint32_t& r3) {
