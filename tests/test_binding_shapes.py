@@ -114,3 +114,16 @@ def test_int8_scales_go_with_an_int8_cache_only():
     with _pt.raises(pkv.PagedKVError):
         pkv.api._int8_scales(pkv.api.KV_FP16, kc8, torch.zeros(4, 2, 2, 16))
     pkv.api._int8_scales(pkv.api.KV_FP16, kc8, None)
+
+
+def test_int8_cache_bytes_are_offset_binary_codes():
+    """A fresh INT8 cache holds code 0 (byte 0x80); int8_codes reads byte u as u - 128."""
+    kc, vc = api.alloc_kv_cache(2, 1, 64, "int8", "cpu")
+    assert kc.dtype == torch.int8 and int(kc.view(torch.uint8)[0, 0, 0, 0]) == 0x80
+    assert int(api.int8_codes(kc).abs().max()) == 0 and int(api.int8_codes(vc).abs().max()) == 0
+    raw = torch.tensor([0x01, 0x7F, 0x80, 0x81, 0xFF], dtype=torch.uint8).view(torch.int8)
+    assert api.int8_codes(raw).tolist() == [-127, -1, 0, 1, 127]
+    with pytest.raises(api.PagedKVError):
+        api.int8_codes(torch.zeros(4, dtype=torch.uint8))
+    e, _ = api.alloc_kv_cache(2, 1, 64, "e5m2", "cpu")
+    assert e.dtype == torch.uint8 and int(e.max()) == 0
