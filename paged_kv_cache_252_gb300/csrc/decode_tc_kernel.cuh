@@ -44,7 +44,7 @@
 //
 // Pipeline per chunk c (softmax warps): read S(c); widen K(c+1) (+ Q of a new
 // piece) -> the MMA thread issues S(c+1) while the softmax of chunk c runs;
-// wait O(c-1); write P(c); widen V(c+1) -> the MMA thread issues O(c).
+// wait O(c-1); write P(c) -> the MMA thread issues O(c) while V(c+1) is widened.
 // P^T is single-buffered; K (TMEM), S^T (TMEM), V16 and Q double-buffered.
 #pragma once
 
@@ -94,9 +94,11 @@ __device__ __forceinline__ float select_lane32(float (&v)[32], int lane) {
 
 // Bounded mbarrier wait in which a waiting warp sleeps (takes no issue slots)
 // until the phase completes; it gives up after kWaitLimitNs or once another
-// warp of the CTA has given up (abort flag).
+// warp of the CTA has given up (abort flag). A phase that is already complete
+// is seen by a plain test first (the test with a suspend hint costs more).
 constexpr uint32_t kTcSleepNs = 1000000;
 __device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
   if (mbar_try_wait_sleep(bar, parity, kTcSleepNs)) return true;
   const uint64_t t0 = global_timer_ns();
   for (;;) {
@@ -827,16 +829,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
 
+        // P(c) is written (and V(c) was widened a chunk ago): the MMA thread may issue O(c).
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        if (alive) mbar_arrive(bar_pvready);
+
         PKV_TL_STEP(7);
         // (5) V of chunk c+1 (its buffer was read by O(c-1)); release the ring buffer.
+        //     These writes are ordered for the tensor core by the fence before the
+        //     next chunk's arrival.
         if (has_next) {
           if (alive) widen_e5m2_half_row(ring_next + kTcChunk * TILE, v16 + ((c + 1) & 1) * kWide, t, hh, valid_next);
           __syncwarp();
           if (alive && lane == 0) mbar_arrive(bars + 8 * (nbuf + buf_next));
         }
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        if (alive) mbar_arrive(bar_pvready);
 
         PKV_TL_STEP(8);
         // (6) end of a piece: normalise and write, or write the split partial.
