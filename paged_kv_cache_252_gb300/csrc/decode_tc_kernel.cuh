@@ -95,16 +95,21 @@ __device__ __forceinline__ float select_lane32(float (&v)[32], int lane) {
 // Bounded mbarrier wait in which a waiting warp sleeps (takes no issue slots)
 // until the phase completes; it gives up after kWaitLimitNs or once another
 // warp of the CTA has given up (abort flag). A phase that is already complete
-// is seen by a plain test first (the test with a suspend hint costs more).
+// is seen by a plain test first (the test with a suspend hint costs more); the
+// rest is one out-of-line function, so the many inlined waits of the chunk loop
+// stay small for the instruction cache.
 constexpr uint32_t kTcSleepNs = 1000000;
-__device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
+static __device__ __noinline__ bool tc_wait_sleeping(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   if (mbar_try_wait_sleep(bar, parity, kTcSleepNs)) return true;
   const uint64_t t0 = global_timer_ns();
   for (;;) {
     if (mbar_try_wait_sleep(bar, parity, kTcSleepNs)) return true;
     if (*abort_flag || global_timer_ns() - t0 > kWaitLimitNs) return false;
   }
+}
+__device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return tc_wait_sleeping(bar, parity, abort_flag);
 }
 
 // Widen half `half` (dimensions 64*half .. 64*half+63) of token row t of an
