@@ -56,7 +56,7 @@ int g_timeline_ctas = 0;
 #define PKV_PIECE_COST_1B 8
 #endif
 #ifndef PKV_PIECE_COST_TC
-#define PKV_PIECE_COST_TC 24
+#define PKV_PIECE_COST_TC 20
 #endif
 constexpr int kPieceCost2B = PKV_PIECE_COST_2B;   // mma.sync kernel, fp16 / bf16 cache
 constexpr int kPieceCost1B = PKV_PIECE_COST_1B;   // mma.sync kernel, E5M2 / INT8 cache
