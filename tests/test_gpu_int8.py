@@ -141,6 +141,17 @@ def test_int8_workload_full_size(orc, dev, gpu):
     _check(orc, gpu, wl.by_name("8b_int8"), dev, values_device=dev)
 
 
+def test_int8_single_token_contexts_are_exact_up_to_the_output_rounding(orc, dev, gpu):
+    """Contexts of one or two tokens put a single token's dequantised V row (code *
+    scale) in the output with weight ~1: the fp16 rounding of P * scale must not
+    reach the output. Many rows of N(0,1) values give row maxima near 4, where the
+    scale's fp16 rounding and the output's are each worth up to ~1.95e-3."""
+    S = 256
+    w = wl.custom(num_seqs=S, num_q_heads=8, num_kv_heads=8, head_size=128, q_per_seq=1, kv_dtype="int8",
+                  context_lens=[1 + (s % 2) for s in range(S)], seed=4242)
+    _check(orc, gpu, w, dev)
+
+
 def test_int8_bad_block_is_flagged_not_faulted(orc, dev, gpu):
     import paged_kv_cache_252_gb300 as pkv
     w = wl.custom(num_seqs=3, num_q_heads=8, num_kv_heads=2, head_size=128, q_per_seq=1, kv_dtype="int8",
