@@ -29,8 +29,8 @@ struct DeviceState {
   bool ready = false;
   int sm_count = 0;
   bool write_attr_done = false;
-  // [kv][d==128][ntw==2]
-  GeomEntry geom[4][2][2];
+  // [kv][d==128][kernel: 0 = NTW 1, 1 = NTW 2, 2 = the 96-thread kernel for narrow units]
+  GeomEntry geom[4][2][3];
   // tcgen05 kernel, [rc - 1]
   GeomEntry tc_geom[2];
 };
@@ -88,6 +88,14 @@ int current_device_state(DeviceState** out) {
   }
   *out = &st;
   return PKV_OK;
+}
+
+// The 96-thread kernel of its own register budget for units of at most 8 rows
+// over a bf16 cache (at four CTAs per SM it beat the shared kernel at five: long
+// bf16 decode 424.1 -> 412.3 us; with an fp16 cache it measured 57.1 -> 57.3 us on
+// the 8B workload, and on 1-byte caches a larger budget was slower).
+const void* decode_narrow_fn(int kv, int d) {
+  return kv == kKvBf16 ? decode_kernel_narrow_ptr_bf16(d) : nullptr;
 }
 
 const void* decode_fn(int kv, int d, int ntw) {
@@ -155,13 +163,15 @@ DecodeGeometry choose_tc_geometry(int rows) {
 int get_geometry(DeviceState* st, int kv, int d, int rows, GeomEntry** out) {
   const bool tc = use_tc(kv, d, rows);
   const DecodeGeometry g0 = tc ? choose_tc_geometry(rows) : choose_geometry(kv, d, rows);
-  GeomEntry& e = tc ? st->tc_geom[g0.rc - 1] : st->geom[kv][d == 128 ? 1 : 0][g0.ntw == 2 ? 1 : 0];
+  const bool narrow = !tc && g0.warps_rows == 1 && g0.ntw == 1 && decode_narrow_fn(kv, d) != nullptr;
+  GeomEntry& e = tc ? st->tc_geom[g0.rc - 1]
+                    : st->geom[kv][d == 128 ? 1 : 0][narrow ? 2 : (g0.ntw == 2 ? 1 : 0)];
   // The cached entry is keyed by (kv, d, ntw); the row count also changes the
   // warp grid and the merge-buffer size, so re-derive and compare.
   if (!e.ready || e.geom.warps_rows != g0.warps_rows || e.geom.warps_blocks != g0.warps_blocks ||
       e.geom.stages != g0.stages || e.geom.smem_bytes != g0.smem_bytes || e.geom.tc != g0.tc ||
       e.geom.rc != g0.rc) {
-    const void* fn = tc ? decode_tc_kernel_ptr(kv, g0.rc) : decode_fn(kv, d, g0.ntw);
+    const void* fn = tc ? decode_tc_kernel_ptr(kv, g0.rc) : (narrow ? decode_narrow_fn(kv, d) : decode_fn(kv, d, g0.ntw));
     if (!fn) return PKV_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(g0.smem_bytes)) != cudaSuccess) {

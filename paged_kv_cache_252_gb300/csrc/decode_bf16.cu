@@ -11,5 +11,11 @@ const void* decode_kernel_ptr_bf16(int d, int ntw) {
   return nullptr;
 }
 
+// Units of at most 8 rows: the 96-thread kernel with 144 registers.
+const void* decode_kernel_narrow_ptr_bf16(int d) {
+  if (d == 64) return reinterpret_cast<const void*>(&decode_kernel_narrow<1, 64, 144>);
+  if (d == 128) return reinterpret_cast<const void*>(&decode_kernel_narrow<1, 128, 144>);
+  return nullptr;
+}
 
 }  // namespace pkv

@@ -11,5 +11,4 @@ const void* decode_kernel_ptr_f16(int d, int ntw) {
   return nullptr;
 }
 
-
 }  // namespace pkv

@@ -100,11 +100,12 @@ __device__ __forceinline__ void mma_kv(float (&d)[4], uint32_t a0, uint32_t a1, 
   }
 }
 
+// The decode CTA's work (inlined into the kernels below; tm_* and a are their
+// grid-constant parameters).
 template <int KV, int D, int NTW>
-__global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
-    decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const __grid_constant__ CUtensorMap tm_k1, const __grid_constant__ CUtensorMap tm_v1,
-                  const DecodeArgs a) {
+__device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                            const CUtensorMap& tm_k1, const CUtensorMap& tm_v1,
+                                            const DecodeArgs& a) {
   constexpr int RB = tile_row_bytes(KV, D);   // bytes of one token row of a tile
   constexpr int TILE = tile_bytes(KV, D);     // bytes of one (block, head) tile
   constexpr int KS = D / 16;                  // k-steps of S^T = K Q^T
@@ -765,6 +766,26 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
     PKV_TL_SET(a, kTlInfo, sm_id() | (tl_pieces << 16) | (tl_blocks << 32));
   }
 #endif
+}
+
+template <int KV, int D, int NTW>
+__global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
+    decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ CUtensorMap tm_k1, const __grid_constant__ CUtensorMap tm_v1,
+                  const DecodeArgs a) {
+  decode_body<KV, D, NTW>(tm_k, tm_v, tm_k1, tm_v1, a);
+}
+
+// Units of at most 8 rows (one row warp, two block-stream warps and the producer:
+// 96 threads) with a register budget of its own (REGS; the shared kernel above
+// stays within 128 so that three 160-thread CTAs fit an SM): four such CTAs per SM
+// instead of five, with fewer instructions spent working around a register limit.
+template <int KV, int D, int REGS>
+__global__ void __launch_bounds__(96) __maxnreg__(REGS)
+    decode_kernel_narrow(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                         const __grid_constant__ CUtensorMap tm_k1, const __grid_constant__ CUtensorMap tm_v1,
+                         const DecodeArgs a) {
+  decode_body<KV, D, 1>(tm_k, tm_v, tm_k1, tm_v1, a);
 }
 
 }  // namespace pkv

@@ -138,6 +138,8 @@ const void* decode_kernel_ptr_f16(int d, int ntw);
 const void* decode_kernel_ptr_bf16(int d, int ntw);
 const void* decode_kernel_ptr_e5m2(int d, int ntw);
 const void* decode_kernel_ptr_int8(int d, int ntw);
+// The 96-thread kernel for units of at most 8 rows over a bf16 cache (nullptr if none).
+const void* decode_kernel_narrow_ptr_bf16(int d);
 const void* kv_cache_write_kernel_ptr();
 const void* kv_cache_write_int8_kernel_ptr();
 
