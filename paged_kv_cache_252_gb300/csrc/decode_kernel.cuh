@@ -781,7 +781,7 @@ __global__ void __launch_bounds__(160, NTW == 1 ? 3 : 2)
 // stays within 128 so that three 160-thread CTAs fit an SM): four such CTAs per SM
 // instead of five, with fewer instructions spent working around a register limit.
 template <int KV, int D, int REGS>
-__global__ void __launch_bounds__(96) __maxnreg__(REGS)
+__global__ void __maxnreg__(REGS)
     decode_kernel_narrow(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                          const __grid_constant__ CUtensorMap tm_k1, const __grid_constant__ CUtensorMap tm_v1,
                          const DecodeArgs a) {
