@@ -197,6 +197,10 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
     int pst = 0;           // i % stages
     uint32_t pwrap = 0;    // (i / stages) & 1
     bool ok = true;
+#ifdef PKV_TIMELINE
+    long long tl_pwait = 0;
+    const long long tl_p0 = clock64();
+#endif
     while (ub < b1 && ok) {
       const int take = static_cast<int>(min(static_cast<long long>(nb), b1 - ub)) - lb;
       const int32_t* bt = a.block_tables + static_cast<size_t>(s) * mbs + lb;
@@ -210,7 +214,14 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
           int good = ok ? 1 : 0;
           if (lane == 0 && good) {
             const int stage = pst;
+#ifdef PKV_TIMELINE
+            const long long tl_w0 = clock64();
+            const bool got = i < stages || wait_or_abort(bars + 8 * (stages + stage), pwrap ^ 1u, abort_flag);
+            tl_pwait += clock64() - tl_w0;
+            if (!got) {
+#else
             if (i >= stages && !wait_or_abort(bars + 8 * (stages + stage), pwrap ^ 1u, abort_flag)) {
+#endif
               good = 0;
               *abort_flag = 1;
               if (a.status) atomicOr(a.status, kDevTimeout);
@@ -265,6 +276,12 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
       }
     }
     if (lane == 0) PKV_TL(a, kTlLastIssue);
+#ifdef PKV_TIMELINE
+    if (lane == 0) {
+      PKV_TL_SET(a, kTlProdWait, tl_pwait);
+      PKV_TL_SET(a, kTlProdTotal, clock64() - tl_p0);
+    }
+#endif
     // Drain: every copy issued into this CTA's shared memory lands before exit.
     if (lane == 0) {
       for (int k = (i > stages ? i - stages : 0); k < i; ++k) {
@@ -287,9 +304,12 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
   uint32_t cph = 0;      // (ib / stages) & 1
 #ifdef PKV_TIMELINE
   unsigned long long tl_blocks = 0, tl_pieces = 0;
+  // Consumer thread 0's cycles per phase, summed over pieces (timeline.py MMA_STEPS).
+  PKV_TL_STEP_BEGIN;
 #endif
 
   while (ub < b1) {
+    if (tid == 0) PKV_TL_STEP(7);
     const int take = static_cast<int>(min(static_cast<long long>(nb), b1 - ub)) - lb;
     const bool first = (lb == 0), last = (lb + take == nb);
     const bool split = !(first && last);
@@ -327,6 +347,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
           *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) + src);
     }
     named_bar_sync(1, nthr_c);
+    if (tid == 0) PKV_TL_STEP(0);
 
     // B fragments of Q^T for this warp's rows (held for the whole piece).
     uint32_t qf[NTW][KS][2];
@@ -412,6 +433,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
       if constexpr (kInt8) o_bias[nt][0] = o_bias[nt][1] = o_bias[nt][2] = o_bias[nt][3] = 0.f;
     }
 
+    if (tid == 0) PKV_TL_STEP(1);
     const int k_first = ((wb - (i % WB)) % WB + WB) % WB;
     for (int k = k_first; k < take; k += WB) {
       const int stage = cst;
@@ -427,6 +449,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
         *abort_flag = 1;
         if (lane == 0 && a.status) atomicOr(a.status, kDevTimeout);
       }
+      if (tid == 0) PKV_TL_STEP(2);
 #ifdef PKV_TIMELINE
       if (tid == 0 && tl_blocks == 0) PKV_TL(a, kTlFirstData);
       tl_blocks += (tid == 0);
@@ -652,6 +675,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bars + 8 * (stages + stage));
+      if (tid == 0) PKV_TL_STEP(3);
     }
     if (tid == 0) PKV_TL(a, kTlLastData);
     i += take;
@@ -704,6 +728,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
       }
     }
     named_bar_sync(2, nthr_c);
+    if (tid == 0) PKV_TL_STEP(4);
     for (int idx = tid; idx < Rs * (D / 4); idx += nthr_c) {
       const int r = idx / (D / 4), d4 = idx - (idx / (D / 4)) * (D / 4);
       float M = kNegInf;
@@ -742,10 +767,12 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
     }
 
     if (tid == 0) PKV_TL(a, kTlPieceOut);
+    if (tid == 0) PKV_TL_STEP(5);
     if (split) {
       finish_split_piece_smem<KV, D>(a, u, ub, nb, total, ncta, Rs, qb, h, tid, nthr_c, 3, fin, fin_cur, mrg_o,
                                      D + 4, fin_ml);
     }
+    if (tid == 0) PKV_TL_STEP(6);
 
     // ---- advance the walk (a piece that stops before the unit's end ended the share) ----
     if (lb + take < nb) break;
@@ -764,6 +791,8 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
   if (tid == 0) {
     PKV_TL(a, kTlExit);
     PKV_TL_SET(a, kTlInfo, sm_id() | (tl_pieces << 16) | (tl_blocks << 32));
+    PKV_TL_STEP(7);
+    PKV_TL_STEP_FLUSH(a);
   }
 #endif
 }

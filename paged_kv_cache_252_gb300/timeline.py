@@ -34,6 +34,10 @@ NEV = 28                                     # 64-bit words per CTA (pkv_timelin
 STEP_NAMES = ["top: next chunk / queries", "wait S + read scores", "wait ring (next chunk)",
               "widen K (next chunk)", "scores, max vote", "rare rescale", "wait O (previous chunk)",
               "exp2 + write P", "widen V (next chunk)", "end of piece"]
+# mma.sync kernel: SM cycles of consumer thread 0 summed over the CTA's pieces, per
+# phase (words 12..19), and the producer's wait for a free ring stage (words 25, 26)
+MMA_STEPS = ["query rows load + barrier", "Q fragments, masks", "wait for a block", "block compute",
+             "stream merge (barrier)", "merge + output", "split finish", "next piece / exit"]
 MAX_CTAS = 4096
 
 
@@ -137,7 +141,19 @@ def summarize(w, rows, event_us: float | None = None) -> str:
             lines.append(f"| {name} - last_data ({int(ok.sum())} CTAs) | " + " | ".join(f"{x:.2f}" for x in q) + " |")
     steps = rows[:, 12:12 + len(STEP_NAMES)].astype(np.float64)
     chunks = ((info >> 32) // 8).astype(np.float64)          # tcgen05 kernel: blocks / 8 per chunk
-    if steps[busy].sum() > 0:
+    is_tc = rows[busy, 24].astype(np.float64).sum() > 0      # only the tcgen05 kernel's MMA thread writes 24
+    if steps[busy].sum() > 0 and not is_tc:
+        per = steps[busy][:, :len(MMA_STEPS)]
+        tot = per.sum(axis=1)
+        lines += ["", "mma.sync consumer thread 0, SM cycles per CTA summed over its pieces:",
+                  "| phase | median cycles | share of the CTA's total |", "|---|---|---|"]
+        for k, name in enumerate(MMA_STEPS):
+            lines.append(f"| {name} | {np.median(per[:, k]):.0f} | {np.median(per[:, k] / tot):.3f} |")
+        lines.append(f"| total | {np.median(tot):.0f} | 1 |")
+        prod = rows[busy, 25:27].astype(np.float64)
+        lines.append(f"producer: waiting for a free stage {np.median(prod[:, 0]):.0f} of "
+                     f"{np.median(prod[:, 1]):.0f} cycles (median per CTA)")
+    if steps[busy].sum() > 0 and is_tc:
         per = steps[busy] / np.maximum(chunks[busy], 1)[:, None]
         lines += ["", "tcgen05 chunk loop, SM cycles per chunk (median over CTAs):",
                   "| step (softmax thread 0) | cycles |", "|---|---|"]
@@ -182,7 +198,7 @@ def main(argv=None):
     w, rows, event_us = run(args.config, args.num_seqs, args.iters)
     print(summarize(w, rows, event_us))
     if args.raw:
-        hdr = ",".join(EVENTS + ["sm", "pieces", "blocks"] + LATE)
+        hdr = ",".join(EVENTS + ["sm", "pieces", "blocks"] + LATE + [f"w{k}" for k in range(12, 27)])
         t0 = rows[:, :7][rows[:, :7] > 0].min()
         with open(args.raw, "w") as f:
             f.write(hdr + "\n")
@@ -190,7 +206,7 @@ def main(argv=None):
                 ev = [f"{(int(x) - int(t0)) / 1e3:.3f}" if x else "" for x in r[:7]]
                 late = [f"{(int(x) - int(t0)) / 1e3:.3f}" if x else "" for x in r[8:11]]
                 f.write(",".join(ev + [str(int(r[7]) & 0xFFFF), str((int(r[7]) >> 16) & 0xFFFF),
-                                       str(int(r[7]) >> 32)] + late) + "\n")
+                                       str(int(r[7]) >> 32)] + late + [str(int(x)) for x in r[12:27]]) + "\n")
 
 
 if __name__ == "__main__":

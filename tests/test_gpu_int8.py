@@ -235,10 +235,17 @@ INT8_TREES = [
     (128, 64, 8, 4),
     (128, 32, 8, [5, 1, 8, 3, 2]),
     (64, 8, 4, [16, 3, 9]),
+    # two row groups, with sequences whose rows fit one group
+    (128, 32, 8, [4, 1, 2, 1, 3]),
 ]
 
 
-@pytest.mark.parametrize("case", INT8_TREES, ids=[f"D{c[0]}-G{c[1] // c[2]}" for c in INT8_TREES])
+def _int8_tree_id(c):
+    n = c[3] if isinstance(c[3], int) else max(c[3])
+    return f"D{c[0]}-G{c[1] // c[2]}-n{n}"
+
+
+@pytest.mark.parametrize("case", INT8_TREES, ids=[_int8_tree_id(c) for c in INT8_TREES])
 def test_int8_tree_verify_parity(orc, dev, gpu, case):
     D, Hq, Hkv, ql = case
     S = 5 if isinstance(ql, int) else len(ql)

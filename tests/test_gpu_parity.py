@@ -248,10 +248,15 @@ VARLEN = [
     ("bf16", 64, 16, 4, [2, 1, 4, 1, 1, 3]),
     ("e5m2", 128, 64, 8, [4, 1, 2, 4, 1]),
     ("fp16", 64, 8, 1, [1, 8, 3, 1, 5, 2]),
+    # units of 9..16 rows run two row groups; a sequence whose rows fit one group
+    # spreads its blocks over every consumer warp (12 rows: 6 per group)
+    ("fp16", 128, 12, 4, [1, 2, 3, 4, 1, 2, 3, 1]),
+    ("e5m2", 128, 32, 8, [1, 4, 2, 1, 3, 1]),
+    ("e5m2", 64, 32, 8, [2, 1, 1, 4, 1, 3]),
 ]
 
 
-@pytest.mark.parametrize("case", VARLEN, ids=[f"{c[0]}-D{c[1]}-G{c[2] // c[3]}" for c in VARLEN])
+@pytest.mark.parametrize("case", VARLEN, ids=[f"{c[0]}-D{c[1]}-G{c[2] // c[3]}-n{max(c[4])}" for c in VARLEN])
 def test_varlen_parity(orc, dev, gpu, case):
     kv, D, Hq, Hkv, q_lens = case
     lens = [max(l, ql) for l, ql in zip([1, 17, 300, 16, 64, 1000, 33, 129], q_lens)]
@@ -325,10 +330,18 @@ TREES = [
     ("fp16", 128, 32, 8, [5, 1, 8, 3, 2]),
     ("bf16", 64, 8, 4, [16, 3, 9]),
     ("fp16", 64, 4, 4, 16),
+    # two row groups, with sequences whose rows fit one group
+    ("fp16", 128, 32, 8, [4, 1, 2, 1, 3]),
+    ("bf16", 64, 12, 4, [1, 2, 4, 3, 1]),
 ]
 
 
-@pytest.mark.parametrize("case", TREES, ids=[f"{c[0]}-D{c[1]}-G{c[2] // c[3]}" for c in TREES])
+def _tree_id(c):
+    n = c[4] if isinstance(c[4], int) else max(c[4])
+    return f"{c[0]}-D{c[1]}-G{c[2] // c[3]}-n{n}"
+
+
+@pytest.mark.parametrize("case", TREES, ids=[_tree_id(c) for c in TREES])
 def test_tree_verify_parity(orc, dev, gpu, case):
     import paged_kv_cache_252_gb300 as pkv
     kv, D, Hq, Hkv, ql = case
