@@ -192,13 +192,38 @@ def decode_family(w) -> str:
     return "tc" if (w.kv_dtype == "e5m2" and w.head_size == 128 and rows > 16) else "mma"
 
 
+def product_source(text: str) -> str:
+    """A source file as the product library compiles it, as far as the profiling
+    build's hooks go: the branches of `#ifdef PKV_TIMELINE` blocks and the lines that
+    call the PKV_TL* macros (which expand to nothing without PKV_TIMELINE) are left
+    out; `#else` branches are kept."""
+    out, stack = [], []      # stack: per open #if*, whether its current branch is dropped
+    for line in text.splitlines(keepends=True):
+        t = line.strip()
+        if t.startswith("#if"):
+            stack.append(t == "#ifdef PKV_TIMELINE")
+            if stack[-1]:
+                continue
+        elif t.startswith("#else") and stack:
+            if stack[-1] is not False:
+                stack[-1] = "else"
+                continue
+        elif t.startswith("#endif") and stack:
+            if stack.pop() is not False:
+                continue
+        if any(x is True for x in stack) or "PKV_TL" in line:
+            continue
+        out.append(line)
+    return "".join(out)
+
+
 def csrc_digest(family: str) -> str:
     src = hashlib.sha256()
     d = os.path.join(ROOT, "paged_kv_cache_252_gb300", "csrc")
     for fn in sorted(_DECODE_COMMON + _DECODE_FAMILY[family]):
-        with open(os.path.join(d, fn), "rb") as f:
+        with open(os.path.join(d, fn), encoding="utf-8") as f:
             src.update(fn.encode())
-            src.update(f.read())
+            src.update(product_source(f.read()).encode())
     return src.hexdigest()
 
 

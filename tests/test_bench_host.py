@@ -77,3 +77,19 @@ def test_reference_arm_reports_the_same_config():
         a = bench.bench_config(w, pools, l2, 1)
         b = bench.bench_config(wl.by_name(key), bench.pool_count(wl.by_name(key), l2), l2, 1)
         assert a == b and a["workload"] == w.name and "l2_policy" in a
+
+
+def test_product_source_drops_only_profiling_hooks():
+    """The traffic digest covers the source the product library compiles: the
+    PKV_TIMELINE branches and PKV_TL* hook lines go, their #else branches and all
+    other preprocessor blocks stay."""
+    text = ("a();\n"
+            "#ifdef PKV_TIMELINE\n  t0 = clock64();\n  if (!got) {\n#else\n  if (x) {\n#endif\n"
+            "  if (tid == 0) PKV_TL_STEP(3);\n"
+            "#if defined(OTHER)\n  b();\n#else\n  c();\n#endif\n"
+            "#ifdef PKV_TIMELINE\n  only_profiling();\n#endif\n"
+            "d();\n")
+    assert bench.product_source(text) == ("a();\n  if (x) {\n#if defined(OTHER)\n  b();\n#else\n  c();\n#endif\n"
+                                          "d();\n")
+    # a change outside the hooks changes the digest input
+    assert bench.product_source(text.replace("d();", "e();")) != bench.product_source(text)
