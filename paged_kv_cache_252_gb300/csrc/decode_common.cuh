@@ -57,6 +57,25 @@ __device__ __forceinline__ uint32_t pack_p(float lo, float hi) {
   }
 }
 
+// Before the wait for the previous grid: bring into L2 the lines the plan and the
+// first copies read, context_lens (every CTA plans from all of it) and the block
+// tables (each CTA fetches its slice of them, so the grid fetches them all; skipped
+// when a slice would exceed 32 lines). L2 is where a previous grid's writes land,
+// so a line fetched early still reads current after the wait; nothing is read here.
+// Out of line: inlined, its few registers shifted the kernels' allocation.
+static __device__ __noinline__ void prefetch_plan_inputs(const int32_t* context_lens, const int32_t* block_tables,
+                                                        int num_seqs, int max_blocks_per_seq) {
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  for (int line = tid; line < (num_seqs + 31) / 32; line += nthr) prefetch_l2(context_lens + 32 * line);
+  // Lines of the block tables (32 entries each; the host keeps num_seqs * max_blocks_per_seq < 2^31).
+  const int bt_lines = static_cast<int>((static_cast<long long>(num_seqs) * max_blocks_per_seq + 31) / 32);
+  const int per = (bt_lines + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+  if (per <= 32 && tid < per) {
+    const long long line = static_cast<long long>(blockIdx.x) * per + tid;
+    if (line < bt_lines) prefetch_l2(block_tables + 32 * line);
+  }
+}
+
 // The work is a line of positions: unit (s, h) in order, each a fixed
 // a.piece_cost positions (its per-piece work: queries, epilogue, split merge,
 // counted in blocks) followed by one position per KV block. CTAs take equal

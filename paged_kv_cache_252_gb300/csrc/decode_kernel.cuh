@@ -159,6 +159,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
     reinterpret_cast<uint4*>(qs + R * QS)[idx] = make_uint4(0, 0, 0, 0);
   }
 
+  prefetch_plan_inputs(a.context_lens, a.block_tables, a.num_seqs, a.max_blocks_per_seq);
   // Everything below reads inputs a previous kernel in the stream may write.
   pdl_wait_prior_grid();
 

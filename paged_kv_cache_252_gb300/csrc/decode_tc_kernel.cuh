@@ -476,6 +476,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
+  prefetch_plan_inputs(a.context_lens, a.block_tables, a.num_seqs, a.max_blocks_per_seq);
   // Everything below reads inputs a previous kernel in the stream may write.
   pdl_wait_prior_grid();
   tc_plan(a, red, plan);

@@ -235,6 +235,12 @@ __device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t nthreads, bool 
   return r != 0;
 }
 
+// Fetch the 128-byte line holding p into L2 (no register result, no fault on any
+// address the caller could load).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)) : "memory");
+}
+
 // ---- programmatic dependent launch ---------------------------------------------
 __device__ __forceinline__ void pdl_wait_prior_grid() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
