@@ -369,13 +369,13 @@ int orc_paged_attention(double* out, double* weights, int64_t weights_stride,
       // Query token j is position ctx - n + j. The context before the n query
       // (draft) tokens is visible to all of them; draft token i (position
       // ctx - n + i) is visible to token j when bit i of j's tree mask is set —
-      // without tree masks, when i <= j (causal among the query tokens).
+      // without tree masks, when i <= j (causal among the query tokens, for any n).
       const int base = ctx - n;
-      const uint64_t mask = tree_masks ? tree_masks[first_row(s) + j]
-                                       : (j >= 63 ? ~0ull : ((2ull << j) - 1ull));
+      const uint64_t mask = tree_masks ? tree_masks[first_row(s) + j] : 0ull;
       auto visible = [&](int p) {
         if (p < base) return true;
         const int i = p - base;
+        if (!tree_masks) return i <= j;
         return i < 64 && ((mask >> i) & 1ull) != 0;
       };
       const int limit = ctx;   // positions 0 .. ctx-1 exist

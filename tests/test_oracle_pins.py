@@ -407,6 +407,22 @@ def test_varlen_matches_sdpa_and_per_sequence_runs(orc):
         assert np.array_equal(out[cu[s]:cu[s + 1]], one)
 
 
+def test_long_query_chunks_are_causal_past_64_tokens(orc):
+    """Prefill chunks longer than 64 tokens mixed with decodes: every query token j
+    sees positions <= ctx - n + j, however far past the 64th draft position (SDPA with
+    the explicit causal mask is the reference)."""
+    q_lens = [1, 150, 3, 70]
+    w = wl.custom(num_seqs=4, num_q_heads=4, num_kv_heads=2, head_size=64, q_per_seq=150,
+                  kv_dtype="fp16", context_lens=[9, 230, 40, 70], seed=61, q_lens=q_lens)
+    vals = wl.token_values(w)
+    kc, vc = oracle_caches(orc, w, vals)
+    out, _, rc = oracle_attention(orc, w, vals, kc, vc)
+    assert rc == 0
+    cu = w.cu_q_lens()
+    for s in range(w.num_seqs):
+        np.testing.assert_allclose(out[cu[s]:cu[s + 1]], sdpa_reference(w, vals, s), rtol=1e-10, atol=1e-12)
+
+
 def test_varlen_with_equal_counts_is_the_uniform_batch(orc):
     w = wl.custom(num_seqs=3, num_q_heads=4, num_kv_heads=2, head_size=64, q_per_seq=2,
                   kv_dtype="fp16", context_lens=[5, 33, 18], seed=23)
