@@ -131,11 +131,14 @@ size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t
  *                 calls in flight at the same time must not share a workspace.
  *                 A call may be captured in a CUDA graph and replayed: every
  *                 launch leaves the workspace's counters clear when it completes.
- *                 The counters are tagged with a per-call number, so counters
- *                 left by an earlier call read as clear; a replayed graph reuses
- *                 its call's number, so after a launch that reported
- *                 PKV_DEV_TIMEOUT (its counters may be left part-way) zero the
- *                 workspace (e.g. cudaMemsetAsync) before replaying that graph.
+ *                 The counters are tagged with a per-call number (a scrambled
+ *                 call count that does not repeat within 2^32 calls), so counters
+ *                 left by an earlier call read as clear, and other data left in
+ *                 the buffer matches a tag only by a 2^-32 chance per 8-byte word
+ *                 (zero a buffer that held other data once if that matters). A
+ *                 replayed graph reuses its call's number, so after a launch that
+ *                 reported PKV_DEV_TIMEOUT (its counters may be left part-way)
+ *                 zero the workspace (e.g. cudaMemsetAsync) before replaying it.
  *
  *   For each sequence s, query head hq (KV head h = hq / (num_q_heads/num_kv_heads))
  *   and query token j, with L = context_lens[s] - q_per_seq + j + 1:
@@ -304,6 +307,46 @@ int pkv_paged_attention_decode_int8_tree(void* out, const void* q, const int32_t
                                          const int32_t* block_tables, int32_t max_blocks_per_seq,
                                          const int32_t* context_lens, float scale, void* workspace,
                                          size_t workspace_bytes, int32_t* device_status, void* stream);
+
+/*
+ * pkv_paged_attention_decode_chunked — decode attention for a batch whose sequences
+ * may carry ANY number of query tokens: prefill chunks beside decode and verify
+ * tokens, packed without padding (the mixed batch of the Continuous Batching
+ * section of the Colossal-Inference release page), with the per-sequence counts
+ * and lengths given in HOST memory, as a scheduler holds them.
+ *
+ *   host_q_lens       [num_seqs] int32, host: n_s >= 1 query tokens of sequence s.
+ *                     Its rows of q / out are cu_s .. cu_s + n_s - 1 with
+ *                     cu_s = n_0 + ... + n_{s-1}.
+ *   host_context_lens [num_seqs] int32, host: ctx_s >= n_s cached tokens including
+ *                     the query tokens; query token j sees positions
+ *                     p <= ctx_s - n_s + j (causal over the whole chunk).
+ *   out, q            [n_0 + ... + n_{S-1}][num_q_heads][head_size], device.
+ *   scales            an INT8 cache's row scales (as for
+ *                     pkv_paged_attention_decode_int8), else NULL.
+ *   workspace         device, 256-byte aligned, at least
+ *                     pkv_decode_chunked_workspace_bytes(host_q_lens, num_seqs,
+ *                     num_q_heads, max_blocks_per_seq, cache) bytes; owned by the
+ *                     caller, reusable by the next call on the same stream.
+ *   Everything else is as for pkv_paged_attention_decode_varlen.
+ * A sequence's tokens run as row tiles of 64 / (num_q_heads / num_kv_heads) tokens
+ * (the decode kernels' unit); each tile re-reads the blocks its tokens see, so a
+ * long chunk costs about (tiles) reads of its context: correct, not tuned for
+ * prefill. The call stages the tiles' lengths from host memory into the workspace
+ * and copies each tile's block-table row there (a small kernel on `stream`), so it
+ * cannot be captured in a CUDA graph. Returns PKV_ERR_INVALID_ARGUMENT for n_s < 1,
+ * ctx_s < n_s or a missing array; other device-side problems are flagged in
+ * device_status as for the _varlen call.
+ */
+size_t pkv_decode_chunked_workspace_bytes(const int32_t* host_q_lens, int32_t num_seqs, int32_t num_q_heads,
+                                          int32_t max_blocks_per_seq, const pkv_cache_desc* cache);
+int pkv_paged_attention_decode_chunked(void* out, const void* q, const int32_t* host_q_lens,
+                                       const int32_t* host_context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                       const void* k_cache, const void* v_cache, const float* scales,
+                                       pkv_dtype kv_dtype, const pkv_cache_desc* cache,
+                                       const int32_t* block_tables, int32_t max_blocks_per_seq, float scale,
+                                       void* workspace, size_t workspace_bytes, int32_t* device_status,
+                                       void* stream);
 
 /* ==== Block pool (host side) =================================================
  *

@@ -12,6 +12,7 @@ import ctypes
 import os
 import threading
 
+import numpy as np
 import torch
 
 KV_FP16, KV_BF16, KV_E5M2, KV_INT8 = 0, 1, 2, 3
@@ -117,6 +118,12 @@ def load_library(path: str | None = None):
             vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, P(_CacheDesc), vp, i32, vp, ctypes.c_float, vp,
             ctypes.c_size_t, vp, vp]
         lib.pkv_paged_attention_decode_int8_tree.restype = ctypes.c_int
+        lib.pkv_decode_chunked_workspace_bytes.argtypes = [vp, i32, i32, i32, P(_CacheDesc)]
+        lib.pkv_decode_chunked_workspace_bytes.restype = ctypes.c_size_t
+        lib.pkv_paged_attention_decode_chunked.argtypes = [
+            vp, vp, vp, vp, i32, i32, vp, vp, vp, ctypes.c_int, P(_CacheDesc), vp, i32, ctypes.c_float, vp,
+            ctypes.c_size_t, vp, vp]
+        lib.pkv_paged_attention_decode_chunked.restype = ctypes.c_int
         lib.pkv_error_string.argtypes = [ctypes.c_int]
         lib.pkv_error_string.restype = ctypes.c_char_p
         lib.pkv_version.restype = ctypes.c_int
@@ -335,7 +342,9 @@ def _workspace(nbytes: int, device) -> torch.Tensor:
     key = (str(device), torch.cuda.current_stream(device).cuda_stream)
     ws = _workspaces.get(key)
     if ws is None or ws.numel() < nbytes:
-        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        # Zeroed once: the piece counters then start clear whatever the allocator
+        # held there before (later calls leave them clear).
+        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
         _workspaces[key] = ws
     return ws
 
@@ -447,6 +456,65 @@ def paged_attention_decode_varlen(out, q, cu_q_lens, k_cache, v_cache, block_tab
                 int(block_tables.shape[1]), _ptr(context_lens), float(scale), *ws, _ptr(device_status),
                 _stream_handle(stream, q.device))
     _check(rc, "paged_attention_decode_varlen")
+    return out
+
+
+def _host_i32(name, x, n=None) -> np.ndarray:
+    """A host int32 array (list, numpy array or CPU tensor) the library reads directly."""
+    if isinstance(x, torch.Tensor):
+        if x.is_cuda:
+            raise PagedKVError(f"{name} must be in host memory")
+        x = x.numpy()
+    a = np.ascontiguousarray(np.asarray(x), dtype=np.int32)
+    if a.ndim != 1 or (n is not None and a.shape[0] != n):
+        raise PagedKVError(f"{name} must be 1-D" + (f" with {n} entries" if n is not None else ""))
+    return a
+
+
+def paged_attention_decode_chunked(out, q, q_lens, context_lens, k_cache, v_cache, block_tables, scale: float,
+                                   kv_dtype=None, *, scales=None, workspace=None, device_status=None,
+                                   stream=None):
+    """Decode attention for a batch whose sequences carry any number of query tokens
+    (prefill chunks beside decode / verify tokens), packed without padding: sequence s
+    owns the next q_lens[s] rows of q/out and its token j sees positions
+    <= context_lens[s] - q_lens[s] + j. q_lens and context_lens are host arrays
+    (lists, numpy arrays or CPU tensors). Not capturable in a CUDA graph."""
+    for nm, t in (("out", out), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
+                  ("block_tables", block_tables)):
+        _need_cuda_contig(nm, t)
+    if block_tables.dtype != torch.int32:
+        raise PagedKVError("block_tables must be int32")
+    if out.dtype != q.dtype:
+        raise PagedKVError("out and q must share a dtype")
+    ql = _host_i32("q_lens", q_lens)
+    S = int(ql.shape[0])
+    cl = _host_i32("context_lens", context_lens, S)
+    if S and (ql.min() < 1 or np.any(cl < ql)):
+        raise PagedKVError("every sequence needs 1 <= q_lens[s] <= context_lens[s]")
+    d = _pair(k_cache, v_cache)
+    if q.dim() != 3 or tuple(out.shape) != tuple(q.shape) or int(q.shape[0]) != int(ql.sum()):
+        raise PagedKVError(f"q and out must both be [sum(q_lens) = {int(ql.sum())}, num_q_heads, head_size]")
+    if int(q.shape[2]) != int(k_cache.shape[3]):
+        raise PagedKVError(f"query head size {int(q.shape[2])} != cache head size {int(k_cache.shape[3])}")
+    if block_tables.dim() != 2 or int(block_tables.shape[0]) < S:
+        raise PagedKVError(f"block_tables must be [num_seqs, max_blocks_per_seq], got {tuple(block_tables.shape)}")
+    code = _kv_code(kv_dtype, k_cache)
+    _int8_scales(code, k_cache, scales)
+    Hq, mbs = int(q.shape[1]), int(block_tables.shape[1])
+    lib = load_library()
+    qp, cp = ql.ctypes.data_as(ctypes.c_void_p), cl.ctypes.data_as(ctypes.c_void_p)
+    with _on_device(q.device):
+        need = int(lib.pkv_decode_chunked_workspace_bytes(qp, S, Hq, mbs, ctypes.byref(d)))
+        if S and need == 0:
+            raise PagedKVError("paged_attention_decode_chunked: unsupported shape")
+        if workspace is None:
+            workspace = _workspace(need, q.device)
+        rc = lib.pkv_paged_attention_decode_chunked(
+            _ptr(out), _ptr(q), qp, cp, S, Hq, _ptr(k_cache), _ptr(v_cache), _ptr(scales), code,
+            ctypes.byref(d), _ptr(block_tables), mbs, float(scale), _ptr(workspace),
+            int(workspace.numel() * workspace.element_size()), _ptr(device_status),
+            _stream_handle(stream, q.device))
+    _check(rc, "paged_attention_decode_chunked")
     return out
 
 

@@ -237,8 +237,20 @@ bool valid_cache(const pkv_cache_desc* c) {
   return rows < (1ll << 31) - kBlockSize;
 }
 
-// Workspace layout: [per-unit piece counters, 8 bytes each, 256-aligned][partial slots].
-size_t desc_bytes(long long units) { return static_cast<size_t>((units * 8 + 255) / 256 * 256); }
+// A bijective mix of the 32-bit call number (odd multiplies and xor-shifts are
+// each invertible modulo 2^32).
+uint32_t call_epoch(uint32_t n) {
+  n ^= n >> 16;
+  n *= 0x7feb352du;
+  n ^= n >> 15;
+  n *= 0x846ca68bu;
+  n ^= n >> 16;
+  return n;
+}
+
+// Workspace layout: [per-unit piece counters, 8 bytes each, 256-aligned][partial
+// slots] (decode_counter_bytes in pkv_internal.h sizes the first part).
+size_t desc_bytes(long long units) { return decode_counter_bytes(units); }
 
 // The decode grid has at most sm_count * ctas_per_sm CTAs, and a split unit's
 // pieces use slots unit + cta, so units + grid slots suffice.
@@ -470,9 +482,14 @@ int decode_impl(void* out, const void* q, const int32_t* cu_q_lens, int32_t num_
   a.slot_floats = partial_slot_floats(rows, d);
   a.scale_log2 = scale * 1.4426950408889634f;
   // Counters from an earlier call carry an older epoch and count as zero, so the
-  // workspace never needs clearing. (0 is skipped so a zeroed buffer is stale too.)
-  uint32_t ep = ++g_call_epoch;
-  if (ep == 0) ep = ++g_call_epoch;
+  // workspace never needs clearing. The epoch is the call number through a
+  // bijective 32-bit mix, so calls never share one (within 2^32 calls) and its
+  // values do not look like the small integers (lengths, block ids) a reused
+  // buffer may hold; 0 and 0xFFFFFFFF are skipped (zeroed and -1-filled memory).
+  uint32_t ep = 0;
+  do {
+    ep = call_epoch(++g_call_epoch);
+  } while (ep == 0u || ep == 0xFFFFFFFFu);
   a.epoch = ep;
   a.piece_cost = piece_cost(g.tc != 0, kv_dtype);
 #ifdef PKV_TIMELINE

@@ -72,6 +72,11 @@ __host__ __device__ constexpr int tile_row_bytes(int kv, int d) { return d * kv_
 __host__ __device__ constexpr int tile_bytes(int kv, int d) { return kBlockSize * tile_row_bytes(kv, d); }
 
 // Floats in one split-KV partial slot: m[rows], l[rows] (padded to 4), o[rows][D].
+// Bytes of a decode workspace's per-unit piece counters (8 each, rounded to 256):
+// the workspace starts with them, then holds the partial slots.
+__host__ __device__ constexpr size_t decode_counter_bytes(long long units) {
+  return static_cast<size_t>((units * 8 + 255) / 256 * 256);
+}
 __host__ __device__ constexpr int partial_o_offset(int rows) { return ((2 * rows + 3) / 4) * 4; }
 __host__ __device__ constexpr int partial_slot_floats(int rows, int d) {
   return partial_o_offset(rows) + rows * d;

@@ -127,3 +127,31 @@ def test_int8_cache_bytes_are_offset_binary_codes():
         api.int8_codes(torch.zeros(4, dtype=torch.uint8))
     e, _ = api.alloc_kv_cache(2, 1, 64, "e5m2", "cpu")
     assert e.dtype == torch.uint8 and int(e.max()) == 0
+
+
+def _chunked_case(q_lens=(1, 40, 3), ctx=(5, 60, 3), Hq=8, Hkv=2, D=64, nb=10, mbs=4):
+    rows = sum(q_lens)
+    q = torch.zeros(rows, Hq, D, dtype=torch.float16)
+    kc = torch.zeros(nb, Hkv, 16, D, dtype=torch.float16)
+    return dict(out=q.clone(), q=q, q_lens=list(q_lens), context_lens=torch.tensor(ctx, dtype=torch.int32),
+                k_cache=kc, v_cache=kc.clone(), block_tables=torch.zeros(len(q_lens), mbs, dtype=torch.int32),
+                scale=0.125)
+
+
+def test_chunked_call_reaches_the_library_and_checks_its_host_arrays(stub):
+    with pytest.raises(_Reached):
+        api.paged_attention_decode_chunked(**_chunked_case())
+    for bad in ("rows", "ctx_short", "zero_tokens", "ctx_len", "bt_rows"):
+        c = _chunked_case()
+        if bad == "rows":
+            c["q"], c["out"] = c["q"][:40].contiguous(), c["out"][:40].contiguous()
+        elif bad == "ctx_short":
+            c["context_lens"] = torch.tensor([5, 39, 3], dtype=torch.int32)
+        elif bad == "zero_tokens":
+            c["q_lens"] = [1, 0, 3]
+        elif bad == "ctx_len":
+            c["context_lens"] = torch.tensor([5, 60], dtype=torch.int32)
+        elif bad == "bt_rows":
+            c["block_tables"] = torch.zeros(2, 4, dtype=torch.int32)
+        with pytest.raises(api.PagedKVError):
+            api.paged_attention_decode_chunked(**c)

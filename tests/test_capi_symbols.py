@@ -83,3 +83,34 @@ def test_host_validation_rejects_bad_arguments_without_a_device(lib):
     assert d(*a) == -1
     a = list(args); a[2] = 0                       # empty batch: no-op
     assert d(*a) == 0
+
+
+def test_chunked_call_checks_its_host_arrays_without_a_device(lib):
+    """The chunked entry point reads the query counts and lengths from host memory and
+    rejects an empty sequence or a context shorter than its query tokens before any
+    device work."""
+    from paged_kv_cache_252_gb300.api import _CacheDesc
+    vp, i32 = ctypes.c_void_p, ctypes.c_int32
+    good = _CacheDesc(32, 16, 2, 64)
+    fake = vp(0x1000)
+    c = lib.pkv_paged_attention_decode_chunked
+    c.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp, vp, ctypes.c_int, ctypes.POINTER(_CacheDesc), vp, i32,
+                  ctypes.c_float, vp, ctypes.c_size_t, vp, vp]
+
+    def call(q_lens, ctx, heads=4, mbs=8):
+        ql = (i32 * len(q_lens))(*q_lens)
+        cl = (i32 * len(ctx))(*ctx)
+        return c(fake, fake, ctypes.cast(ql, vp), ctypes.cast(cl, vp), len(q_lens), heads, fake, fake, None, 0,
+                 ctypes.byref(good), fake, mbs, 0.125, vp(0x10000), 1 << 20, None, None)
+
+    assert call([1, 0, 3], [4, 4, 4]) == -1            # a sequence without query tokens
+    assert call([1, 5, 3], [4, 4, 4]) == -1            # context shorter than its tokens
+    assert call([1, 2], [4, 4], heads=3) == -1         # 3 query heads over 2 KV heads
+    assert call([1, 2], [4, 4], mbs=0) == -1
+    assert c(fake, fake, None, None, 0, 4, fake, fake, None, 0, ctypes.byref(good), fake, 8, 0.125, None, 0,
+             None, None) == 0                           # empty batch: no-op
+    ws = lib.pkv_decode_chunked_workspace_bytes
+    ws.argtypes = [vp, i32, i32, i32, ctypes.POINTER(_CacheDesc)]
+    ws.restype = ctypes.c_size_t
+    bad = (i32 * 2)(1, 0)
+    assert ws(ctypes.cast(bad, vp), 2, 4, 8, ctypes.byref(good)) == 0

@@ -371,3 +371,24 @@ def test_tree_verify_parity(orc, dev, gpu, case):
     ref, _, rc = gpu.oracle_attention(orc, w, vals, okc, ovc, **kw)
     assert rc == 0
     gpu.compare(out, ref, label=f"tree {kv} D{D} G{Hq // Hkv} q_lens {q_lens}")
+
+
+def test_workspace_left_holding_small_integers_gives_the_same_output(dev, gpu):
+    """A workspace reused after holding other data (here every int32 value 0..4095,
+    as block ids or lengths would leave it) decodes exactly as a zeroed one: the
+    piece counters' per-call tags do not look like small integers."""
+    import paged_kv_cache_252_gb300 as pkv
+    w = wl.custom(num_seqs=8, num_q_heads=32, num_kv_heads=8, head_size=128, q_per_seq=1, kv_dtype="fp16",
+                  context_lens=[3000, 17, 2500, 900, 1, 4000, 64, 1200], seed=31)
+    vals = wl.token_values(w)
+    kc, vc, ref = gpu.cuda_path(w, vals, dev)
+    q = vals["q"].to(dev)
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    cl = torch.from_numpy(w.context_lens).to(dev)
+    need = pkv.decode_workspace_bytes(w.num_seqs, w.num_q_heads, 1, kc)
+    for _ in range(3):
+        ws = (torch.arange(need // 4 + 1, dtype=torch.int32, device=dev) % 4096).view(torch.uint8)
+        out = torch.full_like(q, float("nan"))
+        pkv.paged_attention_decode(out, q, kc, vc, bt, cl, 1, w.scale, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
