@@ -330,11 +330,16 @@ int pkv_paged_attention_decode_int8_tree(void* out, const void* q, const int32_t
  *                     caller, reusable by the next call on the same stream.
  *   Everything else is as for pkv_paged_attention_decode_varlen.
  * A sequence's tokens run as row tiles of 64 / (num_q_heads / num_kv_heads) tokens
- * (the decode kernels' unit); each tile re-reads the blocks its tokens see, so a
+ * (the decode kernels' unit; fewer when no sequence has that many, so a batch of
+ * plain decodes runs as it would through the _varlen call); each tile re-reads
+ * the blocks its tokens see, so a
  * long chunk costs about (tiles) reads of its context: correct, not tuned for
- * prefill. The call stages the tiles' lengths from host memory into the workspace
- * and copies each tile's block-table row there (a small kernel on `stream`), so it
- * cannot be captured in a CUDA graph. Returns PKV_ERR_INVALID_ARGUMENT for n_s < 1,
+ * prefill. The call reads the host arrays when it is made and passes the tiles'
+ * lengths to a small setup kernel on `stream` as launch parameters (no host
+ * synchronisation); the setup kernel writes them into the workspace and copies
+ * each tile's block-table row there. The call may be captured in a CUDA graph,
+ * which then replays the captured counts and lengths. Returns
+ * PKV_ERR_INVALID_ARGUMENT for n_s < 1,
  * ctx_s < n_s or a missing array; other device-side problems are flagged in
  * device_status as for the _varlen call.
  */

@@ -478,7 +478,8 @@ def paged_attention_decode_chunked(out, q, q_lens, context_lens, k_cache, v_cach
     (prefill chunks beside decode / verify tokens), packed without padding: sequence s
     owns the next q_lens[s] rows of q/out and its token j sees positions
     <= context_lens[s] - q_lens[s] + j. q_lens and context_lens are host arrays
-    (lists, numpy arrays or CPU tensors). Not capturable in a CUDA graph."""
+    (lists, numpy arrays or CPU tensors), read when the call is made (a captured CUDA
+    graph replays them)."""
     for nm, t in (("out", out), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
                   ("block_tables", block_tables)):
         _need_cuda_contig(nm, t)

@@ -134,3 +134,35 @@ def test_chunked_rows_of_one_chunk_equal_the_single_token_decodes(dev, gpu):
     pkv.paged_attention_decode(one, q, kc, vc, bt.expand(n, -1).contiguous(), lens, 1, w.scale)
     torch.cuda.synchronize()
     gpu.compare(out, one.float().cpu().numpy().astype(np.float64), label="chunk rows vs single-token decodes")
+
+
+def test_chunked_call_replays_from_a_cuda_graph(dev, gpu):
+    """The tiles' metadata travels as launch parameters: a captured call replays to
+    the same output bits."""
+    import paged_kv_cache_252_gb300 as pkv
+    q_lens, ctx = [1, 70, 3], [100, 300, 20]
+    w = wl.custom(num_seqs=3, num_q_heads=16, num_kv_heads=4, head_size=128, q_per_seq=70, kv_dtype="fp16",
+                  context_lens=ctx, seed=19, q_lens=q_lens)
+    vals = wl.token_values(w)
+    kc, vc, _ = _caches(w, vals, dev)
+    q = vals["q"].to(dev)
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    ref = torch.full_like(q, float("nan"))
+    pkv.paged_attention_decode_chunked(ref, q, q_lens, ctx, kc, vc, bt, w.scale)
+    torch.cuda.synchronize()
+    out = torch.full_like(q, float("nan"))
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):   # the binding's workspace for this stream, outside the capture
+        pkv.paged_attention_decode_chunked(out, q, q_lens, ctx, kc, vc, bt, w.scale)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    out.fill_(float("nan"))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        pkv.paged_attention_decode_chunked(out, q, q_lens, ctx, kc, vc, bt, w.scale)
+    for _ in range(3):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
