@@ -353,6 +353,20 @@ int pkv_paged_attention_decode_chunked(void* out, const void* q, const int32_t* 
                                        void* workspace, size_t workspace_bytes, int32_t* device_status,
                                        void* stream);
 
+/*
+ * pkv_selftest_bounded_wait — exercises, on the device, the bounded wait every
+ * decode kernel puts on its pipeline barriers: one thread waits on an mbarrier
+ * phase that nothing completes with a limit of limit_ns (1 .. 2e9 ns), gives up,
+ * raises its CTA's abort flag and ORs PKV_DEV_TIMEOUT into *device_status; a
+ * second thread, waiting with the decode kernels' own 2 s limit, leaves as soon
+ * as it sees the flag. device_elapsed_ns[0..1] (device, 8-byte aligned) receive
+ * the two waits' durations. Nothing faults or hangs; the context stays usable.
+ * Returns PKV_ERR_INVALID_ARGUMENT for a missing or misaligned pointer or a limit
+ * outside the range.
+ */
+int pkv_selftest_bounded_wait(int32_t* device_status, uint64_t limit_ns, unsigned long long* device_elapsed_ns,
+                              void* stream);
+
 /* ==== Block pool (host side) =================================================
  *
  * "AI 大模型推理优化技术详解", 2.1.2 Paged Attention: each sequence's KV cache is

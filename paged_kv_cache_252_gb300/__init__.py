@@ -19,7 +19,7 @@ from . import workloads  # noqa: F401
 from .api import (  # noqa: F401
     KV_FP16, KV_BF16, KV_E5M2, KV_INT8,
     kv_cache_write, paged_attention_decode, paged_attention_decode_varlen,
-    paged_attention_decode_tree, paged_attention_decode_chunked,
+    paged_attention_decode_tree, paged_attention_decode_chunked, selftest_bounded_wait,
     paged_attention_decode_noalloc, decode_workspace_bytes,
     library_path, load_library, alloc_kv_cache, PagedKVError,
     BlockAllocator, copy_blocks,

@@ -124,6 +124,8 @@ def load_library(path: str | None = None):
             vp, vp, vp, vp, i32, i32, vp, vp, vp, ctypes.c_int, P(_CacheDesc), vp, i32, ctypes.c_float, vp,
             ctypes.c_size_t, vp, vp]
         lib.pkv_paged_attention_decode_chunked.restype = ctypes.c_int
+        lib.pkv_selftest_bounded_wait.argtypes = [vp, ctypes.c_uint64, vp, vp]
+        lib.pkv_selftest_bounded_wait.restype = ctypes.c_int
         lib.pkv_error_string.argtypes = [ctypes.c_int]
         lib.pkv_error_string.restype = ctypes.c_char_p
         lib.pkv_version.restype = ctypes.c_int
@@ -517,6 +519,23 @@ def paged_attention_decode_chunked(out, q, q_lens, context_lens, k_cache, v_cach
             _stream_handle(stream, q.device))
     _check(rc, "paged_attention_decode_chunked")
     return out
+
+
+def selftest_bounded_wait(limit_ns: int, device=None, stream=None):
+    """Run the device self-test of the decode kernels' bounded waits (a wait on a
+    barrier phase nothing completes gives up after limit_ns and flags
+    PKV_DEV_TIMEOUT; a second wait leaves on the CTA's abort flag). Returns
+    (status word, [duration of wait 0, duration of wait 1] in ns)."""
+    device = torch.device(device or "cuda")
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    elapsed = torch.zeros(2, dtype=torch.int64, device=device)
+    lib = load_library()
+    with _on_device(status.device):
+        rc = lib.pkv_selftest_bounded_wait(_ptr(status), int(limit_ns), _ptr(elapsed),
+                                           _stream_handle(stream, status.device))
+    _check(rc, "selftest_bounded_wait")
+    torch.cuda.synchronize(status.device)
+    return int(status.item()), [int(x) for x in elapsed.cpu().tolist()]
 
 
 def paged_attention_decode_tree(out, q, tree_masks, k_cache, v_cache, block_tables, context_lens,

@@ -34,7 +34,7 @@ VARIANTS = {  # name -> (object dir, library, extra nvcc flags)
 }
 
 SOURCES = ["capi.cu", "kv_cache_write.cu", "decode_f16.cu", "decode_bf16.cu", "decode_e5m2.cu",
-           "decode_tc.cu", "decode_int8.cu", "noalloc.cu", "copy_blocks.cu", "chunked.cu",
+           "decode_tc.cu", "decode_int8.cu", "noalloc.cu", "copy_blocks.cu", "chunked.cu", "selftest.cu",
            "block_allocator.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

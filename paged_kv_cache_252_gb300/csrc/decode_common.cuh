@@ -33,19 +33,25 @@ __device__ __forceinline__ int unit_blocks(int ctx, int mbs) {
   return (c + kBlockSize - 1) / kBlockSize;
 }
 
-// Wait for an mbarrier phase; gives up after kWaitLimitNs or when another warp
-// of the CTA has already given up (abort flag in shared memory).
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
-                                              volatile int* abort_flag) {
+// Wait for an mbarrier phase; gives up after limit_ns or when another warp of the
+// CTA has already given up (abort flag in shared memory).
+__device__ __forceinline__ bool wait_or_abort_for(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                  uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0u) {
       if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+      if (global_timer_ns() - t0 > limit_ns) return false;
     }
   }
+}
+
+// The decode kernels' waits: limit kWaitLimitNs.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
+                                              volatile int* abort_flag) {
+  return wait_or_abort_for(bar, parity, abort_flag, kWaitLimitNs);
 }
 
 template <int KV>

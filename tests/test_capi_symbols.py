@@ -114,3 +114,14 @@ def test_chunked_call_checks_its_host_arrays_without_a_device(lib):
     ws.restype = ctypes.c_size_t
     bad = (i32 * 2)(1, 0)
     assert ws(ctypes.cast(bad, vp), 2, 4, 8, ctypes.byref(good)) == 0
+
+
+def test_bounded_wait_selftest_checks_its_arguments_without_a_device(lib):
+    vp = ctypes.c_void_p
+    f = lib.pkv_selftest_bounded_wait
+    f.argtypes = [vp, ctypes.c_uint64, vp, vp]
+    assert f(None, 1000, vp(0x1000), None) == -1
+    assert f(vp(0x1000), 1000, None, None) == -1
+    assert f(vp(0x1002), 1000, vp(0x1000), None) == -1     # misaligned status word
+    assert f(vp(0x1000), 0, vp(0x1000), None) == -1        # no limit
+    assert f(vp(0x1000), 3_000_000_000, vp(0x1000), None) == -1

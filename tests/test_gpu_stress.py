@@ -41,3 +41,21 @@ def test_repeated_launches_are_clean_and_deterministic(dev, kv, D, Hq, n):
             assert int(status.item()) == 0, f"device status {int(status.item()):#x} after {it + 1} launches"
             assert torch.equal(out, ref)
     assert torch.isfinite(ref).all()
+
+
+def test_bounded_wait_gives_up_flags_and_leaves_the_context_usable(dev):
+    """A wait on a barrier phase that nothing completes gives up after its limit and
+    flags PKV_DEV_TIMEOUT; a second wait with the decode kernels' 2 s limit leaves on
+    the CTA's abort flag; the next decode runs clean."""
+    import paged_kv_cache_252_gb300 as pkv
+    status, (t0, t1) = pkv.selftest_bounded_wait(2_000_000, dev)   # 2 ms
+    assert status & 0x8
+    assert 2_000_000 <= t0 < 200_000_000
+    assert t1 < 200_000_000                                         # far below its own 2 s
+    w = wl.custom(num_seqs=3, num_q_heads=8, num_kv_heads=2, head_size=128, q_per_seq=1, kv_dtype="fp16",
+                  context_lens=[40, 300, 7], seed=3)
+    import _gpu
+    vals = wl.token_values(w)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    _gpu.cuda_path(w, vals, dev, status=st)
+    assert int(st.item()) == 0
