@@ -259,9 +259,11 @@ int pkv_paged_attention_decode_noalloc(void* out, const void* q, int32_t num_seq
  *
  * The inference-framework survey lists "KV Cache INT8 量化" for LMDeploy
  * without a codec; this one is symmetric per (token, KV head) row:
- *   scale = max|x| / 127,  code = round-half-even(x / scale) clamped to [-127, 127],
+ *   scale = max|x| / 127 rounded up to the nearest fp16 value,
+ *   code = round-half-even(x / scale) clamped to [-127, 127],
  * both divisions in IEEE fp32; an all-zero row has scale 0 and codes 0; an
- * element's value is code * scale.
+ * element's value is code * scale. (An fp16-valued scale folds exactly into the
+ * fp16 weights of the attention's P V product.)
  *
  * Caches: one byte per element, [num_blocks][num_kv_heads][16][head_size],
  * each code stored in offset binary: byte = code + 128 (1..255; the decode

@@ -182,6 +182,15 @@ uint8_t e5m2_from_fp16_bits(uint16_t h) {
   return encode_e5m2(r);
 }
 
+// The smallest fp16 value >= v (v >= 0, below the fp16 maximum): the row scale
+// of an INT8 row is max|x| / 127 rounded up this way.
+float round_up_to_fp16(float v) {
+  if (v == 0.0f) return 0.0f;
+  const uint16_t h = encode_fp16(round_to_format((double)v, 11, -14, 65504.0, false));   // nearest
+  const double r = fp16_value(h);
+  return (float)(r < (double)v ? fp16_value((uint16_t)(h + 1)) : r);
+}
+
 // One INT8 code: fp32 division by the row's scale, round half to even, clamp.
 int8_t int8_code(float x, float scale) {
   if (scale == 0.0f) return 0;
@@ -302,7 +311,7 @@ int orc_kv_cache_write_int8(const uint16_t* key, const uint16_t* value, int num_
         const uint16_t* src = (which ? value : key) + ((int64_t)t * num_kv_heads + h) * head_size;
         float amax = 0.0f;
         for (int d = 0; d < head_size; ++d) amax = std::fmax(amax, std::fabs((float)fp16_value(src[d])));
-        const float scale = amax / 127.0f;
+        const float scale = round_up_to_fp16(amax / 127.0f);
         int8_t* dst = (which ? v_cache : k_cache) + row * head_size;
         for (int d = 0; d < head_size; ++d) dst[d] = int8_code((float)fp16_value(src[d]), scale);
         (which ? v_scale : k_scale)[row] = scale;

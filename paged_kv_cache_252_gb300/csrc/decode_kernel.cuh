@@ -530,19 +530,16 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
         const int p_lo = tok0 + g8, p_hi = p_lo + 8;
         // INT8: this lane's tokens g8 and g8+8 of the block. Their K scales
         // scale the scores; their V scales are folded into P (0 past the context,
-        // where the stage may hold stale scales). The row sums add each token's
-        // weight as the P V product sees it, the fp16 value of P * sv times 1 / sv
-        // (P itself where the scale is 0), so rounding P * sv to fp16 perturbs the
-        // softmax weights (as rounding P does) instead of scaling the output.
+        // where the stage may hold stale scales). The scales are fp16 values, so a
+        // token whose P is 1 (the row's maximum) enters the P V product with exactly
+        // its scale; the rounding of P * sv to fp16 otherwise perturbs a weight by
+        // at most 2^-11, as the rounding of P does in the other paths.
         float sk_lo = a.scale_log2, sk_hi = a.scale_log2, sv_lo = 1.f, sv_hi = 1.f;
-        float isv_lo = 0.f, isv_hi = 0.f;
         if constexpr (kInt8) {
           sk_lo *= sc_k_lo;
           sk_hi *= sc_k_hi;
           sv_lo = p_lo < ctx_eff ? sc_v_lo : 0.f;
           sv_hi = p_hi < ctx_eff ? sc_v_hi : 0.f;
-          isv_lo = sv_lo > 0.f ? __fdividef(1.f, sv_lo) : 0.f;
-          isv_hi = sv_hi > 0.f ? __fdividef(1.f, sv_hi) : 0.f;
         }
         uint32_t pb[NTW][2];
         uint32_t pb_lo[NTW][2];   // bf16 only: P - bf16(P), a second bf16 term
@@ -571,7 +568,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
             alpha[nt][e] = fast_exp2(m_run[nt][e] - m_use);
             pv[e] = fast_exp2(x_lo - m_use);
             pv[2 + e] = fast_exp2(x_hi - m_use);
-            if constexpr (!kInt8) l_run[nt][e] = l_run[nt][e] * alpha[nt][e] + pv[e] + pv[2 + e];
+            l_run[nt][e] = l_run[nt][e] * alpha[nt][e] + pv[e] + pv[2 + e];
             m_run[nt][e] = m_new;
           }
           // P^T fragments: the S^T accumulator layout (token g, rows 2c..2c+1) is an
@@ -581,16 +578,6 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
           const uint32_t h23 = pack_p<KV>(pv[2] * sv_hi, pv[3] * sv_hi);
           pb[nt][0] = movmatrix_t(h01);
           pb[nt][1] = movmatrix_t(h23);
-          if constexpr (kInt8) {
-            const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
-            const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
-            const float w0 = sv_lo > 0.f ? f01.x * isv_lo : pv[0];
-            const float w1 = sv_lo > 0.f ? f01.y * isv_lo : pv[1];
-            const float w2 = sv_hi > 0.f ? f23.x * isv_hi : pv[2];
-            const float w3 = sv_hi > 0.f ? f23.y * isv_hi : pv[3];
-            l_run[nt][0] = l_run[nt][0] * alpha[nt][0] + w0 + w2;
-            l_run[nt][1] = l_run[nt][1] * alpha[nt][1] + w1 + w3;
-          }
           if constexpr (KV == kKvBf16) {
             // bf16 keeps 8 significant bits; P = hi + lo with both in bf16 keeps
             // about 16, so the P V product is as accurate as with an fp16 P.

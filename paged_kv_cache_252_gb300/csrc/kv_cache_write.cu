@@ -70,9 +70,10 @@ const void* kv_cache_write_kernel_ptr() { return reinterpret_cast<const void*>(&
 
 // INT8 cache write (the "KV Cache INT8 量化" the inference-framework survey lists
 // for LMDeploy; the codec is ours): one warp quantises one (token, head) row of
-// K or V. scale = max|x| / 127 and code = round-half-even(x / scale) clamped to
-// [-127, 127]; both divisions are IEEE fp32 (__fdiv_rn), so the codes do not
-// depend on compiler flags. An all-zero row gets scale 0 and codes 0. Codes are
+// K or V. scale = max|x| / 127 rounded up to the nearest fp16 value (so that the
+// decode can fold it into an fp16 weight exactly) and code = round-half-even(x /
+// scale) clamped to [-127, 127]; both divisions are IEEE fp32 (__fdiv_rn), so the
+// codes do not depend on compiler flags. An all-zero row gets scale 0 and codes 0. Codes are
 // stored in offset binary (byte = code + 128), which the decode kernel widens
 // to fp16 with a single byte permute.
 __global__ void __launch_bounds__(256) kv_cache_write_int8_kernel(const CacheWriteArgs a) {
@@ -104,7 +105,7 @@ __global__ void __launch_bounds__(256) kv_cache_write_int8_kernel(const CacheWri
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float scale = __fdiv_rn(amax, 127.0f);
+    const float scale = __half2float(__float2half_ru(__fdiv_rn(amax, 127.0f)));
     uint32_t packed = 0;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {

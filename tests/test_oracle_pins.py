@@ -507,8 +507,12 @@ def test_int8_codes_are_nearest_and_span_the_row(orc):
     codes, scales = _int8_rows(orc, x)
     xf = x.astype(np.float64)
     amax = np.abs(xf).max(axis=2)
-    # the scale is max|x| / 127 rounded to float32
-    np.testing.assert_array_equal(scales, (amax.astype(np.float32) / np.float32(127.0)).astype(np.float32))
+    # the scale is max|x| / 127 (a float32 division) rounded up to the nearest fp16 value
+    s32 = (amax.astype(np.float32) / np.float32(127.0)).astype(np.float32)
+    assert np.array_equal(scales.astype(np.float16).astype(np.float32), scales)   # fp16 values
+    assert np.all(scales >= s32)
+    below = np.nextafter(scales.astype(np.float16), np.float16(0)).astype(np.float32)
+    assert np.all((below < s32) | (scales == 0))                                   # the smallest such
     nz = scales > 0
     ratio = xf / np.where(nz, scales, 1.0)[..., None]
     # each code is the integer nearest x / scale (within the float32 rounding of the ratio)
