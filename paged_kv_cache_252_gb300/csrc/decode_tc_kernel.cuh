@@ -14,10 +14,12 @@
 //
 // Work is done in chunks of 8 KV blocks (128 tokens) of one unit.
 //   S^T (128 tokens x RP rows)  = K_chunk (128 x 128, fp16) . Q^T      [TMEM, fp32]
-//   O^T (128 dims   x RP rows) += V_chunk^T (128 x 128 tokens) . P^T   [TMEM, fp32]
-// with RP = 32 or 64 (rows padded; padding rows of Q are zero). K_chunk is
-// the A operand straight from tensor memory (token t in lane t); Q^T, V^T and
-// P^T come from shared memory.
+//   O^T (128 dims   x 64 rows) += V_chunk^T (128 x 128 tokens) . P^T   [TMEM, fp32]
+// with RP = 32 or 64 (rows padded; padding rows of Q are zero; with RP = 32 the
+// P^T rows 32..63, and O^T's columns 32..63, are never written or read). K_chunk
+// is the A operand straight from tensor memory (token t in lane t); Q^T, V^T and
+// P^T come from shared memory, P^T MN-major so that a thread's probabilities for
+// its rows are adjacent (16-byte stores).
 //
 // Warp roles (320 threads, one CTA per SM):
 //   warp 9      : TMA producer. Copies the chunk's K and V tiles (E5M2,
@@ -417,7 +419,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   constexpr int CHUNK_BYTES = 2 * kTcChunk * TILE;    // one ring buffer: 8 K tiles, then 8 V tiles
   constexpr uint32_t kHalf = 128 * 128;               // one 64-dim half of a widened chunk
   constexpr uint32_t kWide = 2 * kHalf;               // one widened chunk
-  constexpr uint32_t kRowsHalf = RP * 128;            // one 64-element half of Q or P^T
+  constexpr uint32_t kRowsHalf = RP * 128;            // one 64-element half of Q
   constexpr float kNegInf = -INFINITY;
 
   extern __shared__ uint8_t smem_raw[];
@@ -575,7 +577,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // ------------------------------ MMA issue -----------------------------------
       if (lane == 0) {
         const uint32_t id_s = idesc_kind_f16(128, RP, 0, 0, 0);   // K (TMEM, K-major) x Q^T (K-major)
-        const uint32_t id_o = idesc_kind_f16(128, RP, 0, 1, 0);   // V^T (MN-major) x P^T (K-major)
+        const uint32_t id_o = idesc_kind_f16(128, 64, 0, 1, 1);   // V^T (MN-major) x P^T (MN-major, 64 rows)
         const uint32_t t_o = tmem + kTcOCol;
         const uint32_t v16a = smem_addr(v16), pa = smem_addr(pst), qa = smem_addr(qst);
         // Descriptors of the buffers' first atoms, built once: a later atom is the same
@@ -583,7 +585,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // every shared-memory address here stays below 2^18 bytes, so the field never carries.
         const uint64_t dq0 = smem_desc_sw128(qa, 0, 1024), dq1 = smem_desc_sw128(qa + 2 * kRowsHalf, 0, 1024);
         const uint64_t dv0 = smem_desc_sw128(v16a, kHalf, 1024), dv1 = smem_desc_sw128(v16a + kWide, kHalf, 1024);
-        const uint64_t dp = smem_desc_sw128(pa, 0, 1024);
+        const uint64_t dp = smem_desc_sw128(pa, 128 * 128, 1024);
         TcWalk w = w0;
         int c = 0, piece = 0;
         bool prev = false, prev_first = false, ok = true;
@@ -634,8 +636,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint64_t dvs = ((c - 1) & 1) ? dv1 : dv0;
 #pragma unroll
             for (int kk = 0; kk < kTcChunk; ++kk) {
-              const uint64_t db = dp + (((kk >> 2) * kRowsHalf + (kk & 3) * 32) >> 4);
-              tc_mma_f16_ss(t_o, dvs + ((kk * 2048) >> 4), db, id_o, (kk > 0 || !prev_first) ? 1u : 0u);
+              tc_mma_f16_ss(t_o, dvs + ((kk * 2048) >> 4), dp + ((kk * 2048) >> 4), id_o,
+                            (kk > 0 || !prev_first) ? 1u : 0u);
             }
             tc_commit(bar_odone);
           }
@@ -691,10 +693,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       };
 
-      // Swizzled P^T store addresses: row r = r0 + k lives in 16-byte chunk
-      // (t % 64) / 8 ^ (k % 8) of its 128-byte line (r0 is a multiple of 8).
-      uint8_t* pbase = pst + (t >> 6) * kRowsHalf + r0 * 128 + (t & 7) * 2;
-      const int tch = (t & 63) >> 3;
+      // P^T is MN-major with 64 row slots per token: token t's line (128 bytes, 8-token
+      // groups 1024 bytes apart) holds rows 0..63, rows 8j..8j+7 in 16-byte chunk j ^ (t % 8).
+      // This thread's RH rows r0.. are chunks r0/8 .. r0/8 + RH/8 - 1 of its line.
+      uint8_t* pline = pst + (t >> 3) * 1024 + (t & 7) * 128;
 
       float l_run[RH];   // this thread's (token's) share of each row's sum of exponentials
 #pragma unroll
@@ -811,11 +813,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
 
         PKV_TL_STEP(5);
-        // (4) P^T of chunk c: K-major [token half][row][128 B]; the buffer was read by O(c-1).
+        // (4) P^T of chunk c (MN-major, see pline); the buffer was read by O(c-1).
         if (c > 0) wait_o(c - 1);
         PKV_TL_STEP(6);
         if (alive) {
           const float* mrow = row_m + mp * RP + r0;
+          uint32_t pw[4];
 #pragma unroll
           for (int k4 = 0; k4 < RH / 4; ++k4) {
             const float4 m4 = *reinterpret_cast<const float4*>(mrow + 4 * k4);
@@ -826,11 +829,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             l_run[4 * k4 + 1] += __high2float(p01);
             l_run[4 * k4 + 2] += __low2float(p23);
             l_run[4 * k4 + 3] += __high2float(p23);
-            const __half pk[4] = {__low2half(p01), __high2half(p01), __low2half(p23), __high2half(p23)};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int k = 4 * k4 + e;
-              *reinterpret_cast<__half*>(pbase + k * 128 + ((tch ^ (k & 7)) << 4)) = pk[e];
+            pw[2 * (k4 & 1)] = *reinterpret_cast<const uint32_t*>(&p01);
+            pw[2 * (k4 & 1) + 1] = *reinterpret_cast<const uint32_t*>(&p23);
+            if (k4 & 1) {
+              const int j = (r0 >> 3) + (k4 >> 1);
+              *reinterpret_cast<uint4*>(pline + ((j ^ (t & 7)) << 4)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
             }
           }
         }

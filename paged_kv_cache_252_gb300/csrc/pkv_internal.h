@@ -123,8 +123,8 @@ __host__ __device__ inline TcSmem tc_smem_layout(int rows_pad, int nbuf) {
   const size_t wide = 128 * 128 * 2;          // one chunk of V widened to fp16
   const size_t rows_bytes = (size_t)rows_pad * 256;
   s.v16 = 0;                                   // two buffers
-  s.p = s.v16 + 2 * wide;
-  s.q = s.p + rows_bytes;                      // two buffers
+  s.p = s.v16 + 2 * wide;                      // P^T: 128 tokens x 64 row slots (fp16)
+  s.q = s.p + 128 * 64 * 2;                    // two buffers
   s.ring = s.q + 2 * rows_bytes;
   s.bars = s.ring + (size_t)nbuf * 2 * kTcChunk * kBlockSize * 128;
   s.misc = s.bars + (size_t)(2 * nbuf + 5) * 8;
