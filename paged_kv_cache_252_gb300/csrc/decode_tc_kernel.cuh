@@ -420,6 +420,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   constexpr uint32_t kHalf = 128 * 128;               // one 64-dim half of a widened chunk
   constexpr uint32_t kWide = 2 * kHalf;               // one widened chunk
   constexpr uint32_t kRowsHalf = RP * 128;            // one 64-element half of Q
+  constexpr bool kFusedMax = RC == 1;                 // x = score less the running max (see (3))
   constexpr float kNegInf = -INFINITY;
 
   extern __shared__ uint8_t smem_raw[];
@@ -773,20 +774,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
         PKV_TL_STEP(3);
         // (3) scores in base 2, masked; does any exceed its row's running max by the slack?
+        //     With 32 rows per unit x holds the score less the running max (one FMA
+        //     each; the rare path below recomputes it from S when the max moves). With
+        //     64 rows that recompute's live scores spill registers (64-row units: 109 ->
+        //     119 us), so x holds the score and the max comes off at the exponential.
         const int p = cur.first_token() + t;
         const bool valid = (t >> 4) < cur.nblk() && p < pc.ctx_eff;
         const bool allvis = valid && p < pc.cb;
         const unsigned long long vis = allvis ? ~0ull : tc_row_visibility(a, pc, p, valid, r0);
         float x[RH];
-        if (allvis) {
-#pragma unroll
-          for (int k = 0; k < RH; ++k) x[k] = __uint_as_float(sv[k]) * scale_log2;
-        } else {
-#pragma unroll
-          for (int k = 0; k < RH; ++k) x[k] = ((vis >> k) & 1ull) ? __uint_as_float(sv[k]) * scale_log2 : kNegInf;
-        }
         float excess = kNegInf;
-        {
+        if constexpr (kFusedMax) {
+          const float* mrow = row_m + mp * RP + r0;
+#pragma unroll
+          for (int k4 = 0; k4 < RH / 4; ++k4) {
+            const float4 m4 = *reinterpret_cast<const float4*>(mrow + 4 * k4);
+            x[4 * k4] = fmaf(__uint_as_float(sv[4 * k4]), scale_log2, -m4.x);
+            x[4 * k4 + 1] = fmaf(__uint_as_float(sv[4 * k4 + 1]), scale_log2, -m4.y);
+            x[4 * k4 + 2] = fmaf(__uint_as_float(sv[4 * k4 + 2]), scale_log2, -m4.z);
+            x[4 * k4 + 3] = fmaf(__uint_as_float(sv[4 * k4 + 3]), scale_log2, -m4.w);
+          }
+          if (!allvis) {
+#pragma unroll
+            for (int k = 0; k < RH; ++k) x[k] = ((vis >> k) & 1ull) ? x[k] : kNegInf;
+          }
+#pragma unroll
+          for (int k = 0; k < RH; ++k) excess = fmaxf(excess, x[k]);
+        } else {
+          if (allvis) {
+#pragma unroll
+            for (int k = 0; k < RH; ++k) x[k] = __uint_as_float(sv[k]) * scale_log2;
+          } else {
+#pragma unroll
+            for (int k = 0; k < RH; ++k) x[k] = ((vis >> k) & 1ull) ? __uint_as_float(sv[k]) * scale_log2 : kNegInf;
+          }
           const float* mrow = row_m + mp * RP + r0;
 #pragma unroll
           for (int k4 = 0; k4 < RH / 4; ++k4) {
@@ -810,6 +831,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
 #pragma unroll
           for (int k = 0; k < RH; ++k) l_run[k] *= row_alpha[r0 + k];
+          if constexpr (kFusedMax) {
+            // The scores again (S(c) is intact) against the moved maxima.
+            if (alive) {
+              tc_fence_after_sync();
+              tmem_ld<RH>(t_cols + (c & 1) * kTcSCols, sv);
+            }
+            const float* mrow = row_m + mp * RP + r0;
+#pragma unroll
+            for (int k4 = 0; k4 < RH / 4; ++k4) {
+              const float4 m4 = *reinterpret_cast<const float4*>(mrow + 4 * k4);
+              x[4 * k4] = fmaf(__uint_as_float(sv[4 * k4]), scale_log2, -m4.x);
+              x[4 * k4 + 1] = fmaf(__uint_as_float(sv[4 * k4 + 1]), scale_log2, -m4.y);
+              x[4 * k4 + 2] = fmaf(__uint_as_float(sv[4 * k4 + 2]), scale_log2, -m4.z);
+              x[4 * k4 + 3] = fmaf(__uint_as_float(sv[4 * k4 + 3]), scale_log2, -m4.w);
+            }
+#pragma unroll
+            for (int k = 0; k < RH; ++k) x[k] = ((vis >> k) & 1ull) ? x[k] : kNegInf;
+          }
         }
 
         PKV_TL_STEP(5);
@@ -821,7 +860,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           uint32_t pw[4];
 #pragma unroll
           for (int k4 = 0; k4 < RH / 4; ++k4) {
-            const float4 m4 = *reinterpret_cast<const float4*>(mrow + 4 * k4);
+            float4 m4 = make_float4(0.f, 0.f, 0.f, 0.f);   // x already less the max
+            if constexpr (!kFusedMax) m4 = *reinterpret_cast<const float4*>(mrow + 4 * k4);
             const __half2 p01 = __floats2half2_rn(fast_exp2(x[4 * k4] - m4.x), fast_exp2(x[4 * k4 + 1] - m4.y));
             const __half2 p23 = __floats2half2_rn(fast_exp2(x[4 * k4 + 2] - m4.z), fast_exp2(x[4 * k4 + 3] - m4.w));
             // The sums add exactly the fp16 values the P V product uses.
