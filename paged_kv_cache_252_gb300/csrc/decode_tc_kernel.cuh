@@ -380,21 +380,37 @@ __device__ __forceinline__ void tc_piece_output(const DecodeArgs& a, uint32_t t_
   const int G = a.group, Hq = a.num_q_heads;
   tc_fence_after_sync();
   const int r_end = r0 + RH < pc.Rs ? r0 + RH : pc.Rs;
+  // Four columns per TMEM load (RH and r0 are multiples of 4; r_end is the same for
+  // the whole warp, so every lane takes part in every load).
   if (!pc.split) {
     int j = r0 / G, gi = r0 - j * G;
     uint16_t* dst = static_cast<uint16_t*>(a.out) + (static_cast<size_t>(pc.qb + j) * Hq + h * G + gi) * D + t;
 #pragma unroll 1
-    for (int r = r0; r < r_end; ++r) {
-      const float o = __uint_as_float(tmem_ld1(t_cols + kTcOCol + (r - r0)));
-      *dst = __half_as_ushort(__float2half_rn(o * row_inv[r]));
-      // next row: next head of the group, or the first head for the next query token
-      dst += (++gi == G) ? static_cast<ptrdiff_t>(Hq - G + 1) * D : D;
-      if (gi == G) gi = 0;
+    for (int r4 = r0; r4 < r_end; r4 += 4) {
+      uint32_t ov[4];
+      tmem_ld4(t_cols + kTcOCol + (r4 - r0), ov);
+      const float4 inv = *reinterpret_cast<const float4*>(row_inv + r4);
+      const float iv[4] = {inv.x, inv.y, inv.z, inv.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (r4 + e < r_end) {
+          *dst = __half_as_ushort(__float2half_rn(__uint_as_float(ov[e]) * iv[e]));
+          // next row: next head of the group, or the first head for the next query token
+          dst += (++gi == G) ? static_cast<ptrdiff_t>(Hq - G + 1) * D : D;
+          if (gi == G) gi = 0;
+        }
+      }
     }
   } else {
     float* slot = a.partials + static_cast<size_t>(pc.u + cta) * a.slot_floats + partial_o_offset(a.rows) + t;
 #pragma unroll 1
-    for (int r = r0; r < r_end; ++r) slot[r * D] = __uint_as_float(tmem_ld1(t_cols + kTcOCol + (r - r0)));
+    for (int r4 = r0; r4 < r_end; r4 += 4) {
+      uint32_t ov[4];
+      tmem_ld4(t_cols + kTcOCol + (r4 - r0), ov);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (r4 + e < r_end) slot[(r4 + e) * D] = __uint_as_float(ov[e]);
+    }
   }
 }
 
